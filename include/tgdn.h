@@ -1,0 +1,198 @@
+/*
+ * tgdn.h — C ABI of the rollback-free GDN tree-verification library (libtgdn.so).
+ *
+ * One decode step of tree speculative decoding on a hybrid model with Gated
+ * DeltaNet (GDN) layers, as described in "Trees from Marginals: Autoregressive
+ * drafting with factorized priors" (Technisches Resümee, Methodik 3,
+ * "Rollback-freie Baumverifizierung für GDN"):
+ *
+ *   tgdn_tree_prep  sort the draft tree topologically and build its ancestor
+ *                   relation (Methodik 3: "Der Baum wird topologisch sortiert").
+ *   tgdn_verify     every node's output from the committed state S0 in one
+ *                   pass: Gram tiles, a masked triangular solve (I + X) U = R
+ *                   and the output phase, without updating the state
+ *                   (Methodik 3: interaction matrices X and Y; the system
+ *                   (I+X)U = beta V; Implementierung: Gram matrix, tiled
+ *                   forward substitution, output phase).
+ *   tgdn_accept     greedy acceptance: the longest root path whose draft
+ *                   tokens all equal the verifier's tokens (mean acceptance
+ *                   length, Experimentelle Ergebnisse).
+ *   tgdn_commit     the accepted node's state, written from the same factors
+ *                   U once the accepted branch is known; no rollback and no
+ *                   replay (Methodik 3, deferred state commitment).
+ *
+ * The recurrence is the GDN update eq. (Methodik 3, "Herausforderung"):
+ *   S_n = a_n (I - b_n k_n k_n^T) S_parent(n) + b_n k_n v_n^T,  a_n = exp(g_n),
+ * with S a d_k x d_v matrix stored row-major (row = key index), and the output
+ * of node n is o_n = S_n^T q_n.  The root of each tree is a real token whose
+ * parent state is S0.  q and k are used exactly as given (no normalisation,
+ * no 1/sqrt(d) scaling).  v-head h reads query/key head h / (H_v / H_qk).
+ *
+ * Conventions for every call:
+ *   - All array pointers are DEVICE pointers unless stated otherwise.  The
+ *     caller owns and allocates every buffer, workspace included; the library
+ *     never allocates device memory and keeps no state between calls.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream) and returns after enqueueing its kernels.
+ *   - Host-side argument checks run before any launch and return a negative
+ *     tgdn_status; nothing is enqueued in that case.  Errors that only the
+ *     device can see (a malformed tree, an expired bounded wait) are written
+ *     to the per-sequence status word and never trap.
+ *   - Row ranges: sequence b owns node rows cu_nodes[b] .. cu_nodes[b+1]-1 of
+ *     every [T]-leading array; parent[] holds LOCAL indices (0 .. N_b-1,
+ *     -1 for the root).
+ */
+#ifndef TGDN_H_
+#define TGDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* An opaque CUDA stream handle, layout-compatible with cudaStream_t. */
+typedef struct CUstream_st* tgdn_stream_t;
+
+/* Return codes of every call. */
+typedef enum {
+  TGDN_OK = 0,
+  TGDN_EINVAL = -1,       /* null pointer, negative size, inconsistent dims */
+  TGDN_ETOOBIG = -3,      /* a bound above the library's limits (see below) */
+  TGDN_ECUDA = -4,        /* a CUDA launch or driver call failed */
+  TGDN_EUNSUPPORTED = -5  /* a valid combination this build does not run */
+} tgdn_status;
+
+/* Per-sequence status words written by tgdn_tree_prep (values 1-5) and by
+ * the other calls (value 6).  The first failing check, in this order, wins. */
+typedef enum {
+  TGDN_SEQ_OK = 0,
+  TGDN_SEQ_TOO_BIG = 1,     /* N_b > n_max */
+  TGDN_SEQ_BAD_PARENT = 2,  /* some parent < -1, >= N_b, or equal to the node */
+  TGDN_SEQ_ROOTS = 3,       /* N_b > 0 and not exactly one root */
+  TGDN_SEQ_CYCLE = 4,       /* some node never reaches the root */
+  TGDN_SEQ_TOO_DEEP = 5,    /* some depth > depth_max */
+  TGDN_SEQ_TIMEOUT = 6      /* a bounded device wait expired; outputs of the
+                               sequence are unspecified */
+} tgdn_seq_status;
+
+/* Element type of q, k, v and o.  g, b, S0, the state and the workspace are
+ * always fp32. */
+typedef enum { TGDN_F32 = 0, TGDN_BF16 = 1 } tgdn_dtype;
+
+/* Library limits. */
+#define TGDN_MAX_NODES 256  /* n_max bound: nodes per tree, root included */
+#define TGDN_MAX_DEPTH 64   /* depth_max bound: edges on the longest root path */
+#define TGDN_MAX_HEAD_DIM 128
+
+/* A batch of draft trees and the metadata tgdn_tree_prep derives from it.
+ *   B          number of sequences (>= 0)
+ *   T          total nodes, = cu_nodes[B] (host copy, used for bounds only)
+ *   n_max      caller's bound on nodes per sequence, 1 .. TGDN_MAX_NODES
+ *   depth_max  caller's bound on depth, 0 .. TGDN_MAX_DEPTH
+ *   words      64-bit words per ancestor mask, must equal ceil(n_max / 64)
+ *   cu_nodes   [B+1] int32, non-decreasing row offsets, cu_nodes[0] = 0
+ *   parent     [T] int32, local parent index, -1 for the root
+ * Written by tgdn_tree_prep, read by the other calls:
+ *   depth      [T] int32, edges from the node to the root
+ *   order      [T] int32, order[cu_nodes[b] + p] = local index of the node at
+ *              topological position p (stable sort by (depth, index))
+ *   pos        [T] int32, inverse of order: pos[cu_nodes[b] + n] = p
+ *   anc        [T][words] uint64, row cu_nodes[b] + pos(n) has bit pos(s) set
+ *              for every s on the root path of n, n included
+ *   status     [B] int32, tgdn_seq_status
+ * For a sequence whose status is not TGDN_SEQ_OK, depth/order/pos are -1 and
+ * anc rows are 0. */
+typedef struct {
+  int32_t B, T, n_max, depth_max, words;
+  const int32_t* cu_nodes;
+  const int32_t* parent;
+  int32_t* depth;
+  int32_t* order;
+  int32_t* pos;
+  uint64_t* anc;
+  int32_t* status;
+} tgdn_tree;
+
+/* Head geometry of one GDN layer.  H_v must be a multiple of H_qk;
+ * 1 <= d_k, d_v <= TGDN_MAX_HEAD_DIM; io is a tgdn_dtype. */
+typedef struct {
+  int32_t H_qk, H_v, d_k, d_v;
+  int32_t io;
+} tgdn_dims;
+
+/* Topological sort and ancestor masks for every sequence (Methodik 3: "Der
+ * Baum wird topologisch sortiert"; ancestor relations behind X and Y).
+ * Validates each tree and writes depth, order, pos, anc and status.
+ * Returns TGDN_OK, TGDN_EINVAL (null pointer, B < 0, words mismatch) or
+ * TGDN_ETOOBIG (n_max or depth_max above the limits). */
+int tgdn_tree_prep(const tgdn_tree* tree, tgdn_stream_t stream);
+
+/* Bytes of the workspace tgdn_verify writes and tgdn_commit reads for this
+ * tree and geometry: the factors U [T][H_v][d_v] fp32 followed, at the next
+ * 256-byte boundary, by the path-cumulative log-gates G [T][H_v] fp32.
+ * Returns 0 for invalid arguments. */
+size_t tgdn_verify_workspace_bytes(const tgdn_tree* tree, const tgdn_dims* dims);
+
+/* Single-pass verification of every node (Methodik 3 and Implementierung:
+ * Gram matrix, tiled forward substitution, output phase).  With
+ * G_n = sum of g over the root path of n (n included):
+ *   X_ns = b_n exp(G_n - G_s) k_n.k_s   for s a strict ancestor of n,
+ *   Y_ns =     exp(G_n - G_s) q_n.k_s   for s an ancestor of n or n itself,
+ *   (I + X) U = diag(b) (V - diag(exp(G)) K S0)         (one row per node),
+ *   O = diag(exp(G)) Q S0 + Y U,
+ * which equals replaying the recurrence along every root path.
+ *   q, k  [T][H_qk][d_k]   io dtype
+ *   v     [T][H_v][d_v]    io dtype
+ *   g, b  [T][H_v]         fp32; g is the log-gate (<= 0), b the write strength
+ *   S0    [B][H_v][d_k][d_v] fp32, read only
+ *   o     [T][H_v][d_v]    io dtype, written
+ *   ws    tgdn_verify_workspace_bytes() bytes, 256-byte aligned, written
+ * tgdn_tree_prep must have run on `tree` (same stream or ordered before).
+ * A sequence with a bad status gets zero outputs and zero workspace rows.
+ * bf16 io with d_k = d_v = 128 runs the tensor-core kernel when
+ * n_max <= 64 and depth_max <= 32; every other valid case runs the fp32 SIMT
+ * kernel.  Returns TGDN_OK, TGDN_EINVAL, TGDN_ETOOBIG or TGDN_ECUDA. */
+int tgdn_verify(const tgdn_tree* tree, const tgdn_dims* dims, const void* q, const void* k,
+                const void* v, const float* g, const float* b, const float* S0, void* o,
+                void* ws, tgdn_stream_t stream);
+
+/* Greedy acceptance (Experimentelle Ergebnisse, mean acceptance length).  The
+ * root is always accepted; a non-root node is accepted when it and every
+ * non-root node on its root path satisfy target_ids == draft_ids.  The
+ * accepted node is the deepest accepted node, ties going to the smallest
+ * topological position.
+ *   draft_ids, target_ids [T] int32 (target_ids[n]: the verifier's token for
+ *                                     node n's position)
+ *   accept_node [B] int32: local index, -1 for an empty or invalid tree
+ *   accept_len  [B] int32: depth + 1 (root counted), 0 if none
+ *   path        [B][depth_max + 1] int32: local indices root first, -1 padded
+ * Returns TGDN_OK, TGDN_EINVAL or TGDN_ECUDA. */
+int tgdn_accept(const tgdn_tree* tree, const int32_t* draft_ids, const int32_t* target_ids,
+                int32_t* accept_node, int32_t* accept_len, int32_t* path,
+                tgdn_stream_t stream);
+
+/* Deferred, rollback-free state commitment (Methodik 3, last bullet): with
+ * n* = accept_node[b] and P its root path,
+ *   S_out = exp(G_n*) S_in + sum_{s in P} exp(G_n* - G_s) k_s u_s^T
+ * using the U and G that tgdn_verify left in `ws` for the same tree and the
+ * same S_in.  S_in, S_out [B][H_v][d_k][d_v] fp32; S_out may equal S_in (in
+ * place); otherwise the two must not overlap.  Sequences with n* < 0 or a
+ * bad status keep S_in.  k is the same [T][H_qk][d_k] tensor given to verify.
+ * Returns TGDN_OK, TGDN_EINVAL or TGDN_ECUDA. */
+int tgdn_commit(const tgdn_tree* tree, const tgdn_dims* dims, const int32_t* accept_node,
+                const void* k, const void* ws, const float* S_in, float* S_out,
+                tgdn_stream_t stream);
+
+/* Static, human-readable text for a tgdn_status value. */
+const char* tgdn_status_string(int code);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int tgdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TGDN_H_ */

@@ -1,0 +1,154 @@
+// tgdn_api.cu — the C ABI (include/tgdn.h): host-side argument checks,
+// kernel selection and TMA descriptor encoding.  No call allocates memory.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "tgdn_device.cuh"
+#include "tgdn_kernels.h"
+
+namespace {
+
+using tgdn::WsLayout;
+
+int check_tree(const tgdn_tree* t) {
+  if (!t) return TGDN_EINVAL;
+  if (t->B < 0 || t->T < 0 || t->n_max < 1 || t->depth_max < 0) return TGDN_EINVAL;
+  if (t->n_max > TGDN_MAX_NODES || t->depth_max > TGDN_MAX_DEPTH) return TGDN_ETOOBIG;
+  if (t->words != (t->n_max + 63) / 64) return TGDN_EINVAL;
+  if (t->B > 0 && (!t->cu_nodes || !t->status)) return TGDN_EINVAL;
+  if (t->T > 0 && (!t->parent || !t->depth || !t->order || !t->pos || !t->anc))
+    return TGDN_EINVAL;
+  return TGDN_OK;
+}
+
+int check_dims(const tgdn_dims* d) {
+  if (!d) return TGDN_EINVAL;
+  if (d->H_qk < 1 || d->H_v < 1 || d->H_v % d->H_qk != 0) return TGDN_EINVAL;
+  if (d->d_k < 1 || d->d_v < 1) return TGDN_EINVAL;
+  if (d->d_k > TGDN_MAX_HEAD_DIM || d->d_v > TGDN_MAX_HEAD_DIM) return TGDN_ETOOBIG;
+  if (d->io != TGDN_F32 && d->io != TGDN_BF16) return TGDN_EINVAL;
+  return TGDN_OK;
+}
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? TGDN_OK : TGDN_ECUDA; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// q or k [T][H_qk][128] bf16 as a 3-D tensor; box = 64 elements x 1 head x 64 rows,
+// 128-byte swizzle (the tcgen05 K-major SWIZZLE_128B operand layout).
+bool encode_qk_map(CUtensorMap* map, const void* base, int T, int H_qk) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {128, (cuuint64_t)H_qk, (cuuint64_t)T};
+  const cuuint64_t strides[2] = {128 * 2, (cuuint64_t)H_qk * 128 * 2};
+  const cuuint32_t box[3] = {64, 1, 64};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+int tgdn_version(void) { return 100; }
+
+const char* tgdn_status_string(int code) {
+  switch (code) {
+    case TGDN_OK: return "ok";
+    case TGDN_EINVAL: return "invalid argument";
+    case TGDN_ETOOBIG: return "size above the library limits";
+    case TGDN_ECUDA: return "CUDA launch or driver error";
+    case TGDN_EUNSUPPORTED: return "unsupported configuration";
+    default: return "unknown status";
+  }
+}
+
+int tgdn_tree_prep(const tgdn_tree* tree, tgdn_stream_t stream) {
+  int rc = check_tree(tree);
+  if (rc != TGDN_OK) return rc;
+  return from_cuda(tgdn::launch_tree_prep(*tree, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t tgdn_verify_workspace_bytes(const tgdn_tree* tree, const tgdn_dims* dims) {
+  if (check_tree(tree) != TGDN_OK || check_dims(dims) != TGDN_OK) return 0;
+  return tgdn::ws_layout(*tree, *dims).bytes;
+}
+
+int tgdn_verify(const tgdn_tree* tree, const tgdn_dims* dims, const void* q, const void* k,
+                const void* v, const float* g, const float* b, const float* S0, void* o,
+                void* ws, tgdn_stream_t stream) {
+  int rc = check_tree(tree);
+  if (rc != TGDN_OK) return rc;
+  rc = check_dims(dims);
+  if (rc != TGDN_OK) return rc;
+  const tgdn_tree& t = *tree;
+  const tgdn_dims& d = *dims;
+  if (t.T > 0 && (!q || !k || !v || !g || !b || !o || !ws)) return TGDN_EINVAL;
+  if (t.B > 0 && !S0) return TGDN_EINVAL;
+  if (reinterpret_cast<uintptr_t>(ws) % 256 != 0) return TGDN_EINVAL;
+  if (t.B == 0 || t.T == 0) return TGDN_OK;
+  const WsLayout L = tgdn::ws_layout(t, d);
+  float* U = reinterpret_cast<float*>(static_cast<char*>(ws) + L.u_off);
+  float* G = reinterpret_cast<float*>(static_cast<char*>(ws) + L.g_off);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (tgdn::verify_tc_supported(t, d, q, k, v, S0, o)) {
+    CUtensorMap qmap, kmap;
+    if (!encode_qk_map(&qmap, q, t.T, d.H_qk) || !encode_qk_map(&kmap, k, t.T, d.H_qk))
+      return TGDN_ECUDA;  // the driver could not describe q/k for TMA
+    return from_cuda(tgdn::launch_verify_tc(t, d, qmap, kmap, v, g, b, S0, o, U, G, s));
+  }
+  return from_cuda(tgdn::launch_verify_simt(t, d, q, k, v, g, b, S0, o, U, G, s));
+}
+
+int tgdn_accept(const tgdn_tree* tree, const int32_t* draft_ids, const int32_t* target_ids,
+                int32_t* accept_node, int32_t* accept_len, int32_t* path,
+                tgdn_stream_t stream) {
+  int rc = check_tree(tree);
+  if (rc != TGDN_OK) return rc;
+  if (tree->B > 0 && (!accept_node || !accept_len || !path)) return TGDN_EINVAL;
+  if (tree->T > 0 && (!draft_ids || !target_ids)) return TGDN_EINVAL;
+  return from_cuda(tgdn::launch_accept(*tree, draft_ids, target_ids, accept_node, accept_len,
+                                       path, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int tgdn_commit(const tgdn_tree* tree, const tgdn_dims* dims, const int32_t* accept_node,
+                const void* k, const void* ws, const float* S_in, float* S_out,
+                tgdn_stream_t stream) {
+  int rc = check_tree(tree);
+  if (rc != TGDN_OK) return rc;
+  rc = check_dims(dims);
+  if (rc != TGDN_OK) return rc;
+  const tgdn_tree& t = *tree;
+  const tgdn_dims& d = *dims;
+  if (t.B > 0 && (!accept_node || !S_in || !S_out)) return TGDN_EINVAL;
+  if (t.T > 0 && (!k || !ws)) return TGDN_EINVAL;
+  if (t.B == 0) return TGDN_OK;
+  if (S_in != S_out) {  // distinct buffers must not overlap
+    const size_t bytes = (size_t)t.B * d.H_v * d.d_k * d.d_v * sizeof(float);
+    const char* a = reinterpret_cast<const char*>(S_in);
+    const char* c = reinterpret_cast<const char*>(S_out);
+    if (a < c + bytes && c < a + bytes) return TGDN_EINVAL;
+  }
+  const WsLayout L = tgdn::ws_layout(t, d);
+  const float* U = reinterpret_cast<const float*>(static_cast<const char*>(ws) + L.u_off);
+  const float* G = reinterpret_cast<const float*>(static_cast<const char*>(ws) + L.g_off);
+  return from_cuda(tgdn::launch_commit(t, d, accept_node, k, U, G, S_in, S_out,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

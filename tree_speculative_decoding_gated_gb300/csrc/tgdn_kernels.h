@@ -1,0 +1,48 @@
+// tgdn_kernels.h — internal launchers behind the C ABI (not part of the ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/tgdn.h"
+
+namespace tgdn {
+
+// Workspace layout shared by verify (writer) and commit (reader).
+struct WsLayout {
+  size_t u_off, g_off, bytes;
+};
+inline WsLayout ws_layout(const tgdn_tree& t, const tgdn_dims& d) {
+  WsLayout w;
+  w.u_off = 0;
+  const size_t u_bytes = (size_t)t.T * d.H_v * d.d_v * sizeof(float);
+  w.g_off = (u_bytes + 255) / 256 * 256;
+  w.bytes = w.g_off + (size_t)t.T * d.H_v * sizeof(float);
+  return w;
+}
+
+cudaError_t launch_tree_prep(const tgdn_tree& t, cudaStream_t s);
+cudaError_t launch_accept(const tgdn_tree& t, const int32_t* draft, const int32_t* target,
+                          int32_t* accept_node, int32_t* accept_len, int32_t* path,
+                          cudaStream_t s);
+
+// fp32 SIMT verify: any valid geometry (d_k, d_v <= 128, n_max <= 256, depth_max <= 64).
+cudaError_t launch_verify_simt(const tgdn_tree& t, const tgdn_dims& d, const void* q,
+                               const void* k, const void* v, const float* g, const float* b,
+                               const float* S0, void* o, float* U, float* G, cudaStream_t s);
+
+// Tensor-core verify: bf16 io, d_k = d_v = 128, n_max <= 64, depth_max <= 32.
+bool verify_tc_supported(const tgdn_tree& t, const tgdn_dims& d, const void* q, const void* k,
+                         const void* v, const float* S0, const void* o);
+cudaError_t launch_verify_tc(const tgdn_tree& t, const tgdn_dims& d, const CUtensorMap& qmap,
+                             const CUtensorMap& kmap, const void* v, const float* g,
+                             const float* b, const float* S0, void* o, float* U, float* G,
+                             cudaStream_t s);
+
+cudaError_t launch_commit(const tgdn_tree& t, const tgdn_dims& d, const int32_t* accept_node,
+                          const void* k, const float* U, const float* G, const float* S_in,
+                          float* S_out, cudaStream_t s);
+
+}  // namespace tgdn

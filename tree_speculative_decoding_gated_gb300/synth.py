@@ -1,6 +1,6 @@
 """Seeded synthetic inputs for rollback-free GDN tree verification.
 
-This module is shared by the tests, the benchmark and the oracle harness.  It
+This module is shared by the tests and the benchmark.  It
 holds none of the method's arithmetic: it only draws trees, token ids and the
 per-node q/k/v/gate/beta tensors plus the committed state S0, with the shapes
 and distributions of the workloads studied on the pages of "Trees from

@@ -1,0 +1,217 @@
+"""Thin Python binding of libtgdn.so (include/tgdn.h) — argument marshalling only.
+
+Every step of the path runs in the library's CUDA kernels; this module only
+checks that the torch tensors it is handed live on the GPU with the dtype,
+layout and size the C ABI expects (a host pointer handed to a kernel would
+fault the device), packs the C structs and raises on a non-zero status.  There
+is no fallback: if the library has not been built this module fails to load.
+
+Names follow the C ABI: tree_prep, verify_workspace_bytes, verify, accept,
+commit.  All calls are asynchronous on the given stream (default: torch's
+current stream).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtgdn.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "tgdn.h")
+
+OK, EINVAL, ETOOBIG, ECUDA, EUNSUPPORTED = 0, -1, -3, -4, -5
+SEQ_OK, SEQ_TOO_BIG, SEQ_BAD_PARENT, SEQ_ROOTS, SEQ_CYCLE, SEQ_TOO_DEEP, SEQ_TIMEOUT = range(7)
+F32, BF16 = 0, 1
+MAX_NODES, MAX_DEPTH, MAX_HEAD_DIM = 256, 64, 128
+
+
+class TgdnError(RuntimeError):
+    def __init__(self, code: int, call: str):
+        self.code = code
+        super().__init__(f"{call}: {status_string(code)} ({code})")
+
+
+class CTree(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("n_max", ctypes.c_int32),
+                ("depth_max", ctypes.c_int32), ("words", ctypes.c_int32),
+                ("cu_nodes", ctypes.c_void_p), ("parent", ctypes.c_void_p),
+                ("depth", ctypes.c_void_p), ("order", ctypes.c_void_p), ("pos", ctypes.c_void_p),
+                ("anc", ctypes.c_void_p), ("status", ctypes.c_void_p)]
+
+
+class CDims(ctypes.Structure):
+    _fields_ = [("H_qk", ctypes.c_int32), ("H_v", ctypes.c_int32), ("d_k", ctypes.c_int32),
+                ("d_v", ctypes.c_int32), ("io", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libtgdn.so; raises if it has not been built (there is no other path)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, st = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p
+        P = ctypes.POINTER
+        L.tgdn_tree_prep.argtypes = [P(CTree), st]
+        L.tgdn_verify_workspace_bytes.argtypes = [P(CTree), P(CDims)]
+        L.tgdn_verify_workspace_bytes.restype = ctypes.c_size_t
+        L.tgdn_verify.argtypes = [P(CTree), P(CDims), vp, vp, vp, vp, vp, vp, vp, vp, st]
+        L.tgdn_accept.argtypes = [P(CTree), vp, vp, vp, vp, vp, st]
+        L.tgdn_commit.argtypes = [P(CTree), P(CDims), vp, vp, vp, vp, vp, st]
+        L.tgdn_status_string.argtypes = [i32]
+        L.tgdn_status_string.restype = ctypes.c_char_p
+        L.tgdn_version.argtypes = []
+        for f in (L.tgdn_tree_prep, L.tgdn_verify, L.tgdn_accept, L.tgdn_commit, L.tgdn_version):
+            f.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/tgdn.h declares."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(tgdn_\w+)\s*\(", text, re.M)))
+
+
+def status_string(code: int) -> str:
+    return lib().tgdn_status_string(int(code)).decode()
+
+
+def _check(rc: int, call: str):
+    if rc != OK:
+        raise TgdnError(rc, call)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dev(t: torch.Tensor, dtype, numel: int, name: str) -> int:
+    """Device pointer of a contiguous CUDA tensor holding at least `numel` elements."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor (the library takes device pointers)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if t.numel() < numel:
+        raise ValueError(f"{name}: {t.numel()} elements, need {numel}")
+    return t.data_ptr() if numel > 0 else (t.data_ptr() or None)
+
+
+@dataclass
+class Dims:
+    H_qk: int
+    H_v: int
+    d_k: int
+    d_v: int
+    io: int = BF16
+
+    def c(self) -> CDims:
+        return CDims(self.H_qk, self.H_v, self.d_k, self.d_v, self.io)
+
+    @property
+    def torch_dtype(self):
+        return torch.bfloat16 if self.io == BF16 else torch.float32
+
+
+class Tree:
+    """A batch of draft trees on the device plus the metadata tree_prep writes."""
+
+    def __init__(self, cu_nodes: torch.Tensor, parent: torch.Tensor, n_max: int,
+                 depth_max: int, T: int | None = None):
+        self.B = int(cu_nodes.numel()) - 1
+        self.T = int(parent.numel()) if T is None else int(T)
+        self.n_max, self.depth_max = int(n_max), int(depth_max)
+        self.words = max(1, (self.n_max + 63) // 64)
+        dev = cu_nodes.device
+        self.cu_nodes, self.parent = cu_nodes, parent
+        self.depth = torch.empty(self.T, dtype=torch.int32, device=dev)
+        self.order = torch.empty(self.T, dtype=torch.int32, device=dev)
+        self.pos = torch.empty(self.T, dtype=torch.int32, device=dev)
+        self.anc = torch.empty((self.T, self.words), dtype=torch.int64, device=dev)
+        self.status = torch.empty(max(self.B, 0), dtype=torch.int32, device=dev)
+
+    @classmethod
+    def from_host(cls, cu_nodes, parent, n_max: int, depth_max: int, device="cuda"):
+        cu = torch.as_tensor(cu_nodes, dtype=torch.int32).to(device)
+        par = torch.as_tensor(parent, dtype=torch.int32).to(device)
+        return cls(cu, par, n_max, depth_max)
+
+    def c(self) -> CTree:
+        B, T = self.B, self.T
+        return CTree(B, T, self.n_max, self.depth_max, self.words,
+                     _dev(self.cu_nodes, torch.int32, B + 1, "cu_nodes"),
+                     _dev(self.parent, torch.int32, T, "parent"),
+                     _dev(self.depth, torch.int32, T, "depth"),
+                     _dev(self.order, torch.int32, T, "order"),
+                     _dev(self.pos, torch.int32, T, "pos"),
+                     _dev(self.anc, torch.int64, T * self.words, "anc"),
+                     _dev(self.status, torch.int32, B, "status"))
+
+
+def tree_prep(tree: Tree, stream=None) -> None:
+    ct = tree.c()
+    _check(lib().tgdn_tree_prep(ctypes.byref(ct), _stream(stream)), "tgdn_tree_prep")
+
+
+def verify_workspace_bytes(tree: Tree, dims: Dims) -> int:
+    ct, cd = tree.c(), dims.c()
+    return int(lib().tgdn_verify_workspace_bytes(ctypes.byref(ct), ctypes.byref(cd)))
+
+
+def alloc_workspace(tree: Tree, dims: Dims, device="cuda") -> torch.Tensor:
+    n = verify_workspace_bytes(tree, dims)
+    if n == 0 and tree.T > 0:
+        raise TgdnError(EINVAL, "tgdn_verify_workspace_bytes")
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def verify(tree: Tree, dims: Dims, q, k, v, g, b, S0, o, ws, stream=None) -> None:
+    T, B = tree.T, tree.B
+    io = dims.torch_dtype
+    ct, cd = tree.c(), dims.c()
+    args = (_dev(q, io, T * dims.H_qk * dims.d_k, "q"), _dev(k, io, T * dims.H_qk * dims.d_k, "k"),
+            _dev(v, io, T * dims.H_v * dims.d_v, "v"), _dev(g, torch.float32, T * dims.H_v, "g"),
+            _dev(b, torch.float32, T * dims.H_v, "b"),
+            _dev(S0, torch.float32, B * dims.H_v * dims.d_k * dims.d_v, "S0"),
+            _dev(o, io, T * dims.H_v * dims.d_v, "o"),
+            _dev(ws, torch.uint8, verify_workspace_bytes(tree, dims), "ws"))
+    _check(lib().tgdn_verify(ctypes.byref(ct), ctypes.byref(cd), *args, _stream(stream)),
+           "tgdn_verify")
+
+
+def accept(tree: Tree, draft_ids, target_ids, accept_node, accept_len, path, stream=None) -> None:
+    T, B = tree.T, tree.B
+    ct = tree.c()
+    args = (_dev(draft_ids, torch.int32, T, "draft_ids"),
+            _dev(target_ids, torch.int32, T, "target_ids"),
+            _dev(accept_node, torch.int32, B, "accept_node"),
+            _dev(accept_len, torch.int32, B, "accept_len"),
+            _dev(path, torch.int32, B * (tree.depth_max + 1), "path"))
+    _check(lib().tgdn_accept(ctypes.byref(ct), *args, _stream(stream)), "tgdn_accept")
+
+
+def commit(tree: Tree, dims: Dims, accept_node, k, ws, S_in, S_out, stream=None) -> None:
+    T, B = tree.T, tree.B
+    ct, cd = tree.c(), dims.c()
+    ns = B * dims.H_v * dims.d_k * dims.d_v
+    args = (_dev(accept_node, torch.int32, B, "accept_node"),
+            _dev(k, dims.torch_dtype, T * dims.H_qk * dims.d_k, "k"),
+            _dev(ws, torch.uint8, verify_workspace_bytes(tree, dims), "ws"),
+            _dev(S_in, torch.float32, ns, "S_in"), _dev(S_out, torch.float32, ns, "S_out"))
+    _check(lib().tgdn_commit(ctypes.byref(ct), ctypes.byref(cd), *args, _stream(stream)),
+           "tgdn_commit")
