@@ -1,0 +1,437 @@
+"""Benchmark: verified tree nodes/s per GDN layer on one GB300 (or N, weak scaling).
+
+Workload (default): the 36-layer stack — 32 sequences per GPU, each a 64-node
+random draft tree of depth <= 12, H_qk = 16, H_v = 32, d_k = d_v = 128, bf16
+q/k/v, fp32 states (one per layer and v-head).  One step is one decode
+iteration through the library's C ABI:
+    tgdn_tree_prep -> 36 x tgdn_verify -> tgdn_accept -> 36 x tgdn_commit (in place)
+captured once per distinct step input into a CUDA graph and replayed.
+Inputs are seeded synthetic data resident in HBM; a step touches ~9 GB, far
+more than the 129 MB L2, so no flush is needed between steps.
+
+value  = 36 * B * N_nodes * steps * world / max-over-ranks elapsed time
+         (the rate at which one layer's worth of tree nodes is verified).
+e2e    = the same metric with the step's inputs copied from pinned host memory
+         to the device and the accepted paths copied back, inside the timed
+         region, every step.
+roofline: the dominant kernel's algorithmic bytes per launch over its
+         CUDA-event duration, against the measured HBM copy bandwidth.
+
+--impl reference times the fp64 CPU oracle (path replay, all host cores) on a
+bounded sample of the same workload, in the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from tree_speculative_decoding_gated_gb300 import synth  # noqa: E402
+
+CONFIG = "cfg5"
+METRIC = "verified tree nodes/sec per GDN layer (1 GB300); achieved HBM GB/s % of peak"
+UNIT = "nodes/s/layer"
+S0_BYTES_PER_SEQ = 32 * 128 * 128 * 4                     # one layer's state of one sequence
+NODE_BYTES = 2 * 16 * 128 * 2 + 32 * 128 * 2 + 2 * 32 * 4 + 32 * 128 * 2   # q,k,v,g,b in + o out
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="tgdn", choices=["tgdn", "reference"])
+    ap.add_argument("--inputs", type=int, default=2, help="distinct step inputs cycled through")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-seqs", type=int, default=4)
+    ap.add_argument("--layers", type=int, default=36,
+                    help="GDN layers per step (fewer only for small profiler captures)")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"tgdn_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names[1:], parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+class StepInput:
+    """One decode step's inputs for all layers, resident on the device."""
+
+    def __init__(self, cfg, step, layers, gen, device, tgdn, torch):
+        trees = synth.make_trees(cfg, step)
+        draft, target = synth.make_ids(cfg, trees, step)
+        self.host_tree = trees
+        self.tree = tgdn.Tree.from_host(trees.cu_nodes, trees.parent, trees.n_max,
+                                        trees.depth_max, device)
+        self.draft = torch.from_numpy(draft).to(device)
+        self.target = torch.from_numpy(target).to(device)
+        T = trees.T
+        self.q, self.k, self.v, self.g, self.b = [], [], [], [], []
+        for _ in range(layers):
+            q, k, v, g, b = synth.make_node_inputs_device(cfg, T, gen, device)
+            self.q.append(q)
+            self.k.append(k)
+            self.v.append(v)
+            self.g.append(g)
+            self.b.append(b)
+
+    def tensors(self):
+        return [self.tree.cu_nodes, self.tree.parent, self.draft, self.target,
+                *self.q, *self.k, *self.v, *self.g, *self.b]
+
+
+def run_gpu(args, rank, world, local):
+    import torch
+    from tree_speculative_decoding_gated_gb300 import tgdn
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    cfg = synth.CONFIGS[CONFIG]
+    L, B, Nn = args.layers, cfg.B, cfg.n_nodes
+    dims = tgdn.Dims(cfg.H_qk, cfg.H_v, cfg.dk, cfg.dv, tgdn.BF16)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(synth.BASE_SEED + cfg.number + 1000 + 7919 * rank)
+
+    R = max(1, args.inputs)
+    inputs = [StepInput(cfg, r + R * rank, L, gen, device, tgdn, torch) for r in range(R)]
+    states = [synth.make_state_device(cfg, B, gen, device) for _ in range(L)]
+    T = inputs[0].tree.T
+    ws_bytes = tgdn.verify_workspace_bytes(inputs[0].tree, dims)
+    ws = [torch.empty(ws_bytes, dtype=torch.uint8, device=device) for _ in range(L)]
+    outs = [torch.empty((T, cfg.H_v, cfg.dv), dtype=torch.bfloat16, device=device)
+            for _ in range(L)]
+    an = torch.empty(B, dtype=torch.int32, device=device)
+    al = torch.empty(B, dtype=torch.int32, device=device)
+    path = torch.empty((B, cfg.depth_max + 1), dtype=torch.int32, device=device)
+
+    stream = torch.cuda.Stream(device)
+    ev = {"v0": [torch.cuda.Event(enable_timing=True) for _ in range(L)],
+          "v1": [torch.cuda.Event(enable_timing=True) for _ in range(L)],
+          "c0": [torch.cuda.Event(enable_timing=True) for _ in range(L)],
+          "c1": [torch.cuda.Event(enable_timing=True) for _ in range(L)]}
+
+    def step(inp: StepInput, timed_kernels=False):
+        tgdn.tree_prep(inp.tree, stream)
+        for l in range(L):
+            if timed_kernels:
+                ev["v0"][l].record(stream)
+            tgdn.verify(inp.tree, dims, inp.q[l], inp.k[l], inp.v[l], inp.g[l], inp.b[l],
+                        states[l], outs[l], ws[l], stream)
+            if timed_kernels:
+                ev["v1"][l].record(stream)
+        tgdn.accept(inp.tree, inp.draft, inp.target, an, al, path, stream)
+        for l in range(L):
+            if timed_kernels:
+                ev["c0"][l].record(stream)
+            tgdn.commit(inp.tree, dims, an, inp.k[l], ws[l], states[l], states[l], stream)
+            if timed_kernels:
+                ev["c1"][l].record(stream)
+
+    # capture one graph per distinct step input
+    graphs = []
+    with torch.cuda.stream(stream):
+        for inp in inputs:        # warm the launch path before capture
+            step(inp)
+        stream.synchronize()
+        for inp in inputs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(inp)
+            graphs.append(g)
+    torch.cuda.synchronize()
+    launches_per_step = 1 + L + 1 + L
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    def timed(fn, K, W):
+        for s in range(W):
+            fn(s)
+        barrier()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for s in range(K):
+            fn(s)
+        t1.record(stream)
+        barrier()
+        ms = t0.elapsed_time(t1)
+        if world > 1:
+            t = torch.tensor([ms], dtype=torch.float64, device=device)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    torch.cuda.nvtx.range_push("timed")
+    def replay(s):
+        with torch.cuda.stream(stream):   # a graph replays on the current stream
+            graphs[s % R].replay()
+
+    ms = timed(replay, args.steps, args.warmup)
+    torch.cuda.nvtx.range_pop()
+    clk = clocks.stop()
+
+    # Per-kernel durations: the same step run eagerly with CUDA events around every launch.
+    # A spin kernel first holds the stream so that all launches of the step are queued
+    # before the GPU reaches them: they then run back to back, as in the graph.
+    kv, kc = [], []
+    for s in range(max(3, min(args.steps, 8))):
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(50_000_000)
+            step(inputs[s % R], timed_kernels=True)
+        stream.synchronize()
+        kv += [ev["v0"][l].elapsed_time(ev["v1"][l]) for l in range(L)]
+        kc += [ev["c0"][l].elapsed_time(ev["c1"][l]) for l in range(L)]
+    verify_us = 1e3 * statistics.mean(kv)
+    commit_us = 1e3 * statistics.mean(kc)
+
+    total_nodes = L * B * Nn * args.steps * world
+    value = total_nodes / (ms / 1e3)
+    hbm, peak_kind = peaks()
+    verify_bytes = B * S0_BYTES_PER_SEQ + B * Nn * NODE_BYTES
+    commit_bytes = 2 * B * S0_BYTES_PER_SEQ
+    v_gbs = verify_bytes / (verify_us * 1e-6) / 1e9
+    c_gbs = commit_bytes / (commit_us * 1e-6) / 1e9
+    if verify_us >= commit_us:
+        dom = dict(kernel="verify_tc_kernel", us=verify_us, bytes=verify_bytes, gbs=v_gbs)
+        other = dict(kernel="commit_kernel", us=commit_us, bytes=commit_bytes, gbs=c_gbs)
+    else:
+        dom = dict(kernel="commit_kernel", us=commit_us, bytes=commit_bytes, gbs=c_gbs)
+        other = dict(kernel="verify_tc_kernel", us=verify_us, bytes=verify_bytes, gbs=v_gbs)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, inputs, graphs, stream, an, al, path, timed, torch, R, L, B, Nn,
+                      world)
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{L}-layer GDN stack, B={B} per GPU, 64-node random trees "
+                               f"(depth<=12), H_qk=16 H_v=32 d=128, 50-step decode",
+                   "layers": L, "batch_per_gpu": B, "nodes_per_tree": Nn, "depth_max": 12,
+                   "H_qk": 16, "H_v": 32, "d_k": 128, "d_v": 128, "io": "bf16",
+                   "state": "fp32", "accumulate": "fp32",
+                   "step": f"prep + {L} verify + accept + {L} in-place commit (CUDA graph)",
+                   "l2": "inputs larger than L2 (~9 GB touched per step, L2 129 MB)",
+                   "distinct_step_inputs": R, "parallelism": f"dp{world} (sequences)"},
+        "roofline": {"bound": "hbm", "kernel": dom["kernel"], "achieved": dom["gbs"],
+                     "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": dom["gbs"] / hbm, "traffic": None,
+                     "algorithmic_bytes_per_launch": dom["bytes"],
+                     "launch_us": dom["us"],
+                     "other": {"kernel": other["kernel"], "achieved": other["gbs"],
+                               "frac": other["gbs"] / hbm, "launch_us": other["us"],
+                               "algorithmic_bytes_per_launch": other["bytes"]}},
+        "gpu_launches": launches_per_step * (args.steps),
+        "clocks": clk,
+    }
+    if e2e is not None:
+        result["e2e"] = e2e
+    return result
+
+
+def run_e2e(args, inputs, graphs, stream, an, al, path, timed, torch, R, L, B, Nn, world):
+    """Same step, but each step's inputs come from pinned host memory and the accepted
+    paths go back to the host, inside the timed region."""
+    host = []
+    for inp in inputs:
+        host.append([t.detach().to("cpu").pin_memory() for t in inp.tensors()])
+    res_host = [torch.empty_like(x, device="cpu").pin_memory() for x in (an, al, path)]
+    h2d = sum(t.numel() * t.element_size() for t in host[0])
+    d2h = sum(t.numel() * t.element_size() for t in res_host)
+
+    def fn(s):
+        r = s % R
+        with torch.cuda.stream(stream):
+            for dst, src in zip(inputs[r].tensors(), host[r]):
+                dst.copy_(src, non_blocking=True)
+            graphs[r].replay()
+            for dst, src in zip(res_host, (an, al, path)):
+                dst.copy_(src, non_blocking=True)
+
+    ms = timed(fn, args.steps, args.warmup)
+    value = L * B * Nn * args.steps * world / (ms / 1e3)
+    return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms / args.steps}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_sample(n_seqs: int, step: int = 0, layer: int = 0):
+    """A bounded slice of the workload: n_seqs whole sequences of one layer, all heads."""
+    p = synth.make_problem(CONFIG, step=step, layer=layer)
+    return synth.select_sequences(p, range(n_seqs))
+
+
+def time_oracle(n_seqs: int, step: int = 0):
+    import oracle
+    sub = oracle_sample(n_seqs, step=step)
+    t, i = sub.trees, sub.inputs
+    t0 = time.perf_counter()
+    o, used = oracle.verify(t.cu_nodes, t.parent, t.n_max, t.depth_max, i.q, i.k, i.v, i.g, i.b,
+                            sub.S0, return_threads=True)
+    acc = oracle.accept(t.cu_nodes, t.parent, t.n_max, t.depth_max, sub.draft_ids,
+                        sub.target_ids)
+    oracle.commit(t.cu_nodes, t.parent, t.n_max, t.depth_max, i.k, i.v, i.g, i.b, sub.S0,
+                  acc["accept_node"])
+    dt = time.perf_counter() - t0
+    return t.T, dt, used
+
+
+def cpu_baseline(min_seconds: float = 10.0, max_layers: int = 36):
+    """The oracle on whole layers of step 0 (all 32 sequences, all heads), layer after layer
+    until at least `min_seconds` of CPU work has been timed."""
+    import oracle
+    cfg = synth.CONFIGS[CONFIG]
+    nodes, dt, used, layers = 0, 0.0, 1, 0
+    while layers < max_layers and dt < min_seconds:
+        p = synth.make_problem(CONFIG, step=0, layer=layers)
+        t, i = p.trees, p.inputs
+        t0 = time.perf_counter()
+        _, used = oracle.verify(t.cu_nodes, t.parent, t.n_max, t.depth_max, i.q, i.k, i.v, i.g,
+                                i.b, p.S0, return_threads=True)
+        acc = oracle.accept(t.cu_nodes, t.parent, t.n_max, t.depth_max, p.draft_ids,
+                            p.target_ids)
+        oracle.commit(t.cu_nodes, t.parent, t.n_max, t.depth_max, i.k, i.v, i.g, i.b, p.S0,
+                      acc["accept_node"])
+        dt += time.perf_counter() - t0
+        nodes += t.T
+        layers += 1
+    return {"value": nodes / dt, "unit": UNIT, "cores": used, "kind": "oracle",
+            "sample": f"{layers} of 36 layers of step 0, all {cfg.B} sequences x 64 nodes x "
+                      f"32 v-heads: verify + accept + commit by fp64 path replay "
+                      f"({dt:.1f} s)",
+            "seconds": dt}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.lib()
+    n = args.cpu_sample_seqs
+    for _ in range(args.warmup if args.warmup <= 1 else 1):
+        time_oracle(1)
+    total_nodes, total_s, used = 0, 0.0, 1
+    for s in range(args.steps):
+        nodes, dt, used = time_oracle(n, step=s)
+        total_nodes += nodes
+        total_s += dt
+    value = total_nodes / total_s
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "36-layer GDN stack, 64-node random trees (depth<=12), "
+                                   "H_qk=16 H_v=32 d=128; each step a bounded sample",
+                       "sample_per_step": f"{n} sequences x 32 v-heads, one layer"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
+                             "sample": f"{n} sequences of one layer per step, {args.steps} steps"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    res = run_gpu(args, rank, world, local)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
