@@ -185,6 +185,36 @@ int tgdn_commit(const tgdn_tree* tree, const tgdn_dims* dims, const int32_t* acc
                 const void* k, const void* ws, const float* S_in, float* S_out,
                 tgdn_stream_t stream);
 
+/* Verification for callers that cannot allocate device memory.
+ *
+ * The paper has no counterpart to this call; it exists for integrators.  Some
+ * callers of this library cannot call cudaMalloc: a plugin inside a serving
+ * engine that has reserved all device memory for its own pools and hands its
+ * extensions only input and output buffers, or code on a latency-critical
+ * path that must not take cudaMalloc's implicit device synchronisation.
+ * tgdn_verify_noalloc computes exactly what tgdn_verify computes (same
+ * arguments minus the workspace) and keeps the factors U and G in a
+ * library-owned device array of TGDN_NOALLOC_SCRATCH_BYTES instead of a
+ * caller workspace.  That array is a file-scope static: every GPU that loads
+ * the library holds it until the process exits.
+ *   - Sizes: tgdn_verify_workspace_bytes(tree, dims) must not exceed
+ *     TGDN_NOALLOC_SCRATCH_BYTES, otherwise TGDN_ETOOBIG is returned and
+ *     nothing is enqueued.
+ *   - Device: the stream must belong to the current device.  The first call
+ *     on each device looks up the array's device address (cudaGetSymbolAddress)
+ *     with that device current; make that first call before any stream capture.
+ *   - Sharing: every call on a device uses the same array and leaves its
+ *     contents behind.  Calls whose kernels overlap on the GPU (different
+ *     streams without ordering) race on it; order them on one stream.
+ *   - The factors stay inside the library, so tgdn_commit cannot use them:
+ *     a caller that commits uses tgdn_verify with its own workspace.
+ * Allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ * Returns TGDN_OK, TGDN_EINVAL, TGDN_ETOOBIG or TGDN_ECUDA. */
+#define TGDN_NOALLOC_SCRATCH_BYTES (20u * 1024u * 1024u)
+int tgdn_verify_noalloc(const tgdn_tree* tree, const tgdn_dims* dims, const void* q,
+                        const void* k, const void* v, const float* g, const float* b,
+                        const float* S0, void* o, tgdn_stream_t stream);
+
 /* Static, human-readable text for a tgdn_status value. */
 const char* tgdn_status_string(int code);
 

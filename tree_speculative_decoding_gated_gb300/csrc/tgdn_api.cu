@@ -152,3 +152,53 @@ int tgdn_commit(const tgdn_tree* tree, const tgdn_dims* dims, const int32_t* acc
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// tgdn_verify_noalloc: the same verification with the factors kept in a
+// library-owned device array, for callers that cannot allocate.
+// ---------------------------------------------------------------------------
+namespace {
+
+// One array per device that loads the library, alive until the process exits.
+// In host code this name is only a host-side stand-in: the device address is
+// looked up once per device with cudaGetSymbolAddress and passed to kernels.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[TGDN_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the array on the current device (set up on first use).
+int noalloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TGDN_ECUDA;
+  if (dev < 0 || dev >= kMaxDevices) return TGDN_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return TGDN_ECUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return TGDN_OK;
+}
+
+}  // namespace
+
+extern "C" int tgdn_verify_noalloc(const tgdn_tree* tree, const tgdn_dims* dims, const void* q,
+                                   const void* k, const void* v, const float* g,
+                                   const float* b, const float* S0, void* o,
+                                   tgdn_stream_t stream) {
+  int rc = check_tree(tree);
+  if (rc != TGDN_OK) return rc;
+  rc = check_dims(dims);
+  if (rc != TGDN_OK) return rc;
+  if (tgdn::ws_layout(*tree, *dims).bytes > TGDN_NOALLOC_SCRATCH_BYTES) return TGDN_ETOOBIG;
+  void* ws = nullptr;
+  rc = noalloc_scratch(&ws);
+  if (rc != TGDN_OK) return rc;
+  // Every row of U and G that the launch covers is written by it, so the
+  // contents left by an earlier call need no clearing.
+  return tgdn_verify(tree, dims, q, k, v, g, b, S0, o, ws, stream);
+}

@@ -27,6 +27,7 @@ OK, EINVAL, ETOOBIG, ECUDA, EUNSUPPORTED = 0, -1, -3, -4, -5
 SEQ_OK, SEQ_TOO_BIG, SEQ_BAD_PARENT, SEQ_ROOTS, SEQ_CYCLE, SEQ_TOO_DEEP, SEQ_TIMEOUT = range(7)
 F32, BF16 = 0, 1
 MAX_NODES, MAX_DEPTH, MAX_HEAD_DIM = 256, 64, 128
+NOALLOC_SCRATCH_BYTES = 20 * 1024 * 1024
 
 
 class TgdnError(RuntimeError):
@@ -67,6 +68,8 @@ def lib() -> ctypes.CDLL:
         L.tgdn_verify.argtypes = [P(CTree), P(CDims), vp, vp, vp, vp, vp, vp, vp, vp, st]
         L.tgdn_accept.argtypes = [P(CTree), vp, vp, vp, vp, vp, st]
         L.tgdn_commit.argtypes = [P(CTree), P(CDims), vp, vp, vp, vp, vp, st]
+        L.tgdn_verify_noalloc.argtypes = [P(CTree), P(CDims), vp, vp, vp, vp, vp, vp, vp, st]
+        L.tgdn_verify_noalloc.restype = ctypes.c_int
         L.tgdn_status_string.argtypes = [i32]
         L.tgdn_status_string.restype = ctypes.c_char_p
         L.tgdn_version.argtypes = []
@@ -215,3 +218,21 @@ def commit(tree: Tree, dims: Dims, accept_node, k, ws, S_in, S_out, stream=None)
             _dev(S_in, torch.float32, ns, "S_in"), _dev(S_out, torch.float32, ns, "S_out"))
     _check(lib().tgdn_commit(ctypes.byref(ct), ctypes.byref(cd), *args, _stream(stream)),
            "tgdn_commit")
+
+
+def verify_noalloc(tree: Tree, dims: Dims, q, k, v, g, b, S0, o, stream=None) -> None:
+    """tgdn_verify_noalloc: verification for callers that cannot allocate device memory.
+
+    Same outputs as verify(); the factors stay in a library-owned device array of
+    NOALLOC_SCRATCH_BYTES (so they cannot be committed from).  Calls on one device share
+    that array: keep them ordered on one stream."""
+    T, B = tree.T, tree.B
+    io = dims.torch_dtype
+    ct, cd = tree.c(), dims.c()
+    args = (_dev(q, io, T * dims.H_qk * dims.d_k, "q"), _dev(k, io, T * dims.H_qk * dims.d_k, "k"),
+            _dev(v, io, T * dims.H_v * dims.d_v, "v"), _dev(g, torch.float32, T * dims.H_v, "g"),
+            _dev(b, torch.float32, T * dims.H_v, "b"),
+            _dev(S0, torch.float32, B * dims.H_v * dims.d_k * dims.d_v, "S0"),
+            _dev(o, io, T * dims.H_v * dims.d_v, "o"))
+    _check(lib().tgdn_verify_noalloc(ctypes.byref(ct), ctypes.byref(cd), *args, _stream(stream)),
+           "tgdn_verify_noalloc")
