@@ -2,7 +2,7 @@
 
 Covers random small trees (1-40 nodes, depth <= 16) for head sizes 16/64/128
 and both io types, chains, stars, single nodes, empty and invalid sequences in
-ragged batches, the 64-node / depth-32 limits of the tensor-core kernel, a
+ragged batches, the 64-node / depth-30 limits of the tensor-core kernel, a
 129-node tree, non-ancestor invariance (bitwise) and rollback-free two-step
 consistency.
 """
@@ -114,15 +114,15 @@ def test_too_big_and_too_deep():
     assert np.array_equal(got["S"], p.S0)
 
 
-@pytest.mark.parametrize("case", ["chain33", "chain34", "full64", "tree129"])
+@pytest.mark.parametrize("case", ["chain31", "chain32", "full64", "tree129"])
 def test_kernel_limits(case):
     rng = np.random.default_rng(11)
-    if case == "chain33":      # depth 32: the deepest tree the tensor-core kernel takes
-        parents = [synth.chain_tree(33), synth.random_recursive_tree(rng, 64, 32)]
-    elif case == "chain34":    # depth 33: SIMT kernel
-        parents = [synth.chain_tree(34)]
+    if case == "chain31":      # depth 30: the deepest tree the tensor-core kernel takes
+        parents = [synth.chain_tree(31), synth.random_recursive_tree(rng, 64, 30)]
+    elif case == "chain32":    # depth 31: SIMT kernel
+        parents = [synth.chain_tree(32)]
     elif case == "full64":     # 64 nodes in every sequence, mixed depths
-        parents = [synth.random_recursive_tree(rng, 64, int(c)) for c in (1, 4, 16, 32)]
+        parents = [synth.random_recursive_tree(rng, 64, int(c)) for c in (1, 4, 16, 30)]
     else:                      # 129 nodes: above the tensor-core node bound
         parents = [synth.top_m_tree(rng, 8, 16), synth.chain_tree(17)]
     p = custom(parents, 2, 4, 128, "bf16", 5)

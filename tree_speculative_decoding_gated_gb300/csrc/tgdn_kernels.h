@@ -33,7 +33,7 @@ cudaError_t launch_verify_simt(const tgdn_tree& t, const tgdn_dims& d, const voi
                                const void* k, const void* v, const float* g, const float* b,
                                const float* S0, void* o, float* U, float* G, cudaStream_t s);
 
-// Tensor-core verify: bf16 io, d_k = d_v = 128, n_max <= 64, depth_max <= 32.
+// Tensor-core verify: bf16 io, d_k = d_v = 128, n_max <= 64, depth_max <= 30.
 bool verify_tc_supported(const tgdn_tree& t, const tgdn_dims& d, const void* q, const void* k,
                          const void* v, const float* S0, const void* o);
 cudaError_t launch_verify_tc(const tgdn_tree& t, const tgdn_dims& d, const CUtensorMap& qmap,

@@ -2,28 +2,34 @@
 //
 // Single-pass verification of a draft tree through one GDN layer, following
 // "Trees from Marginals" (Technisches Resümee, Methodik 3 and Implementierung:
-// Gram matrix, tiled forward substitution and output phase in one kernel).
-// With G the path-cumulative log-gate,
-//   X_ns = b_n e^{G_n-G_s} k_n.k_s  (s strict ancestor of n)
-//   Y_ns =     e^{G_n-G_s} q_n.k_s  (s ancestor of n or n itself)
-//   (I + X) U = diag(b) (V - diag(e^G) K S0),   O = diag(e^G) Q S0 + Y U.
+// Gram matrix, forward substitution and output phase in one kernel).  With G
+// the path-cumulative log-gate and A(n) / A*(n) the strict / inclusive
+// ancestors of n,
+//   X_ns = b_n e^{G_n-G_s} k_n.k_s  (s in A(n)),  Y_ns = e^{G_n-G_s} q_n.k_s  (s in A*(n))
+//   (I + X) U = R = diag(b) (V - diag(e^G) K S0),   O = diag(e^G) Q S0 + Y U.
+// Because X only links a node to its own ancestors, T = (I + X)^{-1} and
+// W = Y T keep that sparsity, and row n of either depends only on the root
+// path of n: it is the solution of a (depth+1)-sized unit triangular system.
+// So U = T R and O = diag(e^G) Q S0 + W R.
 //
-// One CTA per (sequence, v-head, 64 value columns); 128 threads.
-//   1. TMA brings the tree's key and query rows of the CTA's q/k head into
-//      shared memory as one 128 x 128 bf16 operand A = [K; Q] (rows 0-63 keys,
-//      64-127 queries, 128-byte swizzle).  Meanwhile all threads stream the
-//      fp32 state slice S0[:, c0:c0+64] from HBM and split it into two bf16
-//      operands hi + lo (hi = bf16(S0), lo = bf16(S0 - hi)), so the products
-//      with S0 keep about 16 mantissa bits.
-//   2. One thread issues tcgen05.mma into TMEM (fp32 accumulators):
-//        D[:,  0: 64] = A . S0_hi + A . S0_lo   (K S0 rows and Q S0 rows)
-//        D[:, 64:128] = A . K^T                 (K K^T rows and Q K^T rows)
-//   3. Each thread reads its TMEM lane (one node's key or query row) and forms
-//      R = diag(b)(V - e^G K S0), e^G Q S0 and the ancestor-masked, gated
-//      X and Y entries; the operand buffers are dead by then and are reused.
-//   4. Forward substitution of (I + X) U = R one depth level at a time (nodes
-//      of one depth never depend on each other), then the output phase.  U and
-//      G go to the workspace for tgdn_commit.
+// One CTA per (sequence, v-head, 64 value columns); 128 threads; the tree has
+// at most 64 nodes and depth at most 30.
+//   1. TMA brings the key and query rows of the CTA's q/k head into shared
+//      memory as one 128 x 128 bf16 operand A = [K; Q] (128-byte swizzle).
+//      All threads stream the fp32 state slice S0[:, c0:c0+64] from HBM and
+//      split it into bf16 hi + lo operands (products keep ~16 mantissa bits).
+//   2. tcgen05.mma into TMEM (fp32):  D[:, 0:64] = A S0_hi + A S0_lo,
+//      D[:, 64:128] = A K^T.  Lane n < 64 holds k_n S0 and k_n.K; lane 64 + n
+//      holds q_n S0 and q_n.K.
+//   3. Every lane writes its Gram row to shared memory; key lanes form
+//      R = diag(b)(V - e^G K S0) as a bf16 hi + lo operand.
+//   4. Thread of key lane n solves its root path's system for row n of T,
+//      thread of query lane n for row n of W (back substitution over at most
+//      depth + 1 entries); the rows become a 128 x 64 bf16 hi + lo operand
+//      [T; W] (zero off the path).
+//   5. tcgen05.mma: D[:, 64:128] = [T; W] R (three bf16 products for hi/lo).
+//      Key lanes read U rows, query lanes read W R and add e^G Q S0.  U and G
+//      go to the workspace for tgdn_commit; O is stored as bf16.
 #include "tgdn_device.cuh"
 #include "tgdn_kernels.h"
 
@@ -34,42 +40,44 @@ constexpr int kTcNodes = 64;   // nodes per tree on this kernel
 constexpr int kTcDK = 128;
 constexpr int kTcDV = 128;
 constexpr int kTcCols = 64;    // value columns per CTA
-constexpr int kTcDepth = 32;   // depth bound on this kernel
-constexpr int kTcDM1 = kTcDepth + 1;
+constexpr int kTcDepth = 30;   // depth bound on this kernel
+constexpr int kTcPath = kTcDepth + 1;  // entries of a root path (odd: conflict-free stride)
 constexpr uint32_t kTmemCols = 128;
 
-// Shared-memory map (bytes from a 1024-byte aligned base).
-constexpr int kOffA = 0;           // [2 d_k halves][128 rows][128 B], swizzled
-constexpr int kOffBhi = 32768;     // [16 k-groups][8 rows][128 B], swizzled, MN-major
-constexpr int kOffBlo = 49152;
+// Shared-memory map (bytes from a 1024-byte aligned base).  Operands of the
+// first product are dead once it completes and their space is reused.
+constexpr int kOffA = 0;        // [K;Q] operand: [2 d_k halves][128 rows][128 B]
+constexpr int kOffS0hi = 32768; // S0 operand, MN-major: [16 k-groups][8 rows][128 B]
+constexpr int kOffS0lo = 49152;
+constexpr int kOffGR = 0;       // after product 1: Gram rows, [128 lanes][64] fp32
+constexpr int kOffRhi = 32768;  // R operand, MN-major: [8 node groups][8 rows][128 B]
+constexpr int kOffRlo = 40960;
+constexpr int kOffRS = 49152;   // per-thread path solutions, [128][kTcPath] fp32
+constexpr int kOffA2hi = 0;     // after the path solves: [T; W] operand, K-major
+constexpr int kOffA2lo = 16384;
 constexpr int kOperandBytes = 65536;
-// after the MMAs complete the operand area is reused:
-constexpr int kOffU = 0;           // [64 nodes][16 chunks x 16 B] fp32, chunk ^= row & 7
-constexpr int kOffEQ = 16384;      // e^G Q S0 rows, same layout
-constexpr int kOffXS = 32768;      // [64][33] fp32
-constexpr int kOffYS = kOffXS + kTcNodes * kTcDM1 * 4;
-static_assert(kOffYS + kTcNodes * kTcDM1 * 4 <= kOperandBytes, "scratch fits the operands");
-// persistent metadata
-constexpr int kOffMeta = kOperandBytes;
+static_assert(kOffRS + kTcThreads * kTcPath * 4 <= kOperandBytes, "path scratch fits");
+
 struct TcMeta {
   uint64_t tma_bar;
   uint64_t mma_bar;
-  uint64_t strict[kTcNodes];   // strict-ancestor mask by local index
   uint32_t tmem_slot;
   int bad;
   int tma_ok;
   int mma_issued;
-  int par[kTcNodes];
   int dep[kTcNodes];
+  int pos[kTcNodes];
   int ord[kTcNodes];
-  int lvl[kTcDM1 + 1];
   float G[kTcNodes];
   float bb[kTcNodes];
   float gg[kTcNodes];
-  uint8_t anc_at[kTcNodes][kTcDM1];
+  uint8_t anc_at[kTcNodes][kTcPath + 1];
 };
+constexpr int kOffMeta = kOperandBytes;
 constexpr int kTcSmemBytes = kOffMeta + (int)sizeof(TcMeta) + 1024;  // + alignment slack
 
+// 16-byte chunk swizzle used by every 128-byte-row operand (matches the TMA
+// and tcgen05 SWIZZLE_128B layout for 1024-byte aligned 8-row atoms).
 __device__ __forceinline__ int swz(int row, int chunk) { return chunk ^ (row & 7); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -77,15 +85,32 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&p);
 }
 
+// x ~= hi + lo with hi = bf16(x), lo = bf16(x - hi), for 8 consecutive values.
+__device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo) {
+  float h[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) h[i] = __bfloat162float(__float2bfloat16_rn(x[i]));
+  hi = make_uint4(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]), pack_bf16x2(h[4], h[5]),
+                  pack_bf16x2(h[6], h[7]));
+  lo = make_uint4(pack_bf16x2(x[0] - h[0], x[1] - h[1]), pack_bf16x2(x[2] - h[2], x[3] - h[3]),
+                  pack_bf16x2(x[4] - h[4], x[5] - h[5]), pack_bf16x2(x[6] - h[6], x[7] - h[7]));
+}
+
+// Byte offset of 16-byte chunk `chunk` of 128-byte row `row` in an operand made
+// of 1024-byte, 8-row swizzle atoms stacked along the row index.
+__device__ __forceinline__ int atom_off(int row, int chunk) {
+  return (row >> 3) * 1024 + (row & 7) * 128 + (swz(row, chunk) << 4);
+}
+
 __global__ void __launch_bounds__(kTcThreads)
 verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                  int H_qk, int H_v, int depth_max, const int32_t* __restrict__ cu,
-                 const int32_t* __restrict__ parent, const int32_t* __restrict__ depth,
-                 const int32_t* __restrict__ order, int32_t* __restrict__ status,
-                 const __nv_bfloat16* __restrict__ v, const float* __restrict__ g,
-                 const float* __restrict__ bta, const float* __restrict__ S0,
-                 __nv_bfloat16* __restrict__ o, float* __restrict__ Uws,
-                 float* __restrict__ Gws) {
+                 const int32_t* __restrict__ depth, const int32_t* __restrict__ order,
+                 const int32_t* __restrict__ pos, const uint64_t* __restrict__ anc,
+                 int32_t* __restrict__ status, const __nv_bfloat16* __restrict__ v,
+                 const float* __restrict__ g, const float* __restrict__ bta,
+                 const float* __restrict__ S0, __nv_bfloat16* __restrict__ o,
+                 float* __restrict__ Uws, float* __restrict__ Gws) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -119,7 +144,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     return;
   }
 
-  // ---- 1. operand staging: TMA for [K; Q], register path for S0 hi/lo
+  // ---- 1. operand staging
   if (tid == 0) {
     mbar_init(&m.tma_bar, 1);
     mbar_init(&m.mma_bar, 1);
@@ -137,87 +162,81 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
   __syncwarp();
   if (warp == 0) tmem_alloc(&m.tmem_slot, kTmemCols);
 
-  for (int n = tid; n < N; n += kTcThreads) {
-    const int p = parent[lo + n], dd = depth[lo + n], od = order[lo + n];
-    m.par[n] = p;
-    m.dep[n] = dd;
-    m.ord[n] = od;
-    if (p < -1 || p >= N || dd < 0 || dd > depth_max || dd > kTcDepth || od < 0 || od >= N)
+  const float* s0src = S0 + ((size_t)bi * H_v + h) * kTcDK * kTcDV + c0;
+  const int r0 = tid >> 4, q4 = tid & 15;  // 8 state rows x 16 float4 per pass
+  float4 sbuf[16];
+#pragma unroll
+  for (int p = 0; p < 16; ++p)
+    sbuf[p] = __ldg(reinterpret_cast<const float4*>(s0src + (size_t)(r0 + 8 * p) * kTcDV) + q4);
+
+  uint64_t my_anc = 0;
+  if (tid < N) {
+    const int dd = depth[lo + tid], ps = pos[lo + tid], od = order[lo + tid];
+    m.dep[tid] = dd;
+    m.pos[tid] = ps;
+    m.ord[tid] = od;
+    if (dd < 0 || dd > depth_max || dd > kTcDepth || ps < 0 || ps >= N || od < 0 || od >= N)
       m.bad = 1;
-    m.gg[n] = g[(size_t)(lo + n) * H_v + h];
-    m.bb[n] = bta[(size_t)(lo + n) * H_v + h];
+    else
+      my_anc = anc[lo + ps];  // one 64-bit word: n_max <= 64
+    m.gg[tid] = g[(size_t)(lo + tid) * H_v + h];
+    m.bb[tid] = bta[(size_t)(lo + tid) * H_v + h];
   }
 
-  {  // S0[:, c0:c0+64] -> bf16 hi/lo, MN-major with 128-byte swizzle
-    const float* src = S0 + ((size_t)bi * H_v + h) * kTcDK * kTcDV + c0;
-    const int r0 = tid >> 4, q4 = tid & 15;  // 8 rows x 16 float4 per pass
-    float4 buf[16];
 #pragma unroll
-    for (int p = 0; p < 16; ++p)
-      buf[p] = __ldg(reinterpret_cast<const float4*>(src + (size_t)(r0 + 8 * p) * kTcDV) + q4);
-#pragma unroll
-    for (int p = 0; p < 16; ++p) {
-      const int kr = r0 + 8 * p;  // d_k row
-      const float4 x = buf[p];
-      const float h0 = __bfloat162float(__float2bfloat16_rn(x.x));
-      const float h1 = __bfloat162float(__float2bfloat16_rn(x.y));
-      const float h2 = __bfloat162float(__float2bfloat16_rn(x.z));
-      const float h3 = __bfloat162float(__float2bfloat16_rn(x.w));
-      const uint2 hi = make_uint2(pack_bf16x2(h0, h1), pack_bf16x2(h2, h3));
-      const uint2 lw =
-          make_uint2(pack_bf16x2(x.x - h0, x.y - h1), pack_bf16x2(x.z - h2, x.w - h3));
-      const int off = (kr >> 3) * 1024 + (kr & 7) * 128 + (swz(kr, q4 >> 1) << 4) + (q4 & 1) * 8;
-      *reinterpret_cast<uint2*>(smem + kOffBhi + off) = hi;
-      *reinterpret_cast<uint2*>(smem + kOffBlo + off) = lw;
-    }
-    fence_proxy_async_smem();
+  for (int p = 0; p < 16; ++p) {  // S0 -> bf16 hi/lo, MN-major (row = d_k index)
+    const int kr = r0 + 8 * p;
+    const float4 x = sbuf[p];
+    const float h0 = __bfloat162float(__float2bfloat16_rn(x.x));
+    const float h1 = __bfloat162float(__float2bfloat16_rn(x.y));
+    const float h2 = __bfloat162float(__float2bfloat16_rn(x.z));
+    const float h3 = __bfloat162float(__float2bfloat16_rn(x.w));
+    const int off = atom_off(kr, q4 >> 1) + (q4 & 1) * 8;
+    *reinterpret_cast<uint2*>(smem + kOffS0hi + off) =
+        make_uint2(pack_bf16x2(h0, h1), pack_bf16x2(h2, h3));
+    *reinterpret_cast<uint2*>(smem + kOffS0lo + off) =
+        make_uint2(pack_bf16x2(x.x - h0, x.y - h1), pack_bf16x2(x.z - h2, x.w - h3));
   }
+  fence_proxy_async_smem();
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = m.tmem_slot;
 
-  // ---- root paths, path-cumulative log-gates and depth levels
-  if (!m.bad) {
-    for (int n = tid; n < N; n += kTcThreads) {
-      int s = n;
-      uint64_t strict = 0;
-      const int dn = m.dep[n];
-      for (int d = dn; d >= 0 && s >= 0; --d) {
-        m.anc_at[n][d] = static_cast<uint8_t>(s);
-        if (d < dn) strict |= 1ull << s;
-        s = m.par[s];
+  // ---- root path of every node from its ancestor mask (bits = topological
+  // positions, ascending = root first) and its path-cumulative log-gate
+  if (tid < N && !m.bad) {
+    const int dn = m.dep[tid];
+    uint64_t mk = my_anc;
+    bool ok = __popcll(mk) == dn + 1 && ((mk >> m.pos[tid]) & 1ull);
+    float acc = 0.f;
+    for (int i = 0; ok && i <= dn; ++i) {
+      const int b = __ffsll(static_cast<long long>(mk)) - 1;
+      mk &= mk - 1;
+      if (b >= N) {
+        ok = false;
+        break;
       }
-      if (s != -1) {  // the depth disagrees with the parent chain
-        m.bad = 1;
-        continue;
-      }
-      float acc = 0.f;
-      for (int d = 0; d <= dn; ++d) acc += m.gg[m.anc_at[n][d]];
-      m.G[n] = acc;
-      m.strict[n] = strict;
+      const int s = m.ord[b];
+      ok = m.dep[s] == i;
+      m.anc_at[tid][i] = static_cast<uint8_t>(s);
+      acc += m.gg[s];
     }
-    if (tid == 32) {
-      int cur = 0;
-      for (int p = 0; p < N; ++p) {
-        const int d = m.dep[m.ord[p]];
-        while (cur <= d) m.lvl[cur++] = p;
-      }
-      while (cur <= kTcDM1) m.lvl[cur++] = N;
-    }
+    if (!ok || m.anc_at[tid][dn] != tid) m.bad = 1;
+    m.G[tid] = acc;
   }
   __syncthreads();
 
-  // ---- 2. MMA issue (one thread).  The key/query copies are always waited
-  // for, so no copy is left in flight on any exit path.
+  // ---- 2. first product (one thread).  The key/query copies are always
+  // waited for, so no copy is left in flight on any exit path.
   if (tid == 0) {
     m.tma_ok = mbar_wait(&m.tma_bar, 0);
     m.mma_issued = 0;
     if (m.tma_ok && !m.bad) {
       tc_fence_after_sync();
       const uint32_t sA = smem_addr(smem + kOffA);
-      const uint32_t sHi = smem_addr(smem + kOffBhi);
-      const uint32_t sLo = smem_addr(smem + kOffBlo);
+      const uint32_t sHi = smem_addr(smem + kOffS0hi);
+      const uint32_t sLo = smem_addr(smem + kOffS0lo);
       constexpr uint32_t id_s0 = idesc_bf16_f32(128, kTcCols, 0, 1);
       constexpr uint32_t id_gram = idesc_bf16_f32(128, kTcNodes, 0, 0);
 #pragma unroll
@@ -239,68 +258,176 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
   if (m.mma_issued) mma_ok = !__syncthreads_or(!mbar_wait(&m.mma_bar, 0));
   tc_fence_after_sync();
 
-  // ---- 3. TMEM -> per-node rows (one TMEM lane per thread; warps 0-1 hold
-  // key rows, warps 2-3 query rows).  The operand area is dead and reused.
+  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  const bool key_row = warp < 2;
+  const int n = key_row ? tid : tid - 64;  // this thread's node
+  const bool live = n < N;
+
+  // ---- 3. Gram rows to shared memory; R = diag(b)(V - e^G K S0) as bf16 hi/lo
   if (mma_ok) {
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const bool key_row = warp < 2;
-    const int n = key_row ? tid : tid - 64;
-    const bool live = n < N;
-    float* U = reinterpret_cast<float*>(smem + kOffU);
-    float* EQ = reinterpret_cast<float*>(smem + kOffEQ);
-    float* XS = reinterpret_cast<float*>(smem + kOffXS);
-    float* YS = reinterpret_cast<float*>(smem + kOffYS);
-    const float Gn = live ? m.G[n] : 0.f;
-    const float eG = __expf(Gn);
-    const float bn = live ? m.bb[n] : 0.f;
-    const uint64_t strict = live ? m.strict[n] : 0ull;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      float r[32];
-      uint4 vv[4];
-      if (key_row && live) {
-        const uint4* vp = reinterpret_cast<const uint4*>(
-            v + ((size_t)(lo + n) * H_v + h) * kTcDV + c0 + half * 32);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) vv[i] = __ldg(vp + i);
-      }
-      tmem_ld32(tmem + lane_base + half * 32, r);
-      tmem_ld_wait();
-      if (live) {
-        float* dst = key_row ? U : EQ;
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          float4 w;
-          if (key_row) {
-            const __nv_bfloat162* vb = reinterpret_cast<const __nv_bfloat162*>(&vv[ch >> 1]);
-            const float2 v01 = __bfloat1622float2(vb[(ch & 1) * 2 + 0]);
-            const float2 v23 = __bfloat1622float2(vb[(ch & 1) * 2 + 1]);
-            w.x = bn * (v01.x - eG * r[ch * 4 + 0]);
-            w.y = bn * (v01.y - eG * r[ch * 4 + 1]);
-            w.z = bn * (v23.x - eG * r[ch * 4 + 2]);
-            w.w = bn * (v23.y - eG * r[ch * 4 + 3]);
-          } else {
-            w = make_float4(eG * r[ch * 4 + 0], eG * r[ch * 4 + 1], eG * r[ch * 4 + 2],
-                            eG * r[ch * 4 + 3]);
-          }
-          const int gch = half * 8 + ch;
-          *reinterpret_cast<float4*>(dst + n * 64 + swz(n, gch) * 4) = w;
-        }
-      }
-    }
-    // Gram row: key rows give X (strict ancestors), query rows give Y (ancestors + self)
-    const uint64_t mask = key_row ? strict : (strict | (live ? 1ull << n : 0ull));
-    const float scale = key_row ? bn : 1.f;
-    float* dst = key_row ? XS : YS;
+    float* GR = reinterpret_cast<float*>(smem + kOffGR);
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       float r[32];
       tmem_ld32(tmem + lane_base + kTcCols + half * 32, r);
       tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int s = half * 32 + i;
-        if ((mask >> s) & 1ull) dst[n * kTcDM1 + m.dep[s]] = scale * __expf(Gn - m.G[s]) * r[i];
+      for (int ch = 0; ch < 8; ++ch)
+        *reinterpret_cast<float4*>(GR + tid * 64 + swz(tid, half * 8 + ch) * 4) =
+            make_float4(r[ch * 4], r[ch * 4 + 1], r[ch * 4 + 2], r[ch * 4 + 3]);
+    }
+    if (key_row) {
+      const float eG = live ? __expf(m.G[n]) : 0.f;
+      const float bn = live ? m.bb[n] : 0.f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint4 vv[4] = {};
+        if (live) {
+          const uint4* vp = reinterpret_cast<const uint4*>(
+              v + ((size_t)(lo + n) * H_v + h) * kTcDV + c0 + half * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) vv[i] = __ldg(vp + i);
+        }
+        float r[32];
+        tmem_ld32(tmem + lane_base + half * 32, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {  // 8 columns per 16-byte bf16 chunk
+          const __nv_bfloat162* vb = reinterpret_cast<const __nv_bfloat162*>(&vv[ch]);
+          float x[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 vf = __bfloat1622float2(vb[i]);
+            x[2 * i] = live ? bn * (vf.x - eG * r[ch * 8 + 2 * i]) : 0.f;
+            x[2 * i + 1] = live ? bn * (vf.y - eG * r[ch * 8 + 2 * i + 1]) : 0.f;
+          }
+          uint4 hi, lw;
+          split8(x, hi, lw);  // rows of R beyond the tree are exact zeros
+          const int off = atom_off(n, half * 4 + ch);
+          *reinterpret_cast<uint4*>(smem + kOffRhi + off) = hi;
+          *reinterpret_cast<uint4*>(smem + kOffRlo + off) = lw;
+        }
+      }
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+
+  // ---- 4. one row of T (key lanes) or W (query lanes) per thread, by back
+  // substitution on the root path P = (p_0 = root, ..., p_d = n):
+  //   r (I + X_P) = y,  X_P[i][j] = b_{p_i} e^{G_{p_i} - G_{p_j}} k_{p_i}.k_{p_j} (i > j),
+  //   y = e_d for T;  y_j = e^{G_n - G_{p_j}} q_n.k_{p_j} for W.
+  // Every exponent is <= 0 (G only decreases down a path), so nothing overflows.
+  float* RS = reinterpret_cast<float*>(smem + kOffRS) + tid * kTcPath;
+  const uint8_t* P = m.anc_at[live ? n : 0];
+  const int dn = (mma_ok && live) ? m.dep[n] : -1;
+  if (dn >= 0) {
+    const float* GR = reinterpret_cast<const float*>(smem + kOffGR);
+    const float Gn = m.G[n];
+    for (int j = dn; j >= 0; --j) {
+      const int pj = P[j];
+      const float Gj = m.G[pj];
+      const int cj = pj >> 2, wj = pj & 3;
+      float y;
+      if (key_row)
+        y = (j == dn) ? 1.f : 0.f;
+      else
+        y = __expf(Gn - Gj) * GR[tid * 64 + swz(tid, cj) * 4 + wj];
+      float acc = 0.f;
+      for (int i = j + 1; i <= dn; ++i) {
+        const int pi = P[i];
+        const float x = m.bb[pi] * __expf(m.G[pi] - Gj) * GR[pi * 64 + swz(pi, cj) * 4 + wj];
+        acc = fmaf(RS[i], x, acc);
+      }
+      RS[j] = y - acc;
+    }
+  }
+  __syncthreads();  // the Gram rows are no longer read: their space becomes [T; W]
+
+  // [T; W] row `tid` as a bf16 hi/lo K-major operand: zero, then the path entries
+  {
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+      *reinterpret_cast<uint4*>(smem + kOffA2hi + atom_off(tid, ch)) = zero;
+      *reinterpret_cast<uint4*>(smem + kOffA2lo + atom_off(tid, ch)) = zero;
+    }
+    for (int j = 0; j <= dn; ++j) {
+      const int t = P[j];
+      const float r = RS[j];
+      const __nv_bfloat16 hi = __float2bfloat16_rn(r);
+      const __nv_bfloat16 lw = __float2bfloat16_rn(r - __bfloat162float(hi));
+      const int off = atom_off(tid, t >> 3) + (t & 7) * 2;
+      *reinterpret_cast<__nv_bfloat16*>(smem + kOffA2hi + off) = hi;
+      *reinterpret_cast<__nv_bfloat16*>(smem + kOffA2lo + off) = lw;
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+
+  // ---- 5. second product: D[:, 64:128] = [T; W] R  (hi.hi + hi.lo + lo.hi)
+  if (tid == 0 && mma_ok) {
+    const uint32_t sA2hi = smem_addr(smem + kOffA2hi);
+    const uint32_t sA2lo = smem_addr(smem + kOffA2lo);
+    const uint32_t sRhi = smem_addr(smem + kOffRhi);
+    const uint32_t sRlo = smem_addr(smem + kOffRlo);
+    constexpr uint32_t id_r = idesc_bf16_f32(128, kTcCols, 0, 1);
+#pragma unroll
+    for (int s = 0; s < kTcNodes / 16; ++s) {
+      const uint64_t ah = smem_desc(sA2hi + s * 32, 16, 1024, kSwizzle128B);
+      const uint64_t al = smem_desc(sA2lo + s * 32, 16, 1024, kSwizzle128B);
+      const uint64_t bh = smem_desc(sRhi + s * 2048, 1024, 1024, kSwizzle128B);
+      const uint64_t bl = smem_desc(sRlo + s * 2048, 1024, 1024, kSwizzle128B);
+      umma_bf16(tmem + kTcCols, ah, bh, id_r, s > 0);
+      umma_bf16(tmem + kTcCols, ah, bl, id_r, 1);
+      umma_bf16(tmem + kTcCols, al, bh, id_r, 1);
+    }
+    umma_commit(&m.mma_bar);
+  }
+  bool mma2_ok = false;
+  if (mma_ok) mma2_ok = !__syncthreads_or(!mbar_wait(&m.mma_bar, 1));
+  tc_fence_after_sync();
+
+  // ---- 6. key lanes: U rows to the workspace; query lanes: O = e^G Q S0 + W R
+  if (mma2_ok) {
+    if (key_row) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float r[32];
+        tmem_ld32(tmem + lane_base + kTcCols + half * 32, r);
+        tmem_ld_wait();
+        if (live) {
+          float4* dst = reinterpret_cast<float4*>(
+              Uws + ((size_t)(lo + n) * H_v + h) * kTcDV + c0 + half * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+        }
+      }
+      if (live && c == 0) Gws[(size_t)(lo + n) * H_v + h] = m.G[n];
+    } else {
+      const float eG = live ? __expf(m.G[n]) : 0.f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float a[32], w[32];
+        tmem_ld32(tmem + lane_base + half * 32, a);
+        tmem_ld32(tmem + lane_base + kTcCols + half * 32, w);
+        tmem_ld_wait();
+        if (live) {
+          uint4* dst = reinterpret_cast<uint4*>(
+              o + ((size_t)(lo + n) * H_v + h) * kTcDV + c0 + half * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float* aa = a + 8 * i;
+            const float* ww = w + 8 * i;
+            dst[i] = make_uint4(pack_bf16x2(fmaf(eG, aa[0], ww[0]), fmaf(eG, aa[1], ww[1])),
+                                pack_bf16x2(fmaf(eG, aa[2], ww[2]), fmaf(eG, aa[3], ww[3])),
+                                pack_bf16x2(fmaf(eG, aa[4], ww[4]), fmaf(eG, aa[5], ww[5])),
+                                pack_bf16x2(fmaf(eG, aa[6], ww[6]), fmaf(eG, aa[7], ww[7])));
+          }
+        }
       }
     }
   }
@@ -310,60 +437,13 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
   }
-  if (!mma_ok) {
-    if (!m.bad) {  // a bounded wait expired: report it, leave the outputs alone
-      if (tid == 0) status[bi] = TGDN_SEQ_TIMEOUT;
-    } else {
+  if (!mma2_ok) {
+    if (m.bad) {
       zero_rows();
+    } else if (tid == 0) {  // a bounded wait expired: report it, leave the outputs alone
+      status[bi] = TGDN_SEQ_TIMEOUT;
     }
-    return;
   }
-
-  // ---- 4. forward substitution over depth levels, then the output phase
-  float* U = reinterpret_cast<float*>(smem + kOffU);
-  const float* EQ = reinterpret_cast<const float*>(smem + kOffEQ);
-  const float* XS = reinterpret_cast<const float*>(smem + kOffXS);
-  const float* YS = reinterpret_cast<const float*>(smem + kOffYS);
-  int maxdep = 0;
-  while (maxdep + 1 <= kTcDepth && m.lvl[maxdep + 1] < N) ++maxdep;
-  for (int d = 1; d <= maxdep; ++d) {
-    const int p0 = m.lvl[d], cnt = m.lvl[d + 1] - p0;
-    for (int it = tid; it < cnt * 16; it += kTcThreads) {
-      const int n = m.ord[p0 + (it >> 4)], ch = it & 15;
-      float4 acc = *reinterpret_cast<const float4*>(U + n * 64 + swz(n, ch) * 4);
-      for (int dd = 0; dd < d; ++dd) {
-        const int s = m.anc_at[n][dd];
-        const float x = XS[n * kTcDM1 + dd];
-        const float4 us = *reinterpret_cast<const float4*>(U + s * 64 + swz(s, ch) * 4);
-        acc.x = fmaf(-x, us.x, acc.x);
-        acc.y = fmaf(-x, us.y, acc.y);
-        acc.z = fmaf(-x, us.z, acc.z);
-        acc.w = fmaf(-x, us.w, acc.w);
-      }
-      *reinterpret_cast<float4*>(U + n * 64 + swz(n, ch) * 4) = acc;
-    }
-    __syncthreads();
-  }
-  for (int it = tid; it < N * 16; it += kTcThreads) {
-    const int n = it >> 4, ch = it & 15;
-    float4 acc = *reinterpret_cast<const float4*>(EQ + n * 64 + swz(n, ch) * 4);
-    const int dn = m.dep[n];
-    for (int dd = 0; dd <= dn; ++dd) {
-      const int s = m.anc_at[n][dd];
-      const float y = YS[n * kTcDM1 + dd];
-      const float4 us = *reinterpret_cast<const float4*>(U + s * 64 + swz(s, ch) * 4);
-      acc.x = fmaf(y, us.x, acc.x);
-      acc.y = fmaf(y, us.y, acc.y);
-      acc.z = fmaf(y, us.z, acc.z);
-      acc.w = fmaf(y, us.w, acc.w);
-    }
-    const size_t row = ((size_t)(lo + n) * H_v + h) * kTcDV + c0 + ch * 4;
-    *reinterpret_cast<uint2*>(o + row) = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
-    *reinterpret_cast<float4*>(Uws + row) =
-        *reinterpret_cast<const float4*>(U + n * 64 + swz(n, ch) * 4);
-  }
-  if (c == 0)
-    for (int n = tid; n < N; n += kTcThreads) Gws[(size_t)(lo + n) * H_v + h] = m.G[n];
 }
 
 bool verify_tc_supported(const tgdn_tree& t, const tgdn_dims& d, const void* q, const void* k,
@@ -385,8 +465,9 @@ cudaError_t launch_verify_tc(const tgdn_tree& t, const tgdn_dims& d, const CUten
   if (grid == 0) return cudaSuccess;
   if (grid > 0x7fffffffL) return cudaErrorInvalidConfiguration;
   verify_tc_kernel<<<(unsigned)grid, kTcThreads, kTcSmemBytes, s>>>(
-      qmap, kmap, d.H_qk, d.H_v, t.depth_max, t.cu_nodes, t.parent, t.depth, t.order, t.status,
-      static_cast<const __nv_bfloat16*>(v), g, b, S0, static_cast<__nv_bfloat16*>(o), U, G);
+      qmap, kmap, d.H_qk, d.H_v, t.depth_max, t.cu_nodes, t.depth, t.order, t.pos, t.anc,
+      t.status, static_cast<const __nv_bfloat16*>(v), g, b, S0, static_cast<__nv_bfloat16*>(o),
+      U, G);
   return cudaGetLastError();
 }
 
