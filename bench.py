@@ -59,6 +59,26 @@ def parse():
     return ap.parse_args()
 
 
+def shard_range(n_units: int, world: int, rank: int) -> range:
+    """Contiguous, balanced share of `n_units` independent units (sequences) for `rank`.
+    Sequences never exchange data on this path, so ranks need no collective."""
+    base, extra = divmod(n_units, world)
+    start = rank * base + min(rank, extra)
+    return range(start, start + base + (1 if rank < extra else 0))
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """The slowest rank's elapsed time (the only cross-rank reduction the benchmark does)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -232,12 +252,7 @@ def run_gpu(args, rank, world, local):
             fn(s)
         t1.record(stream)
         barrier()
-        ms = t0.elapsed_time(t1)
-        if world > 1:
-            t = torch.tensor([ms], dtype=torch.float64, device=device)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return max_over_ranks(t0.elapsed_time(t1), world)
 
     clocks = ClockSampler(local)
     clocks.start()

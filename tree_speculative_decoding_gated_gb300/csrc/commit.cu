@@ -8,31 +8,37 @@
 // a rank-|P| update of the d_k x d_v fp32 state (|P| <= depth_max + 1).
 //
 // The kernel streams the state once (read S_in, write S_out; in place is
-// allowed): one CTA per (sequence, v-head, 32 state rows), 256 threads, each
-// thread a 4-row x 4-column register tile, so every warp instruction moves one
-// contiguous 512-byte state row.
+// allowed).  One CTA per (sequence, v-head, 64 state rows), 256 threads, each
+// thread two 4-row x 4-column register tiles, so every warp instruction moves
+// one contiguous 512-byte state row.  The state loads are issued first; the
+// accepted path is read meanwhile from the ancestor mask written by tree prep
+// (one thread per candidate bit, no pointer chasing).
 #include "tgdn_device.cuh"
 #include "tgdn_kernels.h"
 
 namespace tgdn {
 
 constexpr int kCommitThreads = 256;
-constexpr int kCommitRows = 32;  // state rows per CTA
+constexpr int kCommitRows = 64;  // state rows per CTA
+constexpr int kCommitTiles = 2;  // 4x4 tiles per thread on the vector path (d_v = 128)
 
 template <typename T>
 __global__ void __launch_bounds__(kCommitThreads)
-commit_kernel(int H_qk, int H_v, int dk, int dv, int depth_max, const int32_t* __restrict__ cu,
-              const int32_t* __restrict__ parent, const int32_t* __restrict__ depth,
-              const int32_t* __restrict__ status, const int32_t* __restrict__ accept_node,
-              const T* __restrict__ k, const float* __restrict__ Uws,
-              const float* __restrict__ Gws, const float* S_in, float* S_out, int vec) {
+commit_kernel(int H_qk, int H_v, int dk, int dv, int depth_max, int words,
+              const int32_t* __restrict__ cu, const int32_t* __restrict__ depth,
+              const int32_t* __restrict__ order, const int32_t* __restrict__ pos,
+              const uint64_t* __restrict__ anc, const int32_t* __restrict__ status,
+              const int32_t* __restrict__ accept_node, const T* __restrict__ k,
+              const float* __restrict__ Uws, const float* __restrict__ Gws, const float* S_in,
+              float* S_out, int vec128) {
   extern __shared__ __align__(16) float csm[];
   const int DM1 = depth_max + 1;
   float* ck = csm;                          // [DM1][kCommitRows]  e^{G*-G_s} k_s[row]
   float* us = csm + DM1 * kCommitRows;      // [DM1][dv]           u_s
   __shared__ int s_path[TGDN_MAX_DEPTH + 1];
+  __shared__ uint64_t s_mask[TGDN_MAX_NODES / 64];
   __shared__ int s_len;
-  __shared__ float s_decay;
+  __shared__ int s_ok;
 
   const int rblocks = (dk + kCommitRows - 1) / kCommitRows;
   const int rb = blockIdx.x % rblocks;
@@ -42,35 +48,64 @@ commit_kernel(int H_qk, int H_v, int dk, int dv, int depth_max, const int32_t* _
   const int r0 = rb * kCommitRows;
   const int nrows = min(kCommitRows, dk - r0);
   const int tid = threadIdx.x;
-  const int lo = cu[bi], N = cu[bi + 1] - lo;
   const size_t sbase = ((size_t)bi * H_v + h) * dk * dv + (size_t)r0 * dv;
 
+  // ---- state loads first (vector path: d_v = 128, all 64 rows present)
+  const int cg = tid & 31, rg0 = tid >> 5;  // column group, first row group
+  float4 acc[kCommitTiles][4];
+  if (vec128) {
+#pragma unroll
+    for (int t = 0; t < kCommitTiles; ++t)
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+        acc[t][r] = *reinterpret_cast<const float4*>(
+            S_in + sbase + (size_t)((rg0 + 8 * t) * 4 + r) * dv + cg * 4);
+  }
+
+  // ---- the accepted path from tree prep's ancestor mask
+  const int lo = cu[bi], N = cu[bi + 1] - lo;
+  const int n = accept_node[bi];
   if (tid == 0) {
-    const int n = accept_node[bi];
-    int len = 0;
-    if (status[bi] == TGDN_SEQ_OK && n >= 0 && n < N) {
-      const int dn = depth[lo + n];
-      if (dn >= 0 && dn <= depth_max) {
-        int j = n, d = dn;
-        for (; d >= 0 && j >= 0 && j < N; --d) {
-          s_path[d] = j;
-          j = parent[lo + j];
-        }
-        if (d == -1 && j == -1) len = dn + 1;  // the path reached the root at depth 0
-      }
+    s_ok = status[bi] == TGDN_SEQ_OK && n >= 0 && n < N;
+    s_len = 0;
+  }
+  __syncthreads();
+  int p = -1, dn = -1;
+  if (s_ok) {
+    p = pos[lo + n];
+    dn = depth[lo + n];
+    if (p < 0 || p >= N || dn < 0 || dn > depth_max) p = -1;
+  }
+  if (p >= 0 && tid < words) s_mask[tid] = anc[(size_t)(lo + p) * words + tid];
+  __syncthreads();
+  if (p >= 0 && tid < N) {
+    const uint64_t w = s_mask[tid >> 6];
+    if ((w >> (tid & 63)) & 1ull) {
+      int rank = __popcll(w & ((1ull << (tid & 63)) - 1ull));
+      for (int j = 0; j < (tid >> 6); ++j) rank += __popcll(s_mask[j]);
+      if (rank <= dn) s_path[rank] = order[lo + tid];
+      if (rank == dn) s_len = dn + 1;  // the deepest set bit is n* itself
     }
-    s_len = len;
-    s_decay = len ? __expf(Gws[(size_t)(lo + n) * H_v + h]) : 1.f;
   }
   __syncthreads();
   const int L = s_len;
+
   if (L == 0) {  // nothing accepted: the state is kept
-    if (S_out != S_in)
-      for (int e = tid; e < nrows * dv; e += kCommitThreads)
-        S_out[sbase + e] = S_in[sbase + e];
+    if (S_out != S_in) {
+      if (vec128) {
+#pragma unroll
+        for (int t = 0; t < kCommitTiles; ++t)
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+            *reinterpret_cast<float4*>(S_out + sbase + (size_t)((rg0 + 8 * t) * 4 + r) * dv +
+                                       cg * 4) = acc[t][r];
+      } else {
+        for (int e = tid; e < nrows * dv; e += kCommitThreads) S_out[sbase + e] = S_in[sbase + e];
+      }
+    }
     return;
   }
-  const float Gstar = Gws[(size_t)(lo + s_path[L - 1]) * H_v + h];
+  const float Gstar = Gws[(size_t)(lo + n) * H_v + h];
   for (int e = tid; e < L * kCommitRows; e += kCommitThreads) {
     const int l = e / kCommitRows, i = e % kCommitRows;
     const int s = s_path[l];
@@ -82,48 +117,42 @@ commit_kernel(int H_qk, int H_v, int dk, int dv, int depth_max, const int32_t* _
     us[e] = Uws[((size_t)(lo + s_path[l]) * H_v + h) * dv + j];
   }
   __syncthreads();
-  const float decay = s_decay;
+  const float decay = __expf(Gstar);
 
-  if (vec) {
-    // 4x4 register tiles: column group cg, rows rg*4 .. rg*4+3
-    const int ncg = dv >> 2;
-    const int tiles = ((nrows + 3) >> 2) * ncg;
-    for (int t = tid; t < tiles; t += kCommitThreads) {
-      const int cg = t % ncg, rg = t / ncg;
-      float4 acc[4];
+  if (vec128) {
+#pragma unroll
+    for (int t = 0; t < kCommitTiles; ++t) {
+      const int rg = rg0 + 8 * t;
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const int i = rg * 4 + r;
-        acc[r] = (i < nrows) ? *reinterpret_cast<const float4*>(S_in + sbase + (size_t)i * dv + cg * 4)
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
-        acc[r].x *= decay;
-        acc[r].y *= decay;
-        acc[r].z *= decay;
-        acc[r].w *= decay;
+        acc[t][r].x *= decay;
+        acc[t][r].y *= decay;
+        acc[t][r].z *= decay;
+        acc[t][r].w *= decay;
       }
       for (int l = 0; l < L; ++l) {
         const float4 u = *reinterpret_cast<const float4*>(us + l * dv + cg * 4);
+        const float4 kv = *reinterpret_cast<const float4*>(ck + l * kCommitRows + rg * 4);
+        const float kr[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          const float kv = ck[l * kCommitRows + rg * 4 + r];
-          acc[r].x = fmaf(kv, u.x, acc[r].x);
-          acc[r].y = fmaf(kv, u.y, acc[r].y);
-          acc[r].z = fmaf(kv, u.z, acc[r].z);
-          acc[r].w = fmaf(kv, u.w, acc[r].w);
+          acc[t][r].x = fmaf(kr[r], u.x, acc[t][r].x);
+          acc[t][r].y = fmaf(kr[r], u.y, acc[t][r].y);
+          acc[t][r].z = fmaf(kr[r], u.z, acc[t][r].z);
+          acc[t][r].w = fmaf(kr[r], u.w, acc[t][r].w);
         }
       }
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int i = rg * 4 + r;
-        if (i < nrows) *reinterpret_cast<float4*>(S_out + sbase + (size_t)i * dv + cg * 4) = acc[r];
-      }
+      for (int r = 0; r < 4; ++r)
+        *reinterpret_cast<float4*>(S_out + sbase + (size_t)(rg * 4 + r) * dv + cg * 4) =
+            acc[t][r];
     }
   } else {
     for (int e = tid; e < nrows * dv; e += kCommitThreads) {
       const int i = e / dv, j = e % dv;
-      float acc = decay * S_in[sbase + e];
-      for (int l = 0; l < L; ++l) acc = fmaf(ck[l * kCommitRows + i], us[l * dv + j], acc);
-      S_out[sbase + e] = acc;
+      float a = decay * S_in[sbase + e];
+      for (int l = 0; l < L; ++l) a = fmaf(ck[l * kCommitRows + i], us[l * dv + j], a);
+      S_out[sbase + e] = a;
     }
   }
 }
@@ -139,15 +168,16 @@ static cudaError_t launch_commit_t(const tgdn_tree& t, const tgdn_dims& d,
   if (grid > 0x7fffffffL) return cudaErrorInvalidConfiguration;
   const size_t smem = (size_t)(t.depth_max + 1) * (kCommitRows + d.d_v) * sizeof(float);
   const auto kern = commit_kernel<T>;
-  const int vec = (d.d_v % 4 == 0) && (reinterpret_cast<uintptr_t>(S_in) % 16 == 0) &&
-                  (reinterpret_cast<uintptr_t>(S_out) % 16 == 0);
+  // vector path: 128 value columns, whole 64-row blocks, 16-byte aligned states
+  const int vec128 = (d.d_v == 128) && (d.d_k % kCommitRows == 0) &&
+                     (reinterpret_cast<uintptr_t>(S_in) % 16 == 0) &&
+                     (reinterpret_cast<uintptr_t>(S_out) % 16 == 0);
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)grid, kCommitThreads, smem, s>>>(d.H_qk, d.H_v, d.d_k, d.d_v, t.depth_max,
-                                                     t.cu_nodes, t.parent, t.depth, t.status,
-                                                     accept_node, static_cast<const T*>(k), U, G,
-                                                     S_in, S_out, vec);
+  kern<<<(unsigned)grid, kCommitThreads, smem, s>>>(
+      d.H_qk, d.H_v, d.d_k, d.d_v, t.depth_max, t.words, t.cu_nodes, t.depth, t.order, t.pos,
+      t.anc, t.status, accept_node, static_cast<const T*>(k), U, G, S_in, S_out, vec128);
   return cudaGetLastError();
 }
 
