@@ -158,6 +158,19 @@ int tgdn_verify(const tgdn_tree* tree, const tgdn_dims* dims, const void* q, con
                 const void* v, const float* g, const float* b, const float* S0, void* o,
                 void* ws, tgdn_stream_t stream);
 
+/* Per-branch recurrent verification, the method the pages measure the fused
+ * kernel against ("Trees from Marginals", Experimentelle Ergebnisse: the fused
+ * kernel versus per-branch recurrent verification at tree size 128).  Every
+ * root-to-leaf branch is walked token by token with the GDN update eq. from
+ * S0, recomputing shared prefixes; every node's output is written (nodes on
+ * several branches get the same value again).  Same arguments and outputs as
+ * tgdn_verify, without the workspace (no factors are produced, so nothing can
+ * be committed from it).  tgdn_tree_prep must have run on `tree`.
+ * Returns TGDN_OK, TGDN_EINVAL, TGDN_ETOOBIG or TGDN_ECUDA. */
+int tgdn_verify_recurrent(const tgdn_tree* tree, const tgdn_dims* dims, const void* q,
+                          const void* k, const void* v, const float* g, const float* b,
+                          const float* S0, void* o, tgdn_stream_t stream);
+
 /* Greedy acceptance (Experimentelle Ergebnisse, mean acceptance length).  The
  * root is always accepted; a non-root node is accepted when it and every
  * non-root node on its root path satisfy target_ids == draft_ids.  The

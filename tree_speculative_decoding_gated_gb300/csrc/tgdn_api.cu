@@ -115,6 +115,21 @@ int tgdn_verify(const tgdn_tree* tree, const tgdn_dims* dims, const void* q, con
   return from_cuda(tgdn::launch_verify_simt(t, d, q, k, v, g, b, S0, o, U, G, s));
 }
 
+int tgdn_verify_recurrent(const tgdn_tree* tree, const tgdn_dims* dims, const void* q,
+                          const void* k, const void* v, const float* g, const float* b,
+                          const float* S0, void* o, tgdn_stream_t stream) {
+  int rc = check_tree(tree);
+  if (rc != TGDN_OK) return rc;
+  rc = check_dims(dims);
+  if (rc != TGDN_OK) return rc;
+  const tgdn_tree& t = *tree;
+  if (t.T > 0 && (!q || !k || !v || !g || !b || !o)) return TGDN_EINVAL;
+  if (t.B > 0 && !S0) return TGDN_EINVAL;
+  if (t.B == 0 || t.T == 0) return TGDN_OK;
+  return from_cuda(tgdn::launch_verify_recurrent(t, *dims, q, k, v, g, b, S0, o,
+                                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int tgdn_accept(const tgdn_tree* tree, const int32_t* draft_ids, const int32_t* target_ids,
                 int32_t* accept_node, int32_t* accept_len, int32_t* path,
                 tgdn_stream_t stream) {

@@ -41,6 +41,11 @@ cudaError_t launch_verify_tc(const tgdn_tree& t, const tgdn_dims& d, const CUten
                              const float* b, const float* S0, void* o, float* U, float* G,
                              cudaStream_t s);
 
+// Per-branch recurrent verification (every root-to-leaf path replayed from S0).
+cudaError_t launch_verify_recurrent(const tgdn_tree& t, const tgdn_dims& d, const void* q,
+                                    const void* k, const void* v, const float* g,
+                                    const float* b, const float* S0, void* o, cudaStream_t s);
+
 cudaError_t launch_commit(const tgdn_tree& t, const tgdn_dims& d, const int32_t* accept_node,
                           const void* k, const float* U, const float* G, const float* S_in,
                           float* S_out, cudaStream_t s);

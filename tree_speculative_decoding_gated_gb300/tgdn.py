@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
         L.tgdn_verify.argtypes = [P(CTree), P(CDims), vp, vp, vp, vp, vp, vp, vp, vp, st]
         L.tgdn_accept.argtypes = [P(CTree), vp, vp, vp, vp, vp, st]
         L.tgdn_commit.argtypes = [P(CTree), P(CDims), vp, vp, vp, vp, vp, st]
+        L.tgdn_verify_recurrent.argtypes = [P(CTree), P(CDims), vp, vp, vp, vp, vp, vp, vp, st]
+        L.tgdn_verify_recurrent.restype = ctypes.c_int
         L.tgdn_verify_noalloc.argtypes = [P(CTree), P(CDims), vp, vp, vp, vp, vp, vp, vp, st]
         L.tgdn_verify_noalloc.restype = ctypes.c_int
         L.tgdn_status_string.argtypes = [i32]
@@ -195,6 +197,20 @@ def verify(tree: Tree, dims: Dims, q, k, v, g, b, S0, o, ws, stream=None) -> Non
             _dev(ws, torch.uint8, verify_workspace_bytes(tree, dims), "ws"))
     _check(lib().tgdn_verify(ctypes.byref(ct), ctypes.byref(cd), *args, _stream(stream)),
            "tgdn_verify")
+
+
+def verify_recurrent(tree: Tree, dims: Dims, q, k, v, g, b, S0, o, stream=None) -> None:
+    """tgdn_verify_recurrent: the per-branch recurrent baseline (same outputs as verify)."""
+    T, B = tree.T, tree.B
+    io = dims.torch_dtype
+    ct, cd = tree.c(), dims.c()
+    args = (_dev(q, io, T * dims.H_qk * dims.d_k, "q"), _dev(k, io, T * dims.H_qk * dims.d_k, "k"),
+            _dev(v, io, T * dims.H_v * dims.d_v, "v"), _dev(g, torch.float32, T * dims.H_v, "g"),
+            _dev(b, torch.float32, T * dims.H_v, "b"),
+            _dev(S0, torch.float32, B * dims.H_v * dims.d_k * dims.d_v, "S0"),
+            _dev(o, io, T * dims.H_v * dims.d_v, "o"))
+    _check(lib().tgdn_verify_recurrent(ctypes.byref(ct), ctypes.byref(cd), *args,
+                                       _stream(stream)), "tgdn_verify_recurrent")
 
 
 def accept(tree: Tree, draft_ids, target_ids, accept_node, accept_len, path, stream=None) -> None:
