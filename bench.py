@@ -3,9 +3,12 @@
 Workload (default): the 36-layer stack — 32 sequences per GPU, each a 64-node
 random draft tree of depth <= 12, H_qk = 16, H_v = 32, d_k = d_v = 128, bf16
 q/k/v, fp32 states (one per layer and v-head).  One step is one decode
-iteration through the library's C ABI:
-    tgdn_tree_prep -> 36 x tgdn_verify -> tgdn_accept -> 36 x tgdn_commit (in place)
-captured once per distinct step input into a CUDA graph and replayed.
+iteration through the library's C ABI.  Default (--mode fused), the commit of
+the previous step's accepted node is folded into this step's verify:
+    tgdn_tree_prep -> 36 x tgdn_verify_fused -> tgdn_accept
+(--mode separate: tgdn_tree_prep -> 36 x tgdn_verify -> tgdn_accept ->
+36 x tgdn_commit in place), captured once per distinct step input into a CUDA
+graph and replayed.
 Inputs are seeded synthetic data resident in HBM; a step touches ~9 GB, far
 more than the 129 MB L2, so no flush is needed between steps.
 
@@ -56,6 +59,8 @@ def parse():
     ap.add_argument("--cpu-sample-seqs", type=int, default=4)
     ap.add_argument("--layers", type=int, default=36,
                     help="GDN layers per step (fewer only for small profiler captures)")
+    ap.add_argument("--mode", default="fused", choices=["fused", "separate"],
+                    help="fused: commit folded into the next step's verify; separate: own pass")
     return ap.parse_args()
 
 
@@ -183,21 +188,27 @@ def run_gpu(args, rank, world, local):
     device = torch.device("cuda", local)
     cfg = synth.CONFIGS[CONFIG]
     L, B, Nn = args.layers, cfg.B, cfg.n_nodes
+    fused = args.mode == "fused"
     dims = tgdn.Dims(cfg.H_qk, cfg.H_v, cfg.dk, cfg.dv, tgdn.BF16)
     gen = torch.Generator(device=device)
     gen.manual_seed(synth.BASE_SEED + cfg.number + 1000 + 7919 * rank)
 
-    R = max(1, args.inputs)
+    # fused mode needs two inputs at least: a step's workspace must not be the previous one's
+    R = max(2 if fused else 1, args.inputs)
     inputs = [StepInput(cfg, r + R * rank, L, gen, device, tgdn, torch) for r in range(R)]
     states = [synth.make_state_device(cfg, B, gen, device) for _ in range(L)]
     T = inputs[0].tree.T
     ws_bytes = tgdn.verify_workspace_bytes(inputs[0].tree, dims)
-    ws = [torch.empty(ws_bytes, dtype=torch.uint8, device=device) for _ in range(L)]
+    # workspaces and acceptance outputs per distinct input (fused: step r commits from r - 1)
+    n_ws = R if fused else 1
+    ws = [[torch.empty(ws_bytes, dtype=torch.uint8, device=device) for _ in range(L)]
+          for _ in range(n_ws)]
     outs = [torch.empty((T, cfg.H_v, cfg.dv), dtype=torch.bfloat16, device=device)
             for _ in range(L)]
-    an = torch.empty(B, dtype=torch.int32, device=device)
-    al = torch.empty(B, dtype=torch.int32, device=device)
-    path = torch.empty((B, cfg.depth_max + 1), dtype=torch.int32, device=device)
+    an = [torch.empty(B, dtype=torch.int32, device=device) for _ in range(n_ws)]
+    al = [torch.empty(B, dtype=torch.int32, device=device) for _ in range(n_ws)]
+    path = [torch.empty((B, cfg.depth_max + 1), dtype=torch.int32, device=device)
+            for _ in range(n_ws)]
 
     stream = torch.cuda.Stream(device)
     ev = {"v0": [torch.cuda.Event(enable_timing=True) for _ in range(L)],
@@ -205,36 +216,67 @@ def run_gpu(args, rank, world, local):
           "c0": [torch.cuda.Event(enable_timing=True) for _ in range(L)],
           "c1": [torch.cuda.Event(enable_timing=True) for _ in range(L)]}
 
-    def step(inp: StepInput, timed_kernels=False):
+    def step_separate(r: int, timed_kernels=False):
+        inp = inputs[r]
         tgdn.tree_prep(inp.tree, stream)
         for l in range(L):
             if timed_kernels:
                 ev["v0"][l].record(stream)
             tgdn.verify(inp.tree, dims, inp.q[l], inp.k[l], inp.v[l], inp.g[l], inp.b[l],
-                        states[l], outs[l], ws[l], stream)
+                        states[l], outs[l], ws[0][l], stream)
             if timed_kernels:
                 ev["v1"][l].record(stream)
-        tgdn.accept(inp.tree, inp.draft, inp.target, an, al, path, stream)
+        tgdn.accept(inp.tree, inp.draft, inp.target, an[0], al[0], path[0], stream)
         for l in range(L):
             if timed_kernels:
                 ev["c0"][l].record(stream)
-            tgdn.commit(inp.tree, dims, an, inp.k[l], ws[l], states[l], states[l], stream)
+            tgdn.commit(inp.tree, dims, an[0], inp.k[l], ws[0][l], states[l], states[l], stream)
             if timed_kernels:
                 ev["c1"][l].record(stream)
+
+    def step_fused(r: int, timed_kernels=False):
+        inp, pr = inputs[r], (r - 1) % R
+        prev = inputs[pr]
+        tgdn.tree_prep(inp.tree, stream)
+        for l in range(L):
+            if timed_kernels:
+                ev["v0"][l].record(stream)
+            tgdn.verify_fused(inp.tree, dims, inp.q[l], inp.k[l], inp.v[l], inp.g[l], inp.b[l],
+                              states[l], outs[l], ws[r][l], prev.tree, an[pr], path[pr],
+                              prev.k[l], ws[pr][l], stream)
+            if timed_kernels:
+                ev["v1"][l].record(stream)
+        tgdn.accept(inp.tree, inp.draft, inp.target, an[r], al[r], path[r], stream)
+
+    def first_step(r: int):
+        """A plain verify + accept of input r, so that the step after it has a commit pending."""
+        inp = inputs[r]
+        tgdn.tree_prep(inp.tree, stream)
+        for l in range(L):
+            tgdn.verify(inp.tree, dims, inp.q[l], inp.k[l], inp.v[l], inp.g[l], inp.b[l],
+                        states[l], outs[l], ws[r][l], stream)
+        tgdn.accept(inp.tree, inp.draft, inp.target, an[r], al[r], path[r], stream)
+
+    step = step_fused if fused else step_separate
 
     # capture one graph per distinct step input
     graphs = []
     with torch.cuda.stream(stream):
-        for inp in inputs:        # warm the launch path before capture
-            step(inp)
+        if fused:
+            first_step(R - 1)
+        for r in range(R):        # warm the launch path before capture
+            step(r)
         stream.synchronize()
-        for inp in inputs:
+        for r in range(R):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                step(inp)
+                step(r)
             graphs.append(g)
+        if fused:                 # leave input R - 1 as the last step run
+            for r in range(R):
+                step(r)
     torch.cuda.synchronize()
-    launches_per_step = 1 + L + 1 + L
+    launches_per_step = (1 + L + 1) if fused else (1 + L + 1 + L)
 
     def barrier():
         if world > 1:
@@ -257,11 +299,15 @@ def run_gpu(args, rank, world, local):
     clocks = ClockSampler(local)
     clocks.start()
     torch.cuda.nvtx.range_push("timed")
+    # W + K replays from input 0 on; with W + K a multiple of R the last replay is input R - 1
+    K = args.steps
+    W = args.warmup + (-(args.warmup + K)) % R
+
     def replay(s):
         with torch.cuda.stream(stream):   # a graph replays on the current stream
             graphs[s % R].replay()
 
-    ms = timed(replay, args.steps, args.warmup)
+    ms = timed(replay, K, W)
     torch.cuda.nvtx.range_pop()
     clk = clocks.stop()
 
@@ -269,56 +315,70 @@ def run_gpu(args, rank, world, local):
     # A spin kernel first holds the stream so that all launches of the step are queued
     # before the GPU reaches them: they then run back to back, as in the graph.
     kv, kc = [], []
-    for s in range(max(3, min(args.steps, 8))):
+    for s in range(max(3, min(K, 8))):
+        r = s % R
         with torch.cuda.stream(stream):
             torch.cuda._sleep(50_000_000)
-            step(inputs[s % R], timed_kernels=True)
+            step(r, timed_kernels=True)
         stream.synchronize()
         kv += [ev["v0"][l].elapsed_time(ev["v1"][l]) for l in range(L)]
-        kc += [ev["c0"][l].elapsed_time(ev["c1"][l]) for l in range(L)]
+        if not fused:
+            kc += [ev["c0"][l].elapsed_time(ev["c1"][l]) for l in range(L)]
+    if fused and (max(3, min(K, 8)) % R):   # end again on input R - 1 (for the e2e leg)
+        with torch.cuda.stream(stream):
+            for r in range(max(3, min(K, 8)) % R, R):
+                step(r)
+        stream.synchronize()
     verify_us = 1e3 * statistics.mean(kv)
-    commit_us = 1e3 * statistics.mean(kc)
 
-    total_nodes = L * B * Nn * args.steps * world
+    total_nodes = L * B * Nn * K * world
     value = total_nodes / (ms / 1e3)
     hbm, peak_kind = peaks()
     verify_bytes = B * S0_BYTES_PER_SEQ + B * Nn * NODE_BYTES
     commit_bytes = 2 * B * S0_BYTES_PER_SEQ
-    v_gbs = verify_bytes / (verify_us * 1e-6) / 1e9
-    c_gbs = commit_bytes / (commit_us * 1e-6) / 1e9
-    if verify_us >= commit_us:
-        dom = dict(kernel="verify_tc_kernel", us=verify_us, bytes=verify_bytes, gbs=v_gbs)
-        other = dict(kernel="commit_kernel", us=commit_us, bytes=commit_bytes, gbs=c_gbs)
+    if fused:
+        # the fused pass also writes the committed state back (the path factors it reads,
+        # under 1% of the state, are not counted)
+        fv_bytes = verify_bytes + B * S0_BYTES_PER_SEQ
+        dom = dict(kernel="verify_tc_kernel (with the deferred commit)", us=verify_us,
+                   bytes=fv_bytes, gbs=fv_bytes / (verify_us * 1e-6) / 1e9)
+        other = None
     else:
-        dom = dict(kernel="commit_kernel", us=commit_us, bytes=commit_bytes, gbs=c_gbs)
-        other = dict(kernel="verify_tc_kernel", us=verify_us, bytes=verify_bytes, gbs=v_gbs)
+        commit_us = 1e3 * statistics.mean(kc)
+        v_gbs = verify_bytes / (verify_us * 1e-6) / 1e9
+        c_gbs = commit_bytes / (commit_us * 1e-6) / 1e9
+        vd = dict(kernel="verify_tc_kernel", us=verify_us, bytes=verify_bytes, gbs=v_gbs)
+        cd = dict(kernel="commit_kernel", us=commit_us, bytes=commit_bytes, gbs=c_gbs)
+        dom, other = (vd, cd) if verify_us >= commit_us else (cd, vd)
 
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, inputs, graphs, stream, an, al, path, timed, torch, R, L, B, Nn,
                       world)
 
+    step_desc = (f"prep + {L} verify with the previous step's commit folded in + accept"
+                 if fused else f"prep + {L} verify + accept + {L} in-place commit")
+    roof = {"bound": "hbm", "kernel": dom["kernel"], "achieved": dom["gbs"], "peak": hbm,
+            "peak_kind": peak_kind, "unit": "GB/s", "frac": dom["gbs"] / hbm, "traffic": None,
+            "algorithmic_bytes_per_launch": dom["bytes"], "launch_us": dom["us"]}
+    if other is not None:
+        roof["other"] = {"kernel": other["kernel"], "achieved": other["gbs"],
+                         "frac": other["gbs"] / hbm, "launch_us": other["us"],
+                         "algorithmic_bytes_per_launch": other["bytes"]}
     result = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{L}-layer GDN stack, B={B} per GPU, 64-node random trees "
                                f"(depth<=12), H_qk=16 H_v=32 d=128, 50-step decode",
                    "layers": L, "batch_per_gpu": B, "nodes_per_tree": Nn, "depth_max": 12,
                    "H_qk": 16, "H_v": 32, "d_k": 128, "d_v": 128, "io": "bf16",
-                   "state": "fp32", "accumulate": "fp32",
-                   "step": f"prep + {L} verify + accept + {L} in-place commit (CUDA graph)",
+                   "state": "fp32", "accumulate": "fp32", "mode": args.mode,
+                   "step": f"{step_desc} (CUDA graph)",
                    "l2": "inputs larger than L2 (~9 GB touched per step, L2 129 MB)",
                    "distinct_step_inputs": R, "parallelism": f"dp{world} (sequences)"},
-        "roofline": {"bound": "hbm", "kernel": dom["kernel"], "achieved": dom["gbs"],
-                     "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": dom["gbs"] / hbm, "traffic": None,
-                     "algorithmic_bytes_per_launch": dom["bytes"],
-                     "launch_us": dom["us"],
-                     "other": {"kernel": other["kernel"], "achieved": other["gbs"],
-                               "frac": other["gbs"] / hbm, "launch_us": other["us"],
-                               "algorithmic_bytes_per_launch": other["bytes"]}},
-        "gpu_launches": launches_per_step * (args.steps),
+        "roofline": roof,
+        "gpu_launches": launches_per_step * K,
         "clocks": clk,
     }
     if e2e is not None:
@@ -328,21 +388,23 @@ def run_gpu(args, rank, world, local):
 
 def run_e2e(args, inputs, graphs, stream, an, al, path, timed, torch, R, L, B, Nn, world):
     """Same step, but each step's inputs come from pinned host memory and the accepted
-    paths go back to the host, inside the timed region."""
+    paths go back to the host, inside the timed region.  an/al/path: the acceptance
+    outputs per input (one shared set when there is a single one)."""
     host = []
     for inp in inputs:
         host.append([t.detach().to("cpu").pin_memory() for t in inp.tensors()])
-    res_host = [torch.empty_like(x, device="cpu").pin_memory() for x in (an, al, path)]
+    res_host = [torch.empty_like(x, device="cpu").pin_memory() for x in (an[0], al[0], path[0])]
     h2d = sum(t.numel() * t.element_size() for t in host[0])
     d2h = sum(t.numel() * t.element_size() for t in res_host)
 
     def fn(s):
         r = s % R
+        a = r if len(an) > 1 else 0
         with torch.cuda.stream(stream):
             for dst, src in zip(inputs[r].tensors(), host[r]):
                 dst.copy_(src, non_blocking=True)
             graphs[r].replay()
-            for dst, src in zip(res_host, (an, al, path)):
+            for dst, src in zip(res_host, (an[a], al[a], path[a])):
                 dst.copy_(src, non_blocking=True)
 
     ms = timed(fn, args.steps, args.warmup)

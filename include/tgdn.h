@@ -198,6 +198,34 @@ int tgdn_commit(const tgdn_tree* tree, const tgdn_dims* dims, const int32_t* acc
                 const void* k, const void* ws, const float* S_in, float* S_out,
                 tgdn_stream_t stream);
 
+/* One decode step with the previous step's commit deferred into it
+ * (Methodik 3, last bullet: the state is committed in the next decoding
+ * iteration, once the accepted branch is known).  Equivalent to
+ *   tgdn_commit(prev_tree, dims, prev_accept_node, prev_k, prev_ws, S, S);
+ *   tgdn_verify(tree, dims, q, k, v, g, b, S, o, ws);
+ * but, on the tensor-core path, each state block is read once, updated in
+ * registers, written back once and verified from the same registers, so the
+ * state crosses HBM once per direction per step instead of three times.
+ *   S              [B][H_v][d_k][d_v] fp32: on entry the state the previous
+ *                  step verified from; on return the committed state (the S0
+ *                  of this step's verification)
+ *   prev_tree      the previous step's tree (same B, prep'd, unchanged since)
+ *   prev_accept_node, prev_path  the previous step's tgdn_accept outputs
+ *                  ([B] and [B][prev_tree->depth_max + 1])
+ *   prev_k         the previous step's k
+ *   prev_ws        the previous step's verify workspace; it must not overlap
+ *                  ws (alternate two workspaces step after step)
+ * Other arguments as tgdn_verify.  Sequences whose previous tree was empty or
+ * invalid keep their state.  The tensor-core path needs what tgdn_verify's
+ * needs plus prev_tree->depth_max <= 30; other cases run the two passes.
+ * The last step of a decode still needs its own tgdn_commit.
+ * Returns TGDN_OK, TGDN_EINVAL, TGDN_ETOOBIG or TGDN_ECUDA. */
+int tgdn_verify_fused(const tgdn_tree* tree, const tgdn_dims* dims, const void* q,
+                      const void* k, const void* v, const float* g, const float* b, float* S,
+                      void* o, void* ws, const tgdn_tree* prev_tree,
+                      const int32_t* prev_accept_node, const int32_t* prev_path,
+                      const void* prev_k, const void* prev_ws, tgdn_stream_t stream);
+
 /* Verification for callers that cannot allocate device memory.
  *
  * The paper has no counterpart to this call; it exists for integrators.  Some

@@ -48,8 +48,10 @@ def upload(p: synth.Problem, device="cuda", n_max=None, depth_max=None):
     tree = tgdn.Tree.from_host(p.trees.cu_nodes, p.trees.parent,
                                n_max or p.trees.n_max, depth_max if depth_max is not None
                                else p.trees.depth_max, device)
-    dims = tgdn.Dims(cfg.H_qk, cfg.H_v, cfg.dk, cfg.dv, tgdn.BF16 if cfg.io == "bf16" else tgdn.F32)
     i = p.inputs
+    # head counts from the tensors themselves (a head subset keeps the workload's cfg)
+    dims = tgdn.Dims(i.q.shape[1], i.v.shape[1], cfg.dk, cfg.dv,
+                     tgdn.BF16 if cfg.io == "bf16" else tgdn.F32)
     f32 = lambda x: torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(device)
     dev = dict(q=to_device_io(i.q, cfg.io, device), k=to_device_io(i.k, cfg.io, device),
                v=to_device_io(i.v, cfg.io, device), g=f32(i.g), b=f32(i.b), S0=f32(p.S0),

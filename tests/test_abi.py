@@ -149,3 +149,26 @@ def test_product_path_does_not_reach_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in text.lower(), f
     assert "oracle" not in open(os.path.join(ROOT, "include", "tgdn.h")).read().lower()
+
+
+def test_verify_fused_rejects_bad_arguments(L):
+    """Host checks of tgdn_verify_fused: batch sizes must match, the two workspaces must not
+    overlap and both must be 256-byte aligned (nothing is launched)."""
+    d = cdims()
+    t, pt = ctree(B=2, T=10), ctree(B=2, T=10)
+    f = L.tgdn_verify_fused
+    ws, pws = FAKE * 16, FAKE * 64
+
+    def call(t, pt, ws, pws):
+        return f(ctypes.byref(t), ctypes.byref(d), *([FAKE] * 7), ws, ctypes.byref(pt),
+                 FAKE, FAKE, FAKE, pws, None)
+
+    assert call(t, ctree(B=3, T=10), ws, pws) == tgdn.EINVAL      # different batch
+    assert call(t, pt, ws, ws) == tgdn.EINVAL                       # same workspace
+    assert call(t, pt, ws, ws + 256) == tgdn.EINVAL                 # overlapping workspaces
+    assert call(t, pt, ws + 16, pws) == tgdn.EINVAL                 # misaligned
+    assert call(t, pt, ws, pws + 16) == tgdn.EINVAL
+    assert f(ctypes.byref(t), ctypes.byref(d), *([FAKE] * 7), ws, None, FAKE, FAKE, FAKE, pws,
+             None) == tgdn.EINVAL                                   # no previous tree
+    assert f(ctypes.byref(t), ctypes.byref(d), *([FAKE] * 7), ws, ctypes.byref(pt), None,
+             FAKE, FAKE, pws, None) == tgdn.EINVAL                  # no accepted nodes

@@ -110,9 +110,66 @@ int tgdn_verify(const tgdn_tree* tree, const tgdn_dims* dims, const void* q, con
     CUtensorMap qmap, kmap;
     if (!encode_qk_map(&qmap, q, t.T, d.H_qk) || !encode_qk_map(&kmap, k, t.T, d.H_qk))
       return TGDN_ECUDA;  // the driver could not describe q/k for TMA
-    return from_cuda(tgdn::launch_verify_tc(t, d, qmap, kmap, v, g, b, S0, o, U, G, s));
+    const tgdn::PendingCommit none{};
+    return from_cuda(tgdn::launch_verify_tc(t, d, qmap, kmap, v, g, b, const_cast<float*>(S0), o,
+                                            U, G, none, s));
   }
   return from_cuda(tgdn::launch_verify_simt(t, d, q, k, v, g, b, S0, o, U, G, s));
+}
+
+int tgdn_verify_fused(const tgdn_tree* tree, const tgdn_dims* dims, const void* q,
+                      const void* k, const void* v, const float* g, const float* b, float* S,
+                      void* o, void* ws, const tgdn_tree* prev_tree,
+                      const int32_t* prev_accept_node, const int32_t* prev_path,
+                      const void* prev_k, const void* prev_ws, tgdn_stream_t stream) {
+  int rc = check_tree(tree);
+  if (rc != TGDN_OK) return rc;
+  rc = check_tree(prev_tree);
+  if (rc != TGDN_OK) return rc;
+  rc = check_dims(dims);
+  if (rc != TGDN_OK) return rc;
+  const tgdn_tree& t = *tree;
+  const tgdn_tree& pt = *prev_tree;
+  const tgdn_dims& d = *dims;
+  if (pt.B != t.B) return TGDN_EINVAL;  // the same sequences, step after step
+  if (t.T > 0 && (!q || !k || !v || !g || !b || !o || !ws)) return TGDN_EINVAL;
+  if (t.B > 0 && (!S || !prev_accept_node || !prev_path)) return TGDN_EINVAL;
+  if (pt.T > 0 && (!prev_k || !prev_ws)) return TGDN_EINVAL;
+  if (reinterpret_cast<uintptr_t>(ws) % 256 != 0 ||
+      reinterpret_cast<uintptr_t>(prev_ws) % 256 != 0)
+    return TGDN_EINVAL;
+  if (t.B == 0) return TGDN_OK;
+  const WsLayout L = tgdn::ws_layout(t, d);
+  const WsLayout PL = tgdn::ws_layout(pt, d);
+  if (t.T > 0 && pt.T > 0) {  // this step's factors must not overwrite the pending ones
+    const char* a = static_cast<const char*>(ws);
+    const char* c = static_cast<const char*>(prev_ws);
+    if (a < c + PL.bytes && c < a + L.bytes) return TGDN_EINVAL;
+  }
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const float* pU = pt.T > 0 ? reinterpret_cast<const float*>(
+                                   static_cast<const char*>(prev_ws) + PL.u_off)
+                             : nullptr;
+  const float* pG = pt.T > 0 ? reinterpret_cast<const float*>(
+                                   static_cast<const char*>(prev_ws) + PL.g_off)
+                             : nullptr;
+  if (t.T > 0 && pt.T > 0 && tgdn::verify_tc_supported(t, d, q, k, v, S, o) &&
+      tgdn::pending_commit_tc_supported(pt, prev_k)) {
+    CUtensorMap qmap, kmap;
+    if (!encode_qk_map(&qmap, q, t.T, d.H_qk) || !encode_qk_map(&kmap, k, t.T, d.H_qk))
+      return TGDN_ECUDA;
+    float* U = reinterpret_cast<float*>(static_cast<char*>(ws) + L.u_off);
+    float* G = reinterpret_cast<float*>(static_cast<char*>(ws) + L.g_off);
+    const tgdn::PendingCommit cm{pt.cu_nodes, pt.status, prev_path, pt.depth_max + 1,
+                                 prev_k,      pU,        pG};
+    return from_cuda(tgdn::launch_verify_tc(t, d, qmap, kmap, v, g, b, S, o, U, G, cm, s));
+  }
+  // any other case: the commit as its own pass, then the verify
+  if (pt.T > 0) {
+    rc = from_cuda(tgdn::launch_commit(pt, d, prev_accept_node, prev_k, pU, pG, S, S, s));
+    if (rc != TGDN_OK) return rc;
+  }
+  return tgdn_verify(tree, dims, q, k, v, g, b, S, o, ws, stream);
 }
 
 int tgdn_verify_recurrent(const tgdn_tree* tree, const tgdn_dims* dims, const void* q,

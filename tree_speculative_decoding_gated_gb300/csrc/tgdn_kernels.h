@@ -33,13 +33,30 @@ cudaError_t launch_verify_simt(const tgdn_tree& t, const tgdn_dims& d, const voi
                                const void* k, const void* v, const float* g, const float* b,
                                const float* S0, void* o, float* U, float* G, cudaStream_t s);
 
+// The previous decode step's commit, folded into this step's verify: the
+// accepted root path of every sequence and the factors of that step.
+// path == nullptr means there is nothing to commit.
+struct PendingCommit {
+  const int32_t* cu;      // previous tree: cu_nodes [B + 1]
+  const int32_t* status;  // previous tree: status [B]
+  const int32_t* path;    // [B][path_len] accepted root path, root first, -1 padded
+  int path_len;           // previous depth_max + 1
+  const void* k;          // previous keys [T'][H_qk][d_k] (bf16)
+  const float* U;         // previous factors [T'][H_v][d_v]
+  const float* G;         // previous path-cumulative log-gates [T'][H_v]
+};
+
 // Tensor-core verify: bf16 io, d_k = d_v = 128, n_max <= 64, depth_max <= 30.
 bool verify_tc_supported(const tgdn_tree& t, const tgdn_dims& d, const void* q, const void* k,
                          const void* v, const float* S0, const void* o);
+// Whether the tensor-core verify can also apply a pending commit of `prev`.
+bool pending_commit_tc_supported(const tgdn_tree& prev, const void* prev_k);
+// With cm.path set, S is first updated in place by the pending commit and the
+// committed state is verified; otherwise S is only read.
 cudaError_t launch_verify_tc(const tgdn_tree& t, const tgdn_dims& d, const CUtensorMap& qmap,
                              const CUtensorMap& kmap, const void* v, const float* g,
-                             const float* b, const float* S0, void* o, float* U, float* G,
-                             cudaStream_t s);
+                             const float* b, float* S, void* o, float* U, float* G,
+                             const PendingCommit& cm, cudaStream_t s);
 
 // Per-branch recurrent verification (every root-to-leaf path replayed from S0).
 cudaError_t launch_verify_recurrent(const tgdn_tree& t, const tgdn_dims& d, const void* q,

@@ -30,6 +30,16 @@
 //     key lanes store U (workspace), query lanes O = e^G Q S0 + W R (bf16).
 // The halves hand over through mbarriers: "stage 1 done" (the first product's
 // completion plus the producer's metadata) and "TMEM half free".
+//
+// Deferred commit folded into the next verify (Methodik 3, last bullet: the
+// state is committed once the accepted branch is known, in the following
+// decode iteration).  When the previous step left a commit pending, the
+// producer stages that step's accepted path for the item (u_s rows and k_s
+// rows by bulk copy, coefficients e^{G*-G_s}) while the item's state is being
+// prefetched, then forms
+//   S = e^{G*} S_prev + sum_{s on the path} e^{G*-G_s} k_s u_s^T
+// in registers, writes it back in place (the committed state) and verifies
+// from it.  The state then crosses HBM once in each direction per step.
 #include "tgdn_device.cuh"
 #include "tgdn_kernels.h"
 
@@ -56,6 +66,9 @@ constexpr int kOffRlo = 147456;
 constexpr int kOffA2hi = 163840;  // [T; W] operand, K-major [16 row groups][8][128 B]     16 KiB
 constexpr int kOffA2lo = 180224;
 constexpr int kOffSS = 196608;    // path-solve scratch [128 rows][kTcPath] fp32
+// Pending-commit staging, inside the S0 operand area (free between items):
+constexpr int kOffUP = kOffS0hi;          // u_s rows [kTcPath][128] fp32        15.5 KiB
+constexpr int kOffKP = kOffS0hi + 16384;  // k_s rows [kTcPath][128] bf16        7.75 KiB
 constexpr int kOffMeta = kOffSS + 128 * kTcPath * 4;
 
 struct ItemMeta {
@@ -72,9 +85,14 @@ struct TcShared {
   uint64_t tma_bar, mma1_bar, mma2_bar;
   uint64_t s1_done[2];    // consumer waits: first product done + metadata written
   uint64_t tmem_free[2];  // producer waits: consumer finished the item in this half
+  uint64_t cbar;          // pending-commit staging of the next item has landed
   uint32_t tmem_slot;
   int abort;
   int tma_issued;
+  int c_issued;           // pending-commit stagings issued
+  int c_L;                // staged path length (0: nothing to commit)
+  float c_decay;          // e^{G*}
+  float c_coef[kTcPath];  // e^{G* - G_s} along the staged path
   ItemMeta meta[2];
 };
 constexpr int kTcSmemBytes = kOffMeta + (int)sizeof(TcShared) + 1024;  // + alignment slack
@@ -126,9 +144,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                  const int32_t* __restrict__ depth, const int32_t* __restrict__ order,
                  const int32_t* __restrict__ pos, const uint64_t* __restrict__ anc,
                  int32_t* __restrict__ status, const __nv_bfloat16* __restrict__ v,
-                 const float* __restrict__ g, const float* __restrict__ bta,
-                 const float* __restrict__ S0, __nv_bfloat16* __restrict__ o,
-                 float* __restrict__ Uws, float* __restrict__ Gws) {
+                 const float* __restrict__ g, const float* __restrict__ bta, float* S,
+                 __nv_bfloat16* __restrict__ o, float* __restrict__ Uws,
+                 float* __restrict__ Gws, const PendingCommit cm) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -138,6 +156,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
   if ((int)blockIdx.x >= n_items) return;
   const int stride = gridDim.x;
   const int grp = H_v / H_qk;  // v-heads per query/key head
+  const bool fused = cm.path != nullptr;
 
   if (tid == 0) {
     mbar_init(&sh.tma_bar, 1);
@@ -147,10 +166,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     mbar_init(&sh.s1_done[1], 2);
     mbar_init(&sh.tmem_free[0], 1);
     mbar_init(&sh.tmem_free[1], 1);
+    mbar_init(&sh.cbar, 1);
     fence_mbar_init();
     fence_proxy_async_smem();
     sh.abort = 0;
     sh.tma_issued = 0;
+    sh.c_issued = 0;
   }
   if (warp == 0) tmem_alloc(&sh.tmem_slot, kTmemCols);
   tc_fence_before_sync();
@@ -173,13 +194,47 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       sh.tma_issued += 1;
     };
     // S0 of one item: thread p holds rows (p >> 5) + 8 r, float4 column p & 31
+    // (plain loads: with a pending commit the kernel writes these rows back)
     const int srow0 = p >> 5, sq = p & 31;
     float4 sreg[16];
     auto load_s0 = [&](int item) {
-      const float* src = S0 + (size_t)item * kTcDK * kTcDV;  // item = bi * H_v + h
+      const float* src = S + (size_t)item * kTcDK * kTcDV;  // item = bi * H_v + h
 #pragma unroll
       for (int r = 0; r < 16; ++r)
-        sreg[r] = __ldg(reinterpret_cast<const float4*>(src + (size_t)(srow0 + 8 * r) * kTcDV) + sq);
+        sreg[r] = reinterpret_cast<const float4*>(src + (size_t)(srow0 + 8 * r) * kTcDV)[sq];
+    };
+    // Warp 0: stage the pending commit of one item (its accepted path in the
+    // previous tree; entries after the first invalid one are ignored).
+    auto stage_commit = [&](int it) {
+      const int bi = it / H_v, h = it % H_v, qh = h / grp;
+      const int lane = p;
+      const int plo = cm.cu[bi], pN = cm.cu[bi + 1] - plo;
+      int node = -1;
+      if (lane < cm.path_len) node = cm.path[(size_t)bi * cm.path_len + lane];
+      const bool valid = cm.status[bi] == TGDN_SEQ_OK && lane < cm.path_len && node >= 0 &&
+                         node < pN;
+      const int L = __ffs(__ballot_sync(0xffffffffu, !valid)) - 1;  // path_len <= 31
+      float Gl = 0.f;
+      if (lane < L) Gl = cm.G[(size_t)(plo + node) * H_v + h];
+      const float Gstar = __shfl_sync(0xffffffffu, Gl, L > 0 ? L - 1 : 0);
+      if (lane < L) sh.c_coef[lane] = __expf(Gstar - Gl);
+      if (lane == 0) {
+        sh.c_L = L;
+        sh.c_decay = L > 0 ? __expf(Gstar) : 1.f;
+        sh.c_issued += 1;
+      }
+      __syncwarp();
+      if (lane == 0)
+        mbar_arrive_expect_tx(&sh.cbar, static_cast<uint32_t>(L) * (kTcDV * 4 + kTcDK * 2));
+      __syncwarp();
+      if (lane < L) {
+        const size_t row = (size_t)(plo + node);
+        bulk_copy_g2s(smem + kOffUP + lane * (kTcDV * 4), cm.U + (row * H_v + h) * kTcDV,
+                      kTcDV * 4, &sh.cbar);
+        bulk_copy_g2s(smem + kOffKP + lane * (kTcDK * 2),
+                      static_cast<const __nv_bfloat16*>(cm.k) + (row * H_qk + qh) * kTcDK,
+                      kTcDK * 2, &sh.cbar);
+      }
     };
     Prefetch pf;
     auto load_meta = [&](int item) {
@@ -200,6 +255,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     if (p == 0) issue_kq(item);
     load_meta(item);
     load_s0(item);
+    if (fused && p < 32) stage_commit(item);
 
     for (int j = 0; item < n_items; ++j, item += stride) {
       const int slot = j & 1;
@@ -228,6 +284,41 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         M.gg[p] = pf.gg;
         M.bb[p] = pf.bb;
         if (v_ok) my_anc = anc[lo + pf.pos];  // one 64-bit word: n_max <= 64
+      }
+      if (fused) {
+        // the previous step's commit: S = e^{G*} S + sum_l e^{G*-G_l} k_l u_l^T,
+        // written back in place; the committed state is what gets verified
+        if (!group_wait(&sh.cbar, j & 1, kBarP, p == 0, abort)) break;
+        const int L = sh.c_L;
+        if (L > 0) {
+          const float decay = sh.c_decay;
+          const float* UP = reinterpret_cast<const float*>(smem + kOffUP);
+          const __nv_bfloat16* KP = reinterpret_cast<const __nv_bfloat16*>(smem + kOffKP);
+#pragma unroll
+          for (int r = 0; r < 16; ++r) {
+            sreg[r].x *= decay;
+            sreg[r].y *= decay;
+            sreg[r].z *= decay;
+            sreg[r].w *= decay;
+          }
+          for (int l = 0; l < L; ++l) {
+            const float4 u = reinterpret_cast<const float4*>(UP + l * kTcDV)[sq];
+            const float cl = sh.c_coef[l];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+              const float kv = cl * __bfloat162float(KP[l * kTcDK + srow0 + 8 * r]);
+              sreg[r].x = fmaf(kv, u.x, sreg[r].x);
+              sreg[r].y = fmaf(kv, u.y, sreg[r].y);
+              sreg[r].z = fmaf(kv, u.z, sreg[r].z);
+              sreg[r].w = fmaf(kv, u.w, sreg[r].w);
+            }
+          }
+          float* dst = S + (size_t)item * kTcDK * kTcDV;
+#pragma unroll
+          for (int r = 0; r < 16; ++r)
+            reinterpret_cast<float4*>(dst + (size_t)(srow0 + 8 * r) * kTcDV)[sq] = sreg[r];
+        }
+        named_sync(kBarP, kGroup);  // staging read; the operand may overwrite it
       }
       // S0 registers -> bf16 hi/lo operand (the previous product has completed)
 #pragma unroll
@@ -317,6 +408,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       }
       if (!named_sync_and(kBarP, kGroup, step_ok && !*abort)) break;
       if (p == 0 && next < n_items) issue_kq(next);
+      // the S0 operand area is free again: stage the next item's pending commit
+      if (fused && p < 32 && next < n_items) stage_commit(next);
     }
   } else {
     // =================================================== consumer warps 8-15
@@ -545,12 +638,17 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     for (int it2 = blockIdx.x; it2 < n_items; it2 += stride)
       atomicCAS(&status[it2 / H_v], TGDN_SEQ_OK, TGDN_SEQ_TIMEOUT);
     if (sh.tma_issued > 0) (void)mbar_wait(&sh.tma_bar, (sh.tma_issued - 1) & 1);
+    if (sh.c_issued > 0) (void)mbar_wait(&sh.cbar, (sh.c_issued - 1) & 1);
   }
   __syncthreads();
   if (warp == 0) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+bool pending_commit_tc_supported(const tgdn_tree& prev, const void* prev_k) {
+  return prev.depth_max + 1 <= kTcPath && (reinterpret_cast<uintptr_t>(prev_k) % 16) == 0;
 }
 
 bool verify_tc_supported(const tgdn_tree& t, const tgdn_dims& d, const void* q, const void* k,
@@ -576,8 +674,8 @@ static int sm_count() {
 
 cudaError_t launch_verify_tc(const tgdn_tree& t, const tgdn_dims& d, const CUtensorMap& qmap,
                              const CUtensorMap& kmap, const void* v, const float* g,
-                             const float* b, const float* S0, void* o, float* U, float* G,
-                             cudaStream_t s) {
+                             const float* b, float* S, void* o, float* U, float* G,
+                             const PendingCommit& cm, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(verify_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
   if (e != cudaSuccess) return e;
@@ -588,8 +686,8 @@ cudaError_t launch_verify_tc(const tgdn_tree& t, const tgdn_dims& d, const CUten
   const int grid = (int)(items < sms ? items : sms);
   verify_tc_kernel<<<grid, kTcThreads, kTcSmemBytes, s>>>(
       qmap, kmap, (int)items, d.H_qk, d.H_v, t.depth_max, t.cu_nodes, t.depth, t.order, t.pos,
-      t.anc, t.status, static_cast<const __nv_bfloat16*>(v), g, b, S0,
-      static_cast<__nv_bfloat16*>(o), U, G);
+      t.anc, t.status, static_cast<const __nv_bfloat16*>(v), g, b, S,
+      static_cast<__nv_bfloat16*>(o), U, G, cm);
   return cudaGetLastError();
 }
 

@@ -72,6 +72,9 @@ def lib() -> ctypes.CDLL:
         L.tgdn_verify_recurrent.restype = ctypes.c_int
         L.tgdn_verify_noalloc.argtypes = [P(CTree), P(CDims), vp, vp, vp, vp, vp, vp, vp, st]
         L.tgdn_verify_noalloc.restype = ctypes.c_int
+        L.tgdn_verify_fused.argtypes = [P(CTree), P(CDims), vp, vp, vp, vp, vp, vp, vp, vp,
+                                        P(CTree), vp, vp, vp, vp, st]
+        L.tgdn_verify_fused.restype = ctypes.c_int
         L.tgdn_status_string.argtypes = [i32]
         L.tgdn_status_string.restype = ctypes.c_char_p
         L.tgdn_version.argtypes = []
@@ -197,6 +200,27 @@ def verify(tree: Tree, dims: Dims, q, k, v, g, b, S0, o, ws, stream=None) -> Non
             _dev(ws, torch.uint8, verify_workspace_bytes(tree, dims), "ws"))
     _check(lib().tgdn_verify(ctypes.byref(ct), ctypes.byref(cd), *args, _stream(stream)),
            "tgdn_verify")
+
+
+def verify_fused(tree: Tree, dims: Dims, q, k, v, g, b, S, o, ws, prev_tree: Tree,
+                 prev_accept_node, prev_path, prev_k, prev_ws, stream=None) -> None:
+    """tgdn_verify_fused: commit the previous step's accepted node into S (in place),
+    then verify this step's tree from the committed state."""
+    T, B = tree.T, tree.B
+    io = dims.torch_dtype
+    ct, cd, pt = tree.c(), dims.c(), prev_tree.c()
+    args = (_dev(q, io, T * dims.H_qk * dims.d_k, "q"), _dev(k, io, T * dims.H_qk * dims.d_k, "k"),
+            _dev(v, io, T * dims.H_v * dims.d_v, "v"), _dev(g, torch.float32, T * dims.H_v, "g"),
+            _dev(b, torch.float32, T * dims.H_v, "b"),
+            _dev(S, torch.float32, B * dims.H_v * dims.d_k * dims.d_v, "S"),
+            _dev(o, io, T * dims.H_v * dims.d_v, "o"),
+            _dev(ws, torch.uint8, verify_workspace_bytes(tree, dims), "ws"))
+    prev = (_dev(prev_accept_node, torch.int32, prev_tree.B, "prev_accept_node"),
+            _dev(prev_path, torch.int32, prev_tree.B * (prev_tree.depth_max + 1), "prev_path"),
+            _dev(prev_k, io, prev_tree.T * dims.H_qk * dims.d_k, "prev_k"),
+            _dev(prev_ws, torch.uint8, verify_workspace_bytes(prev_tree, dims), "prev_ws"))
+    _check(lib().tgdn_verify_fused(ctypes.byref(ct), ctypes.byref(cd), *args, ctypes.byref(pt),
+                                   *prev, _stream(stream)), "tgdn_verify_fused")
 
 
 def verify_recurrent(tree: Tree, dims: Dims, q, k, v, g, b, S0, o, stream=None) -> None:
