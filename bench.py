@@ -61,6 +61,10 @@ def parse():
                     help="GDN layers per step (fewer only for small profiler captures)")
     ap.add_argument("--mode", default="fused", choices=["fused", "separate"],
                     help="fused: commit folded into the next step's verify; separate: own pass")
+    ap.add_argument("--part", default="stack", choices=["stack", "recurrent", "build"],
+                    help="stack: the decode benchmark (default); recurrent: single-pass verify "
+                         "vs per-branch recurrent verify by tree size; build: top-w tree "
+                         "construction kernel times")
     return ap.parse_args()
 
 
@@ -488,9 +492,112 @@ def run_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+def _flush_l2(buf):
+    buf.add_(1)          # 256 MiB written: nothing of the previous launch stays in L2
+
+
+def _launch_times(torch, stream, fn, iters, flush):
+    """Per-launch device times (us) with L2 flushed before every launch."""
+    ts = []
+    for _ in range(iters):
+        with torch.cuda.stream(stream):
+            _flush_l2(flush)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        stream.synchronize()
+        ts.append(1e3 * e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
+def run_recurrent_compare(args):
+    """Single-pass tree verification (tgdn_verify) against per-branch recurrent verification
+    (tgdn_verify_recurrent) on one GDN layer, by tree size: the pages' comparison at tree
+    size 128 (7.1x on a B200)."""
+    import torch
+    from tree_speculative_decoding_gated_gb300 import tgdn
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    cfg = synth.CONFIGS["cfg3"]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(synth.BASE_SEED + 77)
+    stream = torch.cuda.Stream(dev)
+    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    dims = tgdn.Dims(cfg.H_qk, cfg.H_v, cfg.dk, cfg.dv, tgdn.BF16)
+    B = 16
+    rng = np.random.default_rng(synth.BASE_SEED + 78)
+    cases = [("random", n, 16) for n in (16, 32, 64)] + [("random", 128, 16), ("top-8", 129, 16)]
+    out = []
+    for kind, n, dcap in cases:
+        if kind == "top-8":
+            parents = [synth.top_m_tree(rng, 8, 16) for _ in range(B)]
+        else:
+            parents = [synth.random_recursive_tree(rng, n, dcap) for _ in range(B)]
+        trees = synth.pack_trees(parents, max(len(p) for p in parents), dcap)
+        tree = tgdn.Tree.from_host(trees.cu_nodes, trees.parent, trees.n_max, trees.depth_max,
+                                   dev)
+        q, k, v, g, b = synth.make_node_inputs_device(cfg, trees.T, gen, dev)
+        S0 = synth.make_state_device(cfg, B, gen, dev)
+        o = torch.empty((trees.T, cfg.H_v, cfg.dv), dtype=torch.bfloat16, device=dev)
+        ws = tgdn.alloc_workspace(tree, dims, dev)
+        with torch.cuda.stream(stream):
+            tgdn.tree_prep(tree, stream)
+        f_single = lambda: tgdn.verify(tree, dims, q, k, v, g, b, S0, o, ws, stream)
+        f_rec = lambda: tgdn.verify_recurrent(tree, dims, q, k, v, g, b, S0, o, stream)
+        for f in (f_single, f_rec):
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    f()
+        t1 = _launch_times(torch, stream, f_single, 20, flush)
+        t2 = _launch_times(torch, stream, f_rec, 20, flush)
+        kern = "verify_tc_kernel" if trees.n_max <= 64 else "verify_simt_kernel"
+        out.append({"tree": kind, "nodes": int(trees.n_max), "depth_max": dcap, "B": B,
+                    "single_pass_us": t1, "single_pass_kernel": kern, "recurrent_us": t2,
+                    "ratio": t2 / t1})
+    return {"part": "recurrent", "metric": "per-branch recurrent time / single-pass time, "
+            "one GDN layer (H_qk=16, H_v=32, d=128, bf16), L2 flushed before every launch",
+            "unit": "x", "higher_is_better": True, "cases": out,
+            "pages": "7.1x at tree size 128 on a B200 (Experimentelle Ergebnisse)"}
+
+
+def run_build_times(args):
+    """Top-w best-first tree construction (tgdn_tree_build): kernel time per batch."""
+    import torch
+    from tree_speculative_decoding_gated_gb300 import tgdn
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(dev)
+    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    out = []
+    for B, budget, K, w, dmax in [(32, 64, 8, 1, 12), (32, 64, 8, 4, 12), (32, 64, 8, 8, 12),
+                                  (32, 64, 8, 16, 12), (32, 128, 8, 8, 16),
+                                  (32, 256, 16, 16, 30), (256, 64, 8, 8, 12)]:
+        root, logp, tok = synth.make_build_tables(B, budget, K, seed=budget + w)
+        d = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+        r, lp, tk = d(root), d(logp), d(tok)
+        res = tgdn.tree_build(r, lp, tk, budget, w, dmax, stream=stream)
+        fn = lambda: tgdn.tree_build(r, lp, tk, budget, w, dmax, out=res, stream=stream)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+        t = _launch_times(torch, stream, fn, 20, flush)
+        rounds = int(res["rounds"].max().item())
+        out.append({"B": B, "budget": budget, "K": K, "w": w, "depth_max": dmax, "us": t,
+                    "rounds": rounds, "us_per_round": t / max(rounds, 1)})
+    return {"part": "build", "metric": "tgdn_tree_build kernel time per batch (one warp per "
+            "sequence; latency bound)", "unit": "us", "higher_is_better": False, "cases": out}
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
+    if args.part != "stack":
+        if rank == 0:
+            fn = run_recurrent_compare if args.part == "recurrent" else run_build_times
+            print(json.dumps(fn(args)), flush=True)
+        return
     if args.impl == "reference":
         res = run_reference(args, rank, world)
         if res is not None:

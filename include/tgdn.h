@@ -171,6 +171,35 @@ int tgdn_verify_recurrent(const tgdn_tree* tree, const tgdn_dims* dims, const vo
                           const void* k, const void* v, const float* g, const float* b,
                           const float* S0, void* o, tgdn_stream_t stream);
 
+/* Draft-tree construction by top-w parallel best-first expansion (Methodik 2,
+ * "Baumerstellung": the w best candidates are taken from the candidate heap
+ * and expanded together, so B nodes take about B / w sequential steps).
+ * For each sequence b, slot 0 is the root (root_token[b], score 0, depth 0).
+ * Each round takes the min(w, budget - size) best candidates (fewer if none
+ * are left), gives them the next slots in order of priority, then, unless the
+ * tree is full, expands them: the node in slot i offers its K continuations
+ * child_token[b][i][r] with priority score[i] + child_logp[b][i][r] (one fp32
+ * addition; the path log-probability), except beyond depth_max.  Ties go to
+ * the smaller id i * K + r.  Row i of the tables is the drafter's output for
+ * the node in slot i (rows of slots the tree never reaches are not read).
+ *   root_token  [B] int32
+ *   child_logp  [B][budget][K] fp32, finite
+ *   child_token [B][budget][K] int32
+ *   parent, token, depth [B][budget] int32 out: parent slot (-1 for the root),
+ *               token, depth; -1 in the slots past n_nodes[b]
+ *   score       [B][budget] fp32 out: path log-probability (0 past n_nodes[b])
+ *   n_nodes     [B] int32 out: tree size (budget unless candidates ran out)
+ *   rounds      [B] int32 out: rounds that took at least one candidate
+ * Parents precede children, so parent[b][0:n_nodes[b]] is a tree tgdn_tree_prep
+ * takes as is.  1 <= budget <= TGDN_MAX_NODES, 1 <= K <= TGDN_BUILD_MAX_K,
+ * w >= 1, 0 <= depth_max <= TGDN_MAX_DEPTH.
+ * Returns TGDN_OK, TGDN_EINVAL, TGDN_ETOOBIG or TGDN_ECUDA. */
+#define TGDN_BUILD_MAX_K 16
+int tgdn_tree_build(int32_t B, int32_t budget, int32_t K, int32_t w, int32_t depth_max,
+                    const int32_t* root_token, const float* child_logp,
+                    const int32_t* child_token, int32_t* parent, int32_t* token, float* score,
+                    int32_t* depth, int32_t* n_nodes, int32_t* rounds, tgdn_stream_t stream);
+
 /* Greedy acceptance (Experimentelle Ergebnisse, mean acceptance length).  The
  * root is always accepted; a non-root node is accepted when it and every
  * non-root node on its root path satisfy target_ids == draft_ids.  The

@@ -187,6 +187,22 @@ int tgdn_verify_recurrent(const tgdn_tree* tree, const tgdn_dims* dims, const vo
                                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int tgdn_tree_build(int32_t B, int32_t budget, int32_t K, int32_t w, int32_t depth_max,
+                    const int32_t* root_token, const float* child_logp,
+                    const int32_t* child_token, int32_t* parent, int32_t* token, float* score,
+                    int32_t* depth, int32_t* n_nodes, int32_t* rounds, tgdn_stream_t stream) {
+  if (B < 0 || budget < 1 || K < 1 || w < 1 || depth_max < 0) return TGDN_EINVAL;
+  if (budget > TGDN_MAX_NODES || K > TGDN_BUILD_MAX_K || depth_max > TGDN_MAX_DEPTH)
+    return TGDN_ETOOBIG;
+  if (B == 0) return TGDN_OK;
+  if (!root_token || !child_logp || !child_token || !parent || !token || !score || !depth ||
+      !n_nodes || !rounds)
+    return TGDN_EINVAL;
+  return from_cuda(tgdn::launch_tree_build(B, budget, K, w, depth_max, root_token, child_logp,
+                                           child_token, parent, token, score, depth, n_nodes,
+                                           rounds, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int tgdn_accept(const tgdn_tree* tree, const int32_t* draft_ids, const int32_t* target_ids,
                 int32_t* accept_node, int32_t* accept_len, int32_t* path,
                 tgdn_stream_t stream) {

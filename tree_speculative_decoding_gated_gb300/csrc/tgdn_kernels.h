@@ -63,6 +63,14 @@ cudaError_t launch_verify_recurrent(const tgdn_tree& t, const tgdn_dims& d, cons
                                     const void* k, const void* v, const float* g,
                                     const float* b, const float* S0, void* o, cudaStream_t s);
 
+// Top-w best-first draft-tree construction, one warp per sequence.
+size_t tree_build_smem_bytes(int budget, int K);
+cudaError_t launch_tree_build(int B, int budget, int K, int w, int depth_max,
+                              const int32_t* root_token, const float* child_logp,
+                              const int32_t* child_token, int32_t* parent, int32_t* token,
+                              float* score, int32_t* depth, int32_t* n_nodes, int32_t* rounds,
+                              cudaStream_t s);
+
 cudaError_t launch_commit(const tgdn_tree& t, const tgdn_dims& d, const int32_t* accept_node,
                           const void* k, const float* U, const float* G, const float* S_in,
                           float* S_out, cudaStream_t s);

@@ -332,3 +332,29 @@ def make_node_inputs_device(cfg: Config, T: int, gen, device):
 def make_state_device(cfg: Config, B: int, gen, device):
     import torch
     return cfg.s0_sigma * torch.randn((B, cfg.H_v, cfg.dk, cfg.dv), generator=gen, device=device)
+
+
+# --------------------------------------------------------------------------
+# drafter tables for top-w best-first tree construction
+# --------------------------------------------------------------------------
+def make_build_tables(B: int, budget: int, K: int, seed: int = 0, tie_step: float = 0.0):
+    """Seeded stand-in for the drafter's top-K continuations of every tree slot.
+
+    Per (sequence, slot): K + 1 logits ~ N(0, 2) (the last one standing for the rest of
+    the vocabulary), log-softmax, the K candidate log-probabilities sorted descending;
+    K distinct token ids from the vocabulary.  tie_step > 0 rounds the log-probabilities
+    to multiples of tie_step (many exact ties).  Returns root_token [B], child_logp
+    [B][budget][K] float32, child_token [B][budget][K] int32."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([BASE_SEED, 3000, seed])))
+    logits = 2.0 * rng.standard_normal((B, budget, K + 1))
+    m = logits.max(axis=-1, keepdims=True)
+    lse = m + np.log(np.exp(logits - m).sum(axis=-1, keepdims=True))
+    logp = -np.sort(-(logits[..., :K] - lse), axis=-1)
+    if tie_step > 0:
+        logp = np.minimum(np.round(logp / tie_step) * tie_step, -tie_step)
+    tok = np.empty((B, budget, K), np.int32)
+    for b in range(B):
+        for i in range(budget):
+            tok[b, i] = rng.choice(VOCAB, K, replace=False)
+    root = rng.integers(0, VOCAB, B).astype(np.int32)
+    return root, logp.astype(np.float32), tok

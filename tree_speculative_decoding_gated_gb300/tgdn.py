@@ -75,6 +75,9 @@ def lib() -> ctypes.CDLL:
         L.tgdn_verify_fused.argtypes = [P(CTree), P(CDims), vp, vp, vp, vp, vp, vp, vp, vp,
                                         P(CTree), vp, vp, vp, vp, st]
         L.tgdn_verify_fused.restype = ctypes.c_int
+        L.tgdn_tree_build.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp,
+                                      vp, st]
+        L.tgdn_tree_build.restype = ctypes.c_int
         L.tgdn_status_string.argtypes = [i32]
         L.tgdn_status_string.restype = ctypes.c_char_p
         L.tgdn_version.argtypes = []
@@ -235,6 +238,40 @@ def verify_recurrent(tree: Tree, dims: Dims, q, k, v, g, b, S0, o, stream=None) 
             _dev(o, io, T * dims.H_v * dims.d_v, "o"))
     _check(lib().tgdn_verify_recurrent(ctypes.byref(ct), ctypes.byref(cd), *args,
                                        _stream(stream)), "tgdn_verify_recurrent")
+
+
+BUILD_MAX_K = 16
+
+
+def tree_build(root_token, child_logp, child_token, budget: int, w: int, depth_max: int,
+               out=None, stream=None) -> dict:
+    """tgdn_tree_build: top-w best-first draft trees for a batch of sequences.
+    root_token [B] int32, child_logp [B][budget][K] fp32, child_token [B][budget][K] int32.
+    Returns (or fills `out` with) parent/token/depth [B][budget] int32, score [B][budget]
+    fp32, n_nodes [B] and rounds [B] int32, all on the device."""
+    B = root_token.shape[0]
+    K = child_logp.shape[-1] if child_logp.dim() == 3 else 0
+    dev = root_token.device
+    if out is None:
+        out = dict(parent=torch.empty((B, budget), dtype=torch.int32, device=dev),
+                   token=torch.empty((B, budget), dtype=torch.int32, device=dev),
+                   score=torch.empty((B, budget), dtype=torch.float32, device=dev),
+                   depth=torch.empty((B, budget), dtype=torch.int32, device=dev),
+                   n_nodes=torch.empty(B, dtype=torch.int32, device=dev),
+                   rounds=torch.empty(B, dtype=torch.int32, device=dev))
+    nt = B * budget * K
+    args = (_dev(root_token, torch.int32, B, "root_token"),
+            _dev(child_logp, torch.float32, nt, "child_logp"),
+            _dev(child_token, torch.int32, nt, "child_token"),
+            _dev(out["parent"], torch.int32, B * budget, "parent"),
+            _dev(out["token"], torch.int32, B * budget, "token"),
+            _dev(out["score"], torch.float32, B * budget, "score"),
+            _dev(out["depth"], torch.int32, B * budget, "depth"),
+            _dev(out["n_nodes"], torch.int32, B, "n_nodes"),
+            _dev(out["rounds"], torch.int32, B, "rounds"))
+    _check(lib().tgdn_tree_build(B, budget, K, w, depth_max, *args, _stream(stream)),
+           "tgdn_tree_build")
+    return out
 
 
 def accept(tree: Tree, draft_ids, target_ids, accept_node, accept_len, path, stream=None) -> None:
