@@ -6,6 +6,11 @@ arithmetic lives in ``tgdn_oracle.cpp`` (path replay of the GDN update eq. from
 "Trees from Marginals", Technisches Resümee, Methodik 3); this module only
 marshals numpy arrays into it.
 
+Two further parts of the pages' decode step have oracles of their own, written
+in plain Python: ``tree_build.py`` (top-w best-first draft-tree construction,
+Methodik 2) and ``tree_attention.py`` (ancestor-masked attention for the
+verifier's attention layers); each is pinned by its own test module.
+
 Pins: every function here is checked in ``tests/test_oracle.py`` against
 things other than itself — closed forms (b = 0 pure decay, the scalar
 d_k = d_v = 1 product form), a chain equal to token-by-token GDN, the
