@@ -69,6 +69,7 @@ constexpr int kOffSS = 196608;    // path-solve scratch [128 rows][kTcPath] fp32
 // Pending-commit staging, inside the S0 operand area (free between items):
 constexpr int kOffUP = kOffS0hi;          // u_s rows [kTcPath][128] fp32        15.5 KiB
 constexpr int kOffKP = kOffS0hi + 16384;  // k_s rows [kTcPath][128] bf16        7.75 KiB
+constexpr int kOffGP = kOffS0hi + 24576;  // 16-byte chunks holding G_s [kTcPath][4] fp32
 constexpr int kOffMeta = kOffSS + 128 * kTcPath * 4;
 
 struct ItemMeta {
@@ -91,8 +92,7 @@ struct TcShared {
   int tma_issued;
   int c_issued;           // pending-commit stagings issued
   int c_L;                // staged path length (0: nothing to commit)
-  float c_decay;          // e^{G*}
-  float c_coef[kTcPath];  // e^{G* - G_s} along the staged path
+  int c_gi[kTcPath];      // index of G_s within its staged 16-byte chunk
   ItemMeta meta[2];
 };
 constexpr int kTcSmemBytes = kOffMeta + (int)sizeof(TcShared) + 1024;  // + alignment slack
@@ -203,37 +203,42 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       for (int r = 0; r < 16; ++r)
         sreg[r] = reinterpret_cast<const float4*>(src + (size_t)(srow0 + 8 * r) * kTcDV)[sq];
     };
-    // Warp 0: stage the pending commit of one item (its accepted path in the
-    // previous tree; entries after the first invalid one are ignored).
-    auto stage_commit = [&](int it) {
-      const int bi = it / H_v, h = it % H_v, qh = h / grp;
+    // Warp 0, one item ahead: the item's accepted path in the previous tree
+    // (lane l holds entry l) and that sequence's bounds and status.
+    int c_node = -1, c_plo = 0, c_pN = 0, c_st = TGDN_SEQ_OK;
+    auto load_commit_meta = [&](int it) {
+      const int bi = it / H_v;
+      c_plo = cm.cu[bi];
+      c_pN = cm.cu[bi + 1] - c_plo;
+      c_st = cm.status[bi];
+      c_node = p < cm.path_len ? cm.path[(size_t)bi * cm.path_len + p] : -1;
+    };
+    // Warp 0: stage the pending commit of one item: the u_s and k_s rows of the
+    // path and the 16-byte chunks holding G_s (entries after the first invalid
+    // one are ignored).
+    auto issue_commit = [&](int it) {
+      const int h = it % H_v, qh = h / grp;
       const int lane = p;
-      const int plo = cm.cu[bi], pN = cm.cu[bi + 1] - plo;
-      int node = -1;
-      if (lane < cm.path_len) node = cm.path[(size_t)bi * cm.path_len + lane];
-      const bool valid = cm.status[bi] == TGDN_SEQ_OK && lane < cm.path_len && node >= 0 &&
-                         node < pN;
+      const bool valid =
+          c_st == TGDN_SEQ_OK && lane < cm.path_len && c_node >= 0 && c_node < c_pN;
       const int L = __ffs(__ballot_sync(0xffffffffu, !valid)) - 1;  // path_len <= 31
-      float Gl = 0.f;
-      if (lane < L) Gl = cm.G[(size_t)(plo + node) * H_v + h];
-      const float Gstar = __shfl_sync(0xffffffffu, Gl, L > 0 ? L - 1 : 0);
-      if (lane < L) sh.c_coef[lane] = __expf(Gstar - Gl);
       if (lane == 0) {
         sh.c_L = L;
-        sh.c_decay = L > 0 ? __expf(Gstar) : 1.f;
         sh.c_issued += 1;
+        mbar_arrive_expect_tx(&sh.cbar, static_cast<uint32_t>(L) * (kTcDV * 4 + kTcDK * 2 + 16));
       }
       __syncwarp();
-      if (lane == 0)
-        mbar_arrive_expect_tx(&sh.cbar, static_cast<uint32_t>(L) * (kTcDV * 4 + kTcDK * 2));
-      __syncwarp();
       if (lane < L) {
-        const size_t row = (size_t)(plo + node);
+        const size_t row = (size_t)(c_plo + c_node);
         bulk_copy_g2s(smem + kOffUP + lane * (kTcDV * 4), cm.U + (row * H_v + h) * kTcDV,
                       kTcDV * 4, &sh.cbar);
         bulk_copy_g2s(smem + kOffKP + lane * (kTcDK * 2),
                       static_cast<const __nv_bfloat16*>(cm.k) + (row * H_qk + qh) * kTcDK,
                       kTcDK * 2, &sh.cbar);
+        const size_t ge = row * H_v + h;  // G_s; the workspace base is 256-byte aligned
+        sh.c_gi[lane] = static_cast<int>(ge & 3);
+        bulk_copy_g2s(smem + kOffGP + lane * 16, cm.G + (ge & ~static_cast<size_t>(3)), 16,
+                      &sh.cbar);
       }
     };
     Prefetch pf;
@@ -255,7 +260,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     if (p == 0) issue_kq(item);
     load_meta(item);
     load_s0(item);
-    if (fused && p < 32) stage_commit(item);
+    if (fused && p < 32) {
+      load_commit_meta(item);
+      issue_commit(item);
+    }
 
     for (int j = 0; item < n_items; ++j, item += stride) {
       const int slot = j & 1;
@@ -291,9 +299,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         if (!group_wait(&sh.cbar, j & 1, kBarP, p == 0, abort)) break;
         const int L = sh.c_L;
         if (L > 0) {
-          const float decay = sh.c_decay;
           const float* UP = reinterpret_cast<const float*>(smem + kOffUP);
           const __nv_bfloat16* KP = reinterpret_cast<const __nv_bfloat16*>(smem + kOffKP);
+          const float* GP = reinterpret_cast<const float*>(smem + kOffGP);
+          const float Gstar = GP[(L - 1) * 4 + sh.c_gi[L - 1]];
+          const float decay = __expf(Gstar);
 #pragma unroll
           for (int r = 0; r < 16; ++r) {
             sreg[r].x *= decay;
@@ -303,7 +313,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
           }
           for (int l = 0; l < L; ++l) {
             const float4 u = reinterpret_cast<const float4*>(UP + l * kTcDV)[sq];
-            const float cl = sh.c_coef[l];
+            const float cl = __expf(Gstar - GP[l * 4 + sh.c_gi[l]]);
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
               const float kv = cl * __bfloat162float(KP[l * kTcDK + srow0 + 8 * r]);
@@ -341,6 +351,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       if (next < n_items) {
         load_s0(next);
         load_meta(next);
+        if (fused && p < 32) load_commit_meta(next);
       }
       ok = named_sync_and(kBarP, kGroup, ok);
       // root paths from the ancestor masks (bits = topological positions,
@@ -409,7 +420,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       if (!named_sync_and(kBarP, kGroup, step_ok && !*abort)) break;
       if (p == 0 && next < n_items) issue_kq(next);
       // the S0 operand area is free again: stage the next item's pending commit
-      if (fused && p < 32 && next < n_items) stage_commit(next);
+      if (fused && p < 32 && next < n_items) issue_commit(next);
     }
   } else {
     // =================================================== consumer warps 8-15
@@ -475,6 +486,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         for (int i = 0; i < 8; ++i)  // 32 KiB of [T; W] hi + lo, consecutive 16 B per thread
           *reinterpret_cast<uint4*>(smem + kOffA2hi + (i * kGroup + c) * 16) = zero;
       }
+      named_sync(kBarC, kGroup);  // Gram rows stored, [T; W] operand zeroed
+
+      // Key-lane warps form R while the query-lane warps solve for T and W (the
+      // solve needs only the Gram rows and the metadata).
       // ---- R = diag(b)(V - e^G K S0) as a bf16 hi/lo operand (key lanes)
       if (key_lane) {
         const bool live = lane_node < N;
@@ -505,10 +520,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         }
       }
       if (next < n_items) load_v(next);  // V rows of the next item, ahead of time
-      tc_fence_before_sync();
-      named_sync(kBarC, kGroup);
 
-      // ---- one row of T (c < 64) or W (64 <= c < 128), by back substitution on
+      // ---- one row of T (sc < 64) or W (64 <= sc < 128), by back substitution on
       // the root path P = (p_0 = root, ..., p_d = n):
       //   r (I + X_P) = y,  X_P[i][j] = b_{p_i} e^{G_{p_i} - G_{p_j}} k_{p_i}.k_{p_j} (i > j),
       //   y = e_d for T;  y_j = e^{G_n - G_{p_j}} q_n.k_{p_j} for W.
@@ -516,15 +529,16 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       //   r_j = y_j - (1 / phi_j) sum_{i>j} s_i k_{p_i}.k_{p_j}.
       // (phi is capped at e^80; the capped terms are below fp32 resolution.)
       // Rows are handed out in topological order so that a warp sees similar depths.
-      if (c < 128) {
-        const bool t_row = c < 64;
-        const int spos = c & 63;
+      if (!key_lane) {
+        const int sc = (lq - 2) * 64 + chalf * 32 + (c & 31);  // solver index 0..127
+        const bool t_row = sc < 64;
+        const int spos = sc & 63;
         if (spos < N) {
           const int sn = M.ord[spos];
           const int a2row = t_row ? sn : 64 + sn;
           const int dn = M.dep[sn];
           const uint8_t* P = &M.anc_at[0][sn];  // P[i * kTcNodes]: ancestor at depth i
-          float* SS = SSbase + c * kTcPath;
+          float* SS = SSbase + sc * kTcPath;
           const float* GR = reinterpret_cast<const float*>(smem + kOffGR);
           const float Gn = M.G[sn];
           const int qrow = 64 + sn;
