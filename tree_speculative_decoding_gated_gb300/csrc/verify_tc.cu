@@ -86,12 +86,11 @@ struct TcShared {
   uint64_t tma_bar, mma1_bar, mma2_bar;
   uint64_t s1_done[2];    // consumer waits: first product done + metadata written
   uint64_t tmem_free[2];  // producer waits: consumer finished the item in this half
-  uint64_t cbar;          // pending-commit staging of the next item has landed
   uint32_t tmem_slot;
   int abort;
   int tma_issued;
-  int c_issued;           // pending-commit stagings issued
   int c_L;                // staged path length (0: nothing to commit)
+  int c_row[kTcPath];     // previous-step node rows of the staged path
   int c_gi[kTcPath];      // index of G_s within its staged 16-byte chunk
   ItemMeta meta[2];
 };
@@ -166,12 +165,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     mbar_init(&sh.s1_done[1], 2);
     mbar_init(&sh.tmem_free[0], 1);
     mbar_init(&sh.tmem_free[1], 1);
-    mbar_init(&sh.cbar, 1);
     fence_mbar_init();
     fence_proxy_async_smem();
     sh.abort = 0;
     sh.tma_issued = 0;
-    sh.c_issued = 0;
   }
   if (warp == 0) tmem_alloc(&sh.tmem_slot, kTmemCols);
   tc_fence_before_sync();
@@ -182,9 +179,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
   if (tid < kGroup) {
     // =================================================== producer warps 0-7
     const int p = tid;
-    auto issue_kq = [&](int item) {  // thread 0 only
-      const int bi = item / H_v, qh = (item % H_v) / grp;
-      const int row0 = cu[bi];
+    auto issue_kq = [&](int item, int row0) {  // thread 0 only; row0 = cu[item / H_v]
+      const int qh = (item % H_v) / grp;
       mbar_arrive_expect_tx(&sh.tma_bar, 4 * 64 * 128);
       // box = 64 d_k elements x 1 head x 64 node rows, 128-byte swizzled rows
       tma_load_3d(smem + kOffA + 0, &kmap, &sh.tma_bar, 0, qh, row0);
@@ -213,40 +209,53 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       c_st = cm.status[bi];
       c_node = p < cm.path_len ? cm.path[(size_t)bi * cm.path_len + p] : -1;
     };
-    // Warp 0: stage the pending commit of one item: the u_s and k_s rows of the
-    // path and the 16-byte chunks holding G_s (entries after the first invalid
-    // one are ignored).
-    auto issue_commit = [&](int it) {
-      const int h = it % H_v, qh = h / grp;
-      const int lane = p;
+    // Warp 0: the item's staged path (entries after the first invalid one are
+    // ignored) -> c_L, c_row.
+    auto publish_commit = [&]() {
       const bool valid =
-          c_st == TGDN_SEQ_OK && lane < cm.path_len && c_node >= 0 && c_node < c_pN;
+          c_st == TGDN_SEQ_OK && p < cm.path_len && c_node >= 0 && c_node < c_pN;
       const int L = __ffs(__ballot_sync(0xffffffffu, !valid)) - 1;  // path_len <= 31
-      if (lane == 0) {
-        sh.c_L = L;
-        sh.c_issued += 1;
-        mbar_arrive_expect_tx(&sh.cbar, static_cast<uint32_t>(L) * (kTcDV * 4 + kTcDK * 2 + 16));
+      if (p == 0) sh.c_L = L;
+      if (p < L) sh.c_row[p] = c_plo + c_node;
+    };
+    // All producer threads: 16-byte asynchronous copies of the published path's
+    // u_s rows, k_s rows and the chunks holding G_s (49 chunks per path node).
+    auto stage_commit = [&](int it) {
+      const int h = it % H_v, qh = h / grp;
+      const int L = sh.c_L;
+      for (int e = p; e < L * 49; e += kGroup) {
+        const int l = e / 49, w = e - l * 49;
+        const size_t row = static_cast<size_t>(sh.c_row[l]);
+        if (w < 32) {
+          cp_async16(smem + kOffUP + l * (kTcDV * 4) + w * 16,
+                     cm.U + (row * H_v + h) * kTcDV + w * 4);
+        } else if (w < 48) {
+          cp_async16(smem + kOffKP + l * (kTcDK * 2) + (w - 32) * 16,
+                     static_cast<const __nv_bfloat16*>(cm.k) + (row * H_qk + qh) * kTcDK +
+                         (w - 32) * 8);
+        } else {
+          const size_t ge = row * H_v + h;  // the workspace base is 256-byte aligned
+          sh.c_gi[l] = static_cast<int>(ge & 3);
+          cp_async16(smem + kOffGP + l * 16, cm.G + (ge & ~static_cast<size_t>(3)));
+        }
       }
-      __syncwarp();
-      if (lane < L) {
-        const size_t row = (size_t)(c_plo + c_node);
-        bulk_copy_g2s(smem + kOffUP + lane * (kTcDV * 4), cm.U + (row * H_v + h) * kTcDV,
-                      kTcDV * 4, &sh.cbar);
-        bulk_copy_g2s(smem + kOffKP + lane * (kTcDK * 2),
-                      static_cast<const __nv_bfloat16*>(cm.k) + (row * H_qk + qh) * kTcDK,
-                      kTcDK * 2, &sh.cbar);
-        const size_t ge = row * H_v + h;  // G_s; the workspace base is 256-byte aligned
-        sh.c_gi[lane] = static_cast<int>(ge & 3);
-        bulk_copy_g2s(smem + kOffGP + lane * 16, cm.G + (ge & ~static_cast<size_t>(3)), 16,
-                      &sh.cbar);
-      }
+      cp_async_commit();
+    };
+    // Sequence bounds and status one item ahead of the node metadata, so that no
+    // load waits on another load of the same iteration.
+    int q_lo = 0, q_N = 0, q_st = 0;
+    auto load_seq = [&](int item) {
+      const int bi = item / H_v;
+      q_lo = cu[bi];
+      q_N = cu[bi + 1] - q_lo;
+      q_st = status[bi];
     };
     Prefetch pf;
-    auto load_meta = [&](int item) {
-      const int bi = item / H_v, h = item % H_v;
-      pf.lo = cu[bi];
-      pf.N = cu[bi + 1] - pf.lo;
-      pf.st = status[bi];
+    auto load_meta = [&](int item) {  // node metadata; the bounds come from load_seq
+      const int h = item % H_v;
+      pf.lo = q_lo;
+      pf.N = q_N;
+      pf.st = q_st;
       if (p < pf.N && p < kTcNodes) {
         pf.dep = depth[pf.lo + p];
         pf.pos = pos[pf.lo + p];
@@ -257,12 +266,18 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     };
     int item = blockIdx.x;
     uint32_t mma1_count = 0;  // first products issued so far (thread 0)
-    if (p == 0) issue_kq(item);
+    load_seq(item);
+    if (p == 0) issue_kq(item, q_lo);
     load_meta(item);
+    if (item + stride < n_items) load_seq(item + stride);
     load_s0(item);
-    if (fused && p < 32) {
-      load_commit_meta(item);
-      issue_commit(item);
+    if (fused) {
+      if (p < 32) {
+        load_commit_meta(item);
+        publish_commit();
+      }
+      named_sync(kBarP, kGroup);
+      stage_commit(item);
     }
 
     for (int j = 0; item < n_items; ++j, item += stride) {
@@ -296,7 +311,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       if (fused) {
         // the previous step's commit: S = e^{G*} S + sum_l e^{G*-G_l} k_l u_l^T,
         // written back in place; the committed state is what gets verified
-        if (!group_wait(&sh.cbar, j & 1, kBarP, p == 0, abort)) break;
+        cp_async_wait_all();
+        named_sync(kBarP, kGroup);
         const int L = sh.c_L;
         if (L > 0) {
           const float* UP = reinterpret_cast<const float*>(smem + kOffUP);
@@ -304,6 +320,15 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
           const float* GP = reinterpret_cast<const float*>(smem + kOffGP);
           const float Gstar = GP[(L - 1) * 4 + sh.c_gi[L - 1]];
           const float decay = __expf(Gstar);
+          // CK[l][s][r] = e^{G*-G_l} k_l[8 r + s], in the (free) S0 lo operand area: the
+          // 16 rows a thread owns become four 16-byte loads per path node
+          float* CK = reinterpret_cast<float*>(smem + kOffS0lo);
+          for (int e = p; e < L * kTcDK; e += kGroup) {
+            const int l = e >> 7, row = e & 127;
+            CK[l * kTcDK + (row & 7) * 16 + (row >> 3)] =
+                __expf(Gstar - GP[l * 4 + sh.c_gi[l]]) * __bfloat162float(KP[l * kTcDK + row]);
+          }
+          named_sync(kBarP, kGroup);
 #pragma unroll
           for (int r = 0; r < 16; ++r) {
             sreg[r].x *= decay;
@@ -313,14 +338,19 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
           }
           for (int l = 0; l < L; ++l) {
             const float4 u = reinterpret_cast<const float4*>(UP + l * kTcDV)[sq];
-            const float cl = __expf(Gstar - GP[l * 4 + sh.c_gi[l]]);
+            const float4* c4 = reinterpret_cast<const float4*>(CK + l * kTcDK + srow0 * 16);
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-              const float kv = cl * __bfloat162float(KP[l * kTcDK + srow0 + 8 * r]);
-              sreg[r].x = fmaf(kv, u.x, sreg[r].x);
-              sreg[r].y = fmaf(kv, u.y, sreg[r].y);
-              sreg[r].z = fmaf(kv, u.z, sreg[r].z);
-              sreg[r].w = fmaf(kv, u.w, sreg[r].w);
+            for (int i = 0; i < 4; ++i) {  // rows srow0 + 8 (4 i + t), t = 0..3
+              const float4 x = c4[i];
+              const float kv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                float4& a = sreg[4 * i + t];
+                a.x = fmaf(kv[t], u.x, a.x);
+                a.y = fmaf(kv[t], u.y, a.y);
+                a.z = fmaf(kv[t], u.z, a.z);
+                a.w = fmaf(kv[t], u.w, a.w);
+              }
             }
           }
           float* dst = S + (size_t)item * kTcDK * kTcDV;
@@ -348,10 +378,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       fence_proxy_async_smem();
       // prefetch the next item while this one is finished
       const int next = item + stride;
-      if (next < n_items) {
-        load_s0(next);
+      if (next < n_items) {  // the small loads first: they are not queued behind S0
         load_meta(next);
+        if (next + stride < n_items) load_seq(next + stride);
         if (fused && p < 32) load_commit_meta(next);
+        load_s0(next);
       }
       ok = named_sync_and(kBarP, kGroup, ok);
       // root paths from the ancestor masks (bits = topological positions,
@@ -417,10 +448,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         step_ok = tma_ok && (!issued || mbar_wait_suspend(&sh.mma1_bar, mma1_count & 1, abort));
         if (issued) ++mma1_count;
       }
+      if (fused && p < 32 && next < n_items) publish_commit();
       if (!named_sync_and(kBarP, kGroup, step_ok && !*abort)) break;
-      if (p == 0 && next < n_items) issue_kq(next);
+      if (p == 0 && next < n_items) issue_kq(next, pf.lo);
       // the S0 operand area is free again: stage the next item's pending commit
-      if (fused && p < 32 && next < n_items) issue_commit(next);
+      if (fused && next < n_items) stage_commit(next);
     }
   } else {
     // =================================================== consumer warps 8-15
@@ -433,10 +465,16 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     const bool key_lane = lq < 2;
     const int lane_node = key_lane ? lane_row : lane_row - 64;
     uint4 vreg[8];
+    int cv_lo = 0, cv_N = 0;  // bounds of the sequence load_v reads next (one item ahead)
+    auto load_vseq = [&](int item) {
+      const int bi = item / H_v;
+      cv_lo = cu[bi];
+      cv_N = cu[bi + 1] - cv_lo;
+    };
     auto load_v = [&](int item) {  // this thread's V row, 64 value columns
       if (!key_lane) return;
-      const int bi = item / H_v, h = item % H_v;
-      const int lo = cu[bi], N = cu[bi + 1] - lo;
+      const int h = item % H_v;
+      const int lo = cv_lo, N = cv_N;
       if (lane_node < N && N <= kTcNodes) {
         const uint4* vp = reinterpret_cast<const uint4*>(
             v + ((size_t)(lo + lane_node) * H_v + h) * kTcDV + chalf * 64);
@@ -445,7 +483,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       }
     };
     int item = blockIdx.x;
+    load_vseq(item);
     load_v(item);
+    if (item + stride < n_items) load_vseq(item + stride);
     float* SSbase = reinterpret_cast<float*>(smem + kOffSS);
     uint32_t mma2_count = 0;  // second products issued so far (same in every thread)
     for (int j = 0; item < n_items; ++j, item += stride) {
@@ -465,7 +505,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
           *reinterpret_cast<float4*>(Uws + row) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         for (int n = c; n < N; n += kGroup) Gws[(size_t)(lo + n) * H_v + h] = 0.f;
-        if (next < n_items) load_v(next);
+        if (next < n_items) {
+          load_v(next);
+          if (next + stride < n_items) load_vseq(next + stride);
+        }
         named_sync(kBarC, kGroup);
         if (c == 0) mbar_arrive(&sh.tmem_free[slot]);
         continue;
@@ -519,7 +562,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
           }
         }
       }
-      if (next < n_items) load_v(next);  // V rows of the next item, ahead of time
+      if (next < n_items) {  // V rows of the next item, ahead of time
+        load_v(next);
+        if (next + stride < n_items) load_vseq(next + stride);
+      }
 
       // ---- one row of T (sc < 64) or W (64 <= sc < 128), by back substitution on
       // the root path P = (p_0 = root, ..., p_d = n):
@@ -647,12 +693,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
 
   // ---- end.  After an expired wait every item still owned by this CTA is
   // reported as timed out, and the latest copy and products are drained (bounded).
+  cp_async_wait_all();  // staging copies left by a loop that ended early
   __syncthreads();
   if (sh.abort && tid == 0) {
     for (int it2 = blockIdx.x; it2 < n_items; it2 += stride)
       atomicCAS(&status[it2 / H_v], TGDN_SEQ_OK, TGDN_SEQ_TIMEOUT);
     if (sh.tma_issued > 0) (void)mbar_wait(&sh.tma_bar, (sh.tma_issued - 1) & 1);
-    if (sh.c_issued > 0) (void)mbar_wait(&sh.cbar, (sh.c_issued - 1) & 1);
   }
   __syncthreads();
   if (warp == 0) {
