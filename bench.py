@@ -45,6 +45,10 @@ METRIC = "verified tree nodes/sec per GDN layer (1 GB300); achieved HBM GB/s % o
 UNIT = "nodes/s/layer"
 S0_BYTES_PER_SEQ = 32 * 128 * 128 * 4                     # one layer's state of one sequence
 NODE_BYTES = 2 * 16 * 128 * 2 + 32 * 128 * 2 + 2 * 32 * 4 + 32 * 128 * 2   # q,k,v,g,b in + o out
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant kernel, from the
+# ncu capture summarised in profiles/verify_tc_stack36_layer.md (fused step).  Reset to None
+# whenever that kernel changes, until it is captured again.
+PROFILED_TRAFFIC = {"fused": 105_235_712 + 61_559_552, "separate": None}
 
 
 def parse():
@@ -363,7 +367,8 @@ def run_gpu(args, rank, world, local):
     step_desc = (f"prep + {L} verify with the previous step's commit folded in + accept"
                  if fused else f"prep + {L} verify + accept + {L} in-place commit")
     roof = {"bound": "hbm", "kernel": dom["kernel"], "achieved": dom["gbs"], "peak": hbm,
-            "peak_kind": peak_kind, "unit": "GB/s", "frac": dom["gbs"] / hbm, "traffic": None,
+            "peak_kind": peak_kind, "unit": "GB/s", "frac": dom["gbs"] / hbm,
+            "traffic": PROFILED_TRAFFIC[args.mode],
             "algorithmic_bytes_per_launch": dom["bytes"], "launch_us": dom["us"]}
     if other is not None:
         roof["other"] = {"kernel": other["kernel"], "achieved": other["gbs"],
