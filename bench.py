@@ -65,10 +65,12 @@ def parse():
                     help="GDN layers per step (fewer only for small profiler captures)")
     ap.add_argument("--mode", default="fused", choices=["fused", "separate"],
                     help="fused: commit folded into the next step's verify; separate: own pass")
-    ap.add_argument("--part", default="stack", choices=["stack", "recurrent", "build"],
+    ap.add_argument("--part", default="stack",
+                    choices=["stack", "recurrent", "build", "attention"],
                     help="stack: the decode benchmark (default); recurrent: single-pass verify "
                          "vs per-branch recurrent verify by tree size; build: top-w tree "
-                         "construction kernel times")
+                         "construction kernel times; attention: ancestor-masked tree "
+                         "attention kernel times")
     return ap.parse_args()
 
 
@@ -595,12 +597,58 @@ def run_build_times(args):
             "sequence; latency bound)", "unit": "us", "higher_is_better": False, "cases": out}
 
 
+def run_attention_times(args):
+    """Ancestor-masked tree attention (tgdn_tree_attention): kernel time per layer and its
+    rates against the measured peaks (the cached context is the dominant stream)."""
+    import torch
+    from tree_speculative_decoding_gated_gb300 import tgdn
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(dev)
+    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(synth.BASE_SEED + 91)
+    rng = np.random.default_rng(synth.BASE_SEED + 92)
+    hbm, kind = peaks()
+    out = []
+    for B, N, H_q, H_kv, P in [(16, 64, 16, 4, 1024), (16, 64, 16, 4, 4096), (32, 64, 16, 4, 4096),
+                               (16, 128, 16, 4, 4096)]:
+        parents = [synth.random_recursive_tree(rng, N, 16) for _ in range(B)]
+        trees = synth.pack_trees(parents, N, 16)
+        tree = tgdn.Tree.from_host(trees.cu_nodes, trees.parent, N, 16, dev)
+        T = trees.T
+        rnd = lambda *shape: torch.randn(shape, generator=gen, device=dev).to(torch.bfloat16)
+        q, kt, vt = rnd(T, H_q, 128), rnd(T, H_kv, 128), rnd(T, H_kv, 128)
+        kc, vc = rnd(B, P, H_kv, 128), rnd(B, P, H_kv, 128)
+        pl = torch.full((B,), P, dtype=torch.int32, device=dev)
+        o = torch.empty_like(q)
+        with torch.cuda.stream(stream):
+            tgdn.tree_prep(tree, stream)
+        fn = lambda: tgdn.tree_attention(tree, q, kt, vt, kc, vc, pl, o, 128 ** -0.5, stream)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+        t = _launch_times(torch, stream, fn, 20, flush)
+        depth = np.concatenate([synth.tree_depths(p) for p in parents])
+        keys = float(P * T + (depth + 1).sum())  # visible keys per node (one q head)
+        flops = 4.0 * 128 * keys * H_q           # QK^T and PV, 2 flops per multiply-add
+        cache_bytes = 2 * B * P * H_kv * 128 * 2
+        node_bytes = T * (2 * H_q + 2 * H_kv) * 128 * 2
+        gbs = (cache_bytes + node_bytes) / (t * 1e-6) / 1e9
+        out.append({"B": B, "nodes": N, "H_q": H_q, "H_kv": H_kv, "context": P, "us": t,
+                    "GB/s": gbs, "frac_hbm": gbs / hbm, "TFLOP/s": flops / (t * 1e-6) / 1e12})
+    return {"part": "attention", "metric": "tgdn_tree_attention kernel time per layer, bf16, "
+            "d=128, L2 flushed before every launch", "unit": "us", "higher_is_better": False,
+            "peak_hbm_gbs": hbm, "peak_kind": kind, "cases": out}
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
     if args.part != "stack":
         if rank == 0:
-            fn = run_recurrent_compare if args.part == "recurrent" else run_build_times
+            fn = {"recurrent": run_recurrent_compare, "build": run_build_times,
+                  "attention": run_attention_times}[args.part]
             print(json.dumps(fn(args)), flush=True)
         return
     if args.impl == "reference":

@@ -200,6 +200,27 @@ int tgdn_tree_build(int32_t B, int32_t budget, int32_t K, int32_t w, int32_t dep
                     const int32_t* child_token, int32_t* parent, int32_t* token, float* score,
                     int32_t* depth, int32_t* n_nodes, int32_t* rounds, tgdn_stream_t stream);
 
+/* Ancestor-masked tree attention for the verifier's attention layers
+ * (Problemstellung: tree verification in attention layers uses attention
+ * masks).  Node n of sequence b attends to the sequence's cached context
+ * (positions 0 .. prefix_len[b] - 1) and to the tree nodes on its own root
+ * path, itself included:
+ *   o[n][h] = softmax_j(scale * q[n][h] . k_j) v_j   over those keys j,
+ * query head h reading key/value head h / (H_q / H_kv).  bf16 tensors:
+ *   q       [T][H_q][d]        k_tree, v_tree [T][H_kv][d]  (the tree's own keys)
+ *   k_cache, v_cache [B][P_max][H_kv][d]  (cached context; may be NULL if P_max is 0)
+ *   prefix_len [B] int32 (device; clamped to [0, P_max])
+ *   o       [T][H_q][d] bf16, written
+ * tgdn_tree_prep must have run on `tree`; sequences with a bad status get zero
+ * outputs.  Tensor-core kernel: d = 128, H_q / H_kv in {1, 2, 4, 8, 16},
+ * n_max <= 128; other shapes return TGDN_EUNSUPPORTED.  All pointers 16-byte
+ * aligned.  Returns TGDN_OK, TGDN_EINVAL, TGDN_ETOOBIG, TGDN_EUNSUPPORTED or
+ * TGDN_ECUDA. */
+int tgdn_tree_attention(const tgdn_tree* tree, int32_t H_q, int32_t H_kv, int32_t d,
+                        const void* q, const void* k_tree, const void* v_tree,
+                        const void* k_cache, const void* v_cache, const int32_t* prefix_len,
+                        int32_t P_max, float scale, void* o, tgdn_stream_t stream);
+
 /* Greedy acceptance (Experimentelle Ergebnisse, mean acceptance length).  The
  * root is always accepted; a non-root node is accepted when it and every
  * non-root node on its root path satisfy target_ids == draft_ids.  The

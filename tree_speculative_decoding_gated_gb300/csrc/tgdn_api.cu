@@ -61,6 +61,21 @@ bool encode_qk_map(CUtensorMap* map, const void* base, int T, int H_qk) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A [rows][H][128] bf16 tensor as a 3-D TMA map with box {64, box_h, box_rows},
+// 128-byte swizzle.
+bool encode_rows_map(CUtensorMap* map, const void* base, long rows, int H, int box_h,
+                     int box_rows) {
+  auto fn = encode_fn();
+  if (!fn || rows < 1) return false;
+  const cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {128 * 2, (cuuint64_t)H * 128 * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_h, (cuuint32_t)box_rows};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 extern "C" {
@@ -201,6 +216,38 @@ int tgdn_tree_build(int32_t B, int32_t budget, int32_t K, int32_t w, int32_t dep
   return from_cuda(tgdn::launch_tree_build(B, budget, K, w, depth_max, root_token, child_logp,
                                            child_token, parent, token, score, depth, n_nodes,
                                            rounds, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int tgdn_tree_attention(const tgdn_tree* tree, int32_t H_q, int32_t H_kv, int32_t d,
+                        const void* q, const void* k_tree, const void* v_tree,
+                        const void* k_cache, const void* v_cache, const int32_t* prefix_len,
+                        int32_t P_max, float scale, void* o, tgdn_stream_t stream) {
+  int rc = check_tree(tree);
+  if (rc != TGDN_OK) return rc;
+  const tgdn_tree& t = *tree;
+  if (H_q < 1 || H_kv < 1 || H_q % H_kv != 0 || d < 1 || P_max < 0) return TGDN_EINVAL;
+  if (!tgdn::tree_attn_supported(t, H_q, H_kv, d)) return TGDN_EUNSUPPORTED;
+  if (t.B > 0 && (!prefix_len || (P_max > 0 && (!k_cache || !v_cache)))) return TGDN_EINVAL;
+  if (t.T > 0 && (!q || !k_tree || !v_tree || !o)) return TGDN_EINVAL;
+  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) % 16) == 0; };
+  if (!al16(q) || !al16(k_tree) || !al16(v_tree) || !al16(k_cache) || !al16(v_cache) ||
+      !al16(o))
+    return TGDN_EINVAL;
+  if (t.B == 0 || t.T == 0) return TGDN_OK;
+  const int G = H_q / H_kv;
+  CUtensorMap qm, ktm, vtm, kcm, vcm;
+  // with no cached context the cache maps are never read; describe the tree instead
+  const void* kc = P_max > 0 ? k_cache : k_tree;
+  const void* vc = P_max > 0 ? v_cache : v_tree;
+  const long crows = P_max > 0 ? (long)t.B * P_max : t.T;
+  if (!encode_rows_map(&qm, q, t.T, H_q, G, 128 / G) ||
+      !encode_rows_map(&ktm, k_tree, t.T, H_kv, 1, 64) ||
+      !encode_rows_map(&vtm, v_tree, t.T, H_kv, 1, 64) ||
+      !encode_rows_map(&kcm, kc, crows, H_kv, 1, 64) ||
+      !encode_rows_map(&vcm, vc, crows, H_kv, 1, 64))
+    return TGDN_ECUDA;
+  return from_cuda(tgdn::launch_tree_attn(t, H_q, H_kv, P_max, scale, qm, ktm, vtm, kcm, vcm,
+                                          prefix_len, o, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int tgdn_accept(const tgdn_tree* tree, const int32_t* draft_ids, const int32_t* target_ids,

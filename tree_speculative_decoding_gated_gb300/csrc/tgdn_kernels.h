@@ -71,6 +71,17 @@ cudaError_t launch_tree_build(int B, int budget, int K, int w, int depth_max,
                               float* score, int32_t* depth, int32_t* n_nodes, int32_t* rounds,
                               cudaStream_t s);
 
+// Ancestor-masked tree attention (bf16, d = 128), one CTA per (sequence, key/value
+// head, 128 query rows).  Tensor maps: q [T][H_q][128] with box {64, G, 128 / G};
+// k_tree, v_tree [T][H_kv][128] and k_cache, v_cache [B * P_max][H_kv][128] with
+// box {64, 1, 64}; all 128-byte swizzled.
+bool tree_attn_supported(const tgdn_tree& t, int H_q, int H_kv, int d);
+cudaError_t launch_tree_attn(const tgdn_tree& t, int H_q, int H_kv, int P_max, float scale,
+                             const CUtensorMap& qmap, const CUtensorMap& ktmap,
+                             const CUtensorMap& vtmap, const CUtensorMap& kcmap,
+                             const CUtensorMap& vcmap, const int32_t* prefix_len, void* o,
+                             cudaStream_t s);
+
 cudaError_t launch_commit(const tgdn_tree& t, const tgdn_dims& d, const int32_t* accept_node,
                           const void* k, const float* U, const float* G, const float* S_in,
                           float* S_out, cudaStream_t s);

@@ -1,0 +1,340 @@
+// tree_attn.cu — ancestor-masked tree attention on tensor cores (bf16, d = 128).
+//
+// "Trees from Marginals" (Technisches Resümee, Problemstellung): in attention
+// layers a draft tree is verified with an attention mask, each node seeing the
+// sequence's cached context and its own root path.  The hybrid verifier's
+// attention layers run this on the same trees as its GDN layers, with the same
+// ancestor-or-self bitmasks from tree prep.
+//
+// One CTA per (sequence, key/value head, tile of 128 query rows); a query row
+// is (node, query head of the group), row = node * G + g.  128 threads, one per
+// row (= TMEM lane).  Keys come in tiles of 64: first the cached context
+// (prefix_len[b] positions), then the tree's own nodes.  Two passes over the
+// key tiles: the first finds each row's maximum logit and normaliser, the
+// second forms P = exp(logit - max) / sum as a bf16 operand and accumulates
+// O = P V on the tensor cores, so O never needs rescaling.
+//   S tile = Q K^T: tcgen05.mma, A = Q (TMA, 128-byte swizzle), B = K tile
+//   O     += P V:   A = P (written by the threads), B = V tile (MN-major)
+// Every wait is bounded; on expiry the sequence is marked TGDN_SEQ_TIMEOUT.
+#include "tgdn_device.cuh"
+#include "tgdn_kernels.h"
+
+namespace tgdn {
+
+constexpr int kAtThreads = 128;
+constexpr int kAtKeys = 64;              // keys per tile
+constexpr int kAtD = 128;
+constexpr int kAtMaxNodes = 128;         // tree nodes per sequence on this kernel
+constexpr uint32_t kAtTmemCols = 256;    // S tile: cols 0-63; O: cols 64-191
+constexpr int kAtOffQ = 0;               // [2 d halves][128 rows][128 B]     32 KiB
+constexpr int kAtOffK = 32768;           // [2 d halves][64 keys][128 B]      16 KiB
+constexpr int kAtOffV = 49152;           // [2 d atoms][64 keys][128 B]       16 KiB
+constexpr int kAtOffP = 65536;           // [128 rows][64 keys] bf16          16 KiB
+constexpr int kAtOffMask = 81920;        // [kAtMaxNodes][2] uint64          2 KiB
+constexpr int kAtOffBar = kAtOffMask + kAtMaxNodes * 16;
+constexpr int kAtSmemBytes = kAtOffBar + 64 + 1024;
+
+__device__ __forceinline__ int at_swz(int row, int chunk) {
+  return (row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+struct AtArgs {
+  int H_q, H_kv, G, n_max, P_max, mtiles, n_items;
+  float scale;
+  const int32_t* cu;
+  const int32_t* order;
+  const int32_t* pos;
+  const uint64_t* anc;
+  int words;
+  int32_t* status;
+  const int32_t* prefix_len;
+  __nv_bfloat16* o;
+};
+
+__global__ void __launch_bounds__(kAtThreads)
+tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
+                 const __grid_constant__ CUtensorMap ktmap,
+                 const __grid_constant__ CUtensorMap vtmap,
+                 const __grid_constant__ CUtensorMap kcmap,
+                 const __grid_constant__ CUtensorMap vcmap, const AtArgs a) {
+  extern __shared__ uint8_t at_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(at_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* amask = reinterpret_cast<uint64_t*>(smem + kAtOffMask);
+  uint64_t* tma_bar = reinterpret_cast<uint64_t*>(smem + kAtOffBar);
+  uint64_t* mma_bar = tma_bar + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_bar + 1);
+  int* s_abort = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int item = blockIdx.x;
+  if (item >= a.n_items) return;
+  const int mt = item % a.mtiles;
+  const int hk = (item / a.mtiles) % a.H_kv;
+  const int b = item / (a.mtiles * a.H_kv);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int lo = a.cu[b], N = a.cu[b + 1] - lo;
+  const int npt = kAtThreads / a.G;          // nodes per tile of query rows
+  const int node0 = mt * npt;
+  if (N <= 0 || node0 >= N) return;          // no rows of this tile exist
+  const int my_node = node0 + tid / a.G, my_g = tid % a.G;
+  const bool row_live = my_node < N;
+  __nv_bfloat16* orow =
+      a.o + ((size_t)(lo + my_node) * a.H_q + hk * a.G + my_g) * kAtD;
+  if (a.status[b] != TGDN_SEQ_OK || N > kAtMaxNodes || N > a.n_max) {
+    if (row_live)
+      for (int c = 0; c < kAtD / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = make_uint4(0, 0, 0, 0);
+    return;
+  }
+  const int P = max(0, min(a.prefix_len[b], a.P_max));
+
+  if (tid == 0) {
+    mbar_init(tma_bar, 1);
+    mbar_init(mma_bar, 1);
+    fence_mbar_init();
+    *s_abort = 0;
+  }
+  // ancestor-or-self sets in node-index space (bit s of word s / 64)
+  if (tid < N) {
+    uint64_t m0 = 0, m1 = 0;
+    const int p = a.pos[lo + tid];
+    if (p >= 0 && p < N) {
+      for (int w = 0; w < a.words && w < 2; ++w) {
+        uint64_t bits = a.anc[(size_t)(lo + p) * a.words + w];
+        while (bits) {
+          const int bp = w * 64 + __ffsll(static_cast<long long>(bits)) - 1;
+          bits &= bits - 1;
+          const int s = bp < N ? a.order[lo + bp] : -1;
+          if (s >= 0 && s < 64) m0 |= 1ull << s;
+          else if (s >= 64 && s < 128) m1 |= 1ull << (s - 64);
+        }
+      }
+    }
+    amask[2 * tid] = m0;
+    amask[2 * tid + 1] = m1;
+  }
+  if (warp == 0) tmem_alloc(tmem_slot, kAtTmemCols);
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem, tO = tmem + 64;
+  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  volatile int* abort = s_abort;
+
+  const int nt_pre = (P + kAtKeys - 1) / kAtKeys;
+  const int nt_tree = (N + kAtKeys - 1) / kAtKeys;
+  const int nt = nt_pre + nt_tree;
+  uint32_t tma_phase = 0, mma_phase = 0;
+  const uint64_t m_lo = row_live ? amask[2 * my_node] : 0;
+  const uint64_t m_hi = row_live ? amask[2 * my_node + 1] : 0;
+
+  // thread 0: the key (and value) tile t into shared memory, then S = Q K^T.
+  // Called once every thread is done with the previous tile's S and P.  On an
+  // expired wait it raises *abort and commits nothing (wait_mma then gives up).
+  auto load_and_score = [&](int t, bool with_v, bool first) {
+    if (tid != 0) return;
+    ++tma_phase;
+    const bool pre = t < nt_pre;
+    const int row = pre ? b * a.P_max + t * kAtKeys : lo + (t - nt_pre) * kAtKeys;
+    const CUtensorMap* km = pre ? &kcmap : &ktmap;
+    const CUtensorMap* vm = pre ? &vcmap : &vtmap;
+    uint32_t bytes = 2 * kAtKeys * 128 + (with_v ? 2 * kAtKeys * 128 : 0) + (first ? 32768 : 0);
+    mbar_arrive_expect_tx(tma_bar, bytes);
+    if (first) {
+      tma_load_3d(smem + kAtOffQ, &qmap, tma_bar, 0, hk * a.G, lo + node0);
+      tma_load_3d(smem + kAtOffQ + 16384, &qmap, tma_bar, 64, hk * a.G, lo + node0);
+    }
+    tma_load_3d(smem + kAtOffK, km, tma_bar, 0, hk, row);
+    tma_load_3d(smem + kAtOffK + 8192, km, tma_bar, 64, hk, row);
+    if (with_v) {
+      tma_load_3d(smem + kAtOffV, vm, tma_bar, 0, hk, row);
+      tma_load_3d(smem + kAtOffV + 8192, vm, tma_bar, 64, hk, row);
+    }
+    if (!mbar_wait_suspend(tma_bar, (tma_phase - 1) & 1, abort)) return;
+    tc_fence_after_sync();
+    const uint32_t sQ = smem_addr(smem + kAtOffQ), sK = smem_addr(smem + kAtOffK);
+    constexpr uint32_t id_s = idesc_bf16_f32(128, kAtKeys, 0, 0);
+#pragma unroll
+    for (int s = 0; s < kAtD / 16; ++s) {
+      const uint64_t ad = smem_desc(sQ + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024, kSwizzle128B);
+      const uint64_t bd = smem_desc(sK + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024, kSwizzle128B);
+      umma_bf16(tS, ad, bd, id_s, s > 0);
+    }
+    umma_commit(mma_bar);
+  };
+  auto tile_sync = [&]() {
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+  };
+  // every thread: wait for the latest products (bounded; the CTA agrees on the outcome)
+  auto wait_mma = [&]() -> bool {
+    const bool ok = mbar_wait_or_abort(mma_bar, mma_phase & 1, abort);
+    ++mma_phase;
+    return __syncthreads_and(ok) != 0;
+  };
+  // this row's 64 logits of tile t, scaled, masked to -inf
+  auto read_logits = [&](int t, float (&x)[kAtKeys]) {
+    float r[32];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      tmem_ld32(tS + lane_base + h * 32, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < 32; ++c) x[h * 32 + c] = r[c] * a.scale;
+    }
+    if (t < nt_pre) {
+      const int lim = P - t * kAtKeys;  // keys t*64 + c with c < lim are cached context
+#pragma unroll
+      for (int c = 0; c < kAtKeys; ++c)
+        if (c >= lim || !row_live) x[c] = -INFINITY;
+    } else {
+      const int s0 = (t - nt_pre) * kAtKeys;
+      const uint64_t mk = s0 == 0 ? m_lo : m_hi;
+#pragma unroll
+      for (int c = 0; c < kAtKeys; ++c)
+        if (s0 + c >= N || !((mk >> c) & 1ull)) x[c] = -INFINITY;
+    }
+  };
+
+  bool ok = true;
+  // ---- pass 1: row maximum and normaliser
+  float m = -INFINITY, l = 0.f;
+  for (int t = 0; t < nt && ok; ++t) {
+    tile_sync();
+    load_and_score(t, false, t == 0);
+    ok = wait_mma();
+    if (!ok) break;
+    tc_fence_after_sync();
+    float x[kAtKeys];
+    read_logits(t, x);
+    float mt_ = m;
+#pragma unroll
+    for (int c = 0; c < kAtKeys; ++c) mt_ = fmaxf(mt_, x[c]);
+    if (mt_ > -INFINITY) {
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < kAtKeys; ++c) sum += __expf(x[c] - mt_);
+      l = l * __expf(m - mt_) + sum;
+      m = mt_;
+    }
+  }
+  const float inv_l = l > 0.f ? 1.f / l : 0.f;
+  // ---- pass 2: P = exp(logit - m) / l as a bf16 operand, O += P V
+  for (int t = 0; t < nt && ok; ++t) {
+    tile_sync();
+    load_and_score(t, true, false);
+    ok = wait_mma();
+    if (!ok) break;
+    tc_fence_after_sync();
+    float x[kAtKeys];
+    read_logits(t, x);
+#pragma unroll
+    for (int c8 = 0; c8 < kAtKeys / 8; ++c8) {
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float p0 = l > 0.f ? __expf(x[c8 * 8 + 2 * i] - m) * inv_l : 0.f;
+        const float p1 = l > 0.f ? __expf(x[c8 * 8 + 2 * i + 1] - m) * inv_l : 0.f;
+        const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
+        w[i] = *reinterpret_cast<const uint32_t*>(&pp);
+      }
+      *reinterpret_cast<uint4*>(smem + kAtOffP + at_swz(tid, c8)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after_sync();
+      const uint32_t sP = smem_addr(smem + kAtOffP), sV = smem_addr(smem + kAtOffV);
+      constexpr uint32_t id_o = idesc_bf16_f32(128, 64, 0, 1);
+#pragma unroll
+      for (int s = 0; s < kAtKeys / 16; ++s) {
+        const uint64_t ad = smem_desc(sP + s * 32, 16, 1024, kSwizzle128B);
+#pragma unroll
+        for (int at = 0; at < 2; ++at) {
+          const uint64_t bd = smem_desc(sV + at * 8192 + s * 2048, 1024, 1024, kSwizzle128B);
+          umma_bf16(tO + at * 64, ad, bd, id_o, (t > 0 || s > 0) ? 1u : 0u);
+        }
+      }
+      umma_commit(mma_bar);
+    }
+    ok = wait_mma();
+  }
+  // ---- epilogue: O rows to global (bf16)
+  if (ok) {
+    tc_fence_after_sync();
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float r[32];
+      tmem_ld32(tO + lane_base + q * 32, r);
+      tmem_ld_wait();
+      if (row_live) {
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 pp =
+                __floats2bfloat162_rn(r[c8 * 8 + 2 * i], r[c8 * 8 + 2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t*>(&pp);
+          }
+          reinterpret_cast<uint4*>(orow)[q * 4 + c8] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    }
+  } else if (tid == 0) {
+    // an expired wait: report it, and let the latest copy and products land (bounded)
+    atomicCAS(&a.status[b], TGDN_SEQ_OK, TGDN_SEQ_TIMEOUT);
+    if (tma_phase > 0) (void)mbar_wait(tma_bar, (tma_phase - 1) & 1);
+    if (mma_phase > 0) (void)mbar_wait(mma_bar, (mma_phase - 1) & 1);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kAtTmemCols);
+  }
+}
+
+bool tree_attn_supported(const tgdn_tree& t, int H_q, int H_kv, int d) {
+  const int G = H_kv > 0 ? H_q / H_kv : 0;
+  return d == kAtD && H_kv > 0 && H_q % H_kv == 0 && (G == 1 || G == 2 || G == 4 || G == 8 ||
+                                                      G == 16) &&
+         t.n_max <= kAtMaxNodes;
+}
+
+cudaError_t launch_tree_attn(const tgdn_tree& t, int H_q, int H_kv, int P_max, float scale,
+                             const CUtensorMap& qmap, const CUtensorMap& ktmap,
+                             const CUtensorMap& vtmap, const CUtensorMap& kcmap,
+                             const CUtensorMap& vcmap, const int32_t* prefix_len, void* o,
+                             cudaStream_t s) {
+  AtArgs a;
+  a.H_q = H_q;
+  a.H_kv = H_kv;
+  a.G = H_q / H_kv;
+  a.n_max = t.n_max;
+  a.P_max = P_max;
+  a.mtiles = (t.n_max * a.G + kAtThreads - 1) / kAtThreads;
+  const long items = (long)t.B * H_kv * a.mtiles;
+  if (items == 0) return cudaSuccess;
+  if (items > 0x7fffffffL) return cudaErrorInvalidConfiguration;
+  a.n_items = (int)items;
+  a.scale = scale;
+  a.cu = t.cu_nodes;
+  a.order = t.order;
+  a.pos = t.pos;
+  a.anc = t.anc;
+  a.words = t.words;
+  a.status = t.status;
+  a.prefix_len = prefix_len;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  cudaError_t e = cudaFuncSetAttribute(tree_attn_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kAtSmemBytes);
+  if (e != cudaSuccess) return e;
+  tree_attn_kernel<<<(unsigned)items, kAtThreads, kAtSmemBytes, s>>>(qmap, ktmap, vtmap, kcmap,
+                                                                     vcmap, a);
+  return cudaGetLastError();
+}
+
+}  // namespace tgdn

@@ -78,6 +78,9 @@ def lib() -> ctypes.CDLL:
         L.tgdn_tree_build.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp,
                                       vp, st]
         L.tgdn_tree_build.restype = ctypes.c_int
+        L.tgdn_tree_attention.argtypes = [P(CTree), i32, i32, i32, vp, vp, vp, vp, vp, vp, i32,
+                                          ctypes.c_float, vp, st]
+        L.tgdn_tree_attention.restype = ctypes.c_int
         L.tgdn_status_string.argtypes = [i32]
         L.tgdn_status_string.restype = ctypes.c_char_p
         L.tgdn_version.argtypes = []
@@ -272,6 +275,27 @@ def tree_build(root_token, child_logp, child_token, budget: int, w: int, depth_m
     _check(lib().tgdn_tree_build(B, budget, K, w, depth_max, *args, _stream(stream)),
            "tgdn_tree_build")
     return out
+
+
+def tree_attention(tree: Tree, q, k_tree, v_tree, k_cache, v_cache, prefix_len, o,
+                   scale: float, stream=None) -> None:
+    """tgdn_tree_attention: each node attends to its sequence's cached context and its
+    own root path.  q/o [T][H_q][d], k_tree/v_tree [T][H_kv][d], k_cache/v_cache
+    [B][P_max][H_kv][d] (bf16), prefix_len [B] int32."""
+    T, B = tree.T, tree.B
+    H_q, d = q.shape[1], q.shape[2]
+    H_kv = k_tree.shape[1]
+    P_max = k_cache.shape[1] if k_cache is not None else 0
+    bf = torch.bfloat16
+    ncache = B * P_max * H_kv * d
+    args = (_dev(q, bf, T * H_q * d, "q"), _dev(k_tree, bf, T * H_kv * d, "k_tree"),
+            _dev(v_tree, bf, T * H_kv * d, "v_tree"),
+            _dev(k_cache, bf, ncache, "k_cache") if P_max > 0 else None,
+            _dev(v_cache, bf, ncache, "v_cache") if P_max > 0 else None,
+            _dev(prefix_len, torch.int32, B, "prefix_len"))
+    _check(lib().tgdn_tree_attention(ctypes.byref(tree.c()), H_q, H_kv, d, *args, P_max,
+                                     float(scale), _dev(o, bf, T * H_q * d, "o"),
+                                     _stream(stream)), "tgdn_tree_attention")
 
 
 def accept(tree: Tree, draft_ids, target_ids, accept_node, accept_len, path, stream=None) -> None:
