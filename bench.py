@@ -66,11 +66,12 @@ def parse():
     ap.add_argument("--mode", default="fused", choices=["fused", "separate"],
                     help="fused: commit folded into the next step's verify; separate: own pass")
     ap.add_argument("--part", default="stack",
-                    choices=["stack", "recurrent", "build", "attention"],
+                    choices=["stack", "recurrent", "build", "attention", "configs"],
                     help="stack: the decode benchmark (default); recurrent: single-pass verify "
                          "vs per-branch recurrent verify by tree size; build: top-w tree "
                          "construction kernel times; attention: ancestor-masked tree "
-                         "attention kernel times")
+                         "attention kernel times; configs: verify and commit per launch on "
+                         "the single-layer workloads, with the oracle's time beside them")
     return ap.parse_args()
 
 
@@ -642,13 +643,76 @@ def run_attention_times(args):
             "peak_hbm_gbs": hbm, "peak_kind": kind, "cases": out}
 
 
+def run_config_times(args):
+    """tgdn_verify and tgdn_commit per launch on the single-layer workloads (one B=1 top-4
+    tree; 16 x 64-node random trees; 64 mixed chains and 129-node top-8 trees), against the
+    measured HBM copy bandwidth, with the oracle's all-core time for the same launch."""
+    import torch
+    import oracle
+    from tree_speculative_decoding_gated_gb300 import tgdn
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(dev)
+    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    hbm, kind = peaks()
+    out = []
+    for name in ("cfg2", "cfg3", "cfg4"):
+        p = synth.make_problem(name)
+        cfg, t, i = p.cfg, p.trees, p.inputs
+        tree = tgdn.Tree.from_host(t.cu_nodes, t.parent, t.n_max, t.depth_max, dev)
+        dims = tgdn.Dims(cfg.H_qk, cfg.H_v, cfg.dk, cfg.dv, tgdn.BF16)
+        bf = lambda x: torch.from_numpy(synth.bf16_bits(x)).view(torch.bfloat16).to(dev)
+        f32 = lambda x: torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(dev)
+        q, k, v, g, b, S0 = bf(i.q), bf(i.k), bf(i.v), f32(i.g), f32(i.b), f32(p.S0)
+        o = torch.empty((t.T, cfg.H_v, cfg.dv), dtype=torch.bfloat16, device=dev)
+        ws = tgdn.alloc_workspace(tree, dims, dev)
+        S = torch.empty_like(S0)
+        an = torch.empty(t.B, dtype=torch.int32, device=dev)
+        al = torch.empty_like(an)
+        path = torch.empty((t.B, t.depth_max + 1), dtype=torch.int32, device=dev)
+        draft = torch.from_numpy(p.draft_ids).to(dev)
+        target = torch.from_numpy(p.target_ids).to(dev)
+        with torch.cuda.stream(stream):
+            tgdn.tree_prep(tree, stream)
+            tgdn.verify(tree, dims, q, k, v, g, b, S0, o, ws, stream)
+            tgdn.accept(tree, draft, target, an, al, path, stream)
+        fv = lambda: tgdn.verify(tree, dims, q, k, v, g, b, S0, o, ws, stream)
+        fc = lambda: tgdn.commit(tree, dims, an, k, ws, S0, S, stream)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fv()
+                fc()
+        tv = _launch_times(torch, stream, fv, 30, flush)
+        tcm = _launch_times(torch, stream, fc, 30, flush)
+        vb = t.B * S0_BYTES_PER_SEQ + t.T * NODE_BYTES
+        cb = 2 * t.B * S0_BYTES_PER_SEQ
+        t0 = time.perf_counter()
+        _, used = oracle.verify(t.cu_nodes, t.parent, t.n_max, t.depth_max, i.q, i.k, i.v, i.g,
+                                i.b, p.S0, return_threads=True)
+        acc = oracle.accept(t.cu_nodes, t.parent, t.n_max, t.depth_max, p.draft_ids,
+                            p.target_ids)
+        oracle.commit(t.cu_nodes, t.parent, t.n_max, t.depth_max, i.k, i.v, i.g, i.b, p.S0,
+                      acc["accept_node"])
+        t_or = time.perf_counter() - t0
+        kern = "verify_tc_kernel" if t.n_max <= 64 else "verify_simt_kernel"
+        out.append({"workload": name, "B": t.B, "nodes": t.T, "verify_kernel": kern,
+                    "verify_us": tv, "verify_frac_hbm": vb / (tv * 1e-6) / 1e9 / hbm,
+                    "commit_us": tcm, "commit_frac_hbm": cb / (tcm * 1e-6) / 1e9 / hbm,
+                    "nodes_per_s_verify": t.T / (tv * 1e-6),
+                    "nodes_per_s_verify_commit": t.T / ((tv + tcm) * 1e-6),
+                    "oracle_ms": 1e3 * t_or, "oracle_cores": used})
+    return {"part": "configs", "metric": "per-launch verify and commit on the single-layer "
+            "workloads, L2 flushed before every launch", "unit": "us", "peak_hbm_gbs": hbm,
+            "peak_kind": kind, "cases": out}
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
     if args.part != "stack":
         if rank == 0:
             fn = {"recurrent": run_recurrent_compare, "build": run_build_times,
-                  "attention": run_attention_times}[args.part]
+                  "attention": run_attention_times, "configs": run_config_times}[args.part]
             print(json.dumps(fn(args)), flush=True)
         return
     if args.impl == "reference":

@@ -165,23 +165,35 @@ verify_simt_kernel(int n_max, int depth_max, int H_qk, int H_v, int dk, int dv,
     return;
   }
 
-  // --- ancestor-masked Gram entries: X (strict ancestors, x b_n) and Y (ancestors + self)
-  for (int it = tid; it < N * DM1; it += kSimtThreads) {
-    const int n = it / DM1, d = it % DM1;
-    if (d > dep[n]) continue;
-    const int s = anc_at[it];
-    const T* kn = k + ((size_t)(lo + n) * H_qk + qh) * dk;
-    const T* qn = q + ((size_t)(lo + n) * H_qk + qh) * dk;
-    const T* ks = k + ((size_t)(lo + s) * H_qk + qh) * dk;
-    float kk = 0.f, qk = 0.f;
-    for (int i = 0; i < dk; ++i) {
-      const float kv = Io<T>::load(ks + i);
-      kk = fmaf(Io<T>::load(kn + i), kv, kk);
-      qk = fmaf(Io<T>::load(qn + i), kv, qk);
+  // --- ancestor-masked Gram entries: X (strict ancestors, x b_n) and Y (ancestors + self).
+  // One warp per (node, ancestor) pair: the lanes split d_k, so the three rows are read
+  // with coalesced loads, and a warp sum finishes each dot product.
+  {
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int it = warp; it < N * DM1; it += kSimtThreads / 32) {
+      const int n = it / DM1, d = it % DM1;
+      if (d > dep[n]) continue;
+      const int s = anc_at[it];
+      const T* kn = k + ((size_t)(lo + n) * H_qk + qh) * dk;
+      const T* qn = q + ((size_t)(lo + n) * H_qk + qh) * dk;
+      const T* ks = k + ((size_t)(lo + s) * H_qk + qh) * dk;
+      float kk = 0.f, qk = 0.f;
+      for (int i = lane; i < dk; i += 32) {
+        const float kv = Io<T>::load(ks + i);
+        kk = fmaf(Io<T>::load(kn + i), kv, kk);
+        qk = fmaf(Io<T>::load(qn + i), kv, qk);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        kk += __shfl_xor_sync(0xffffffffu, kk, off);
+        qk += __shfl_xor_sync(0xffffffffu, qk, off);
+      }
+      if (lane == 0) {
+        const float e = expf(G[n] - G[s]);
+        YS[it] = e * qk;
+        XS[it] = (d < dep[n]) ? bb[n] * e * kk : 0.f;
+      }
     }
-    const float e = expf(G[n] - G[s]);
-    YS[it] = e * qk;
-    XS[it] = (d < dep[n]) ? bb[n] * e * kk : 0.f;
   }
   // --- right-hand side R = diag(b) (V - diag(e^G) K S0), stored in U
   for (int it = tid; it < N * kSimtCols; it += kSimtThreads) {
