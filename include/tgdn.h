@@ -151,9 +151,10 @@ size_t tgdn_verify_workspace_bytes(const tgdn_tree* tree, const tgdn_dims* dims)
  *   ws    tgdn_verify_workspace_bytes() bytes, 256-byte aligned, written
  * tgdn_tree_prep must have run on `tree` (same stream or ordered before).
  * A sequence with a bad status gets zero outputs and zero workspace rows.
- * bf16 io with d_k = d_v = 128 runs the tensor-core kernel when
- * n_max <= 64 and depth_max <= 30; every other valid case runs the fp32 SIMT
- * kernel.  Returns TGDN_OK, TGDN_EINVAL, TGDN_ETOOBIG or TGDN_ECUDA. */
+ * bf16 io with d_k = d_v = 128 and depth_max <= 30 runs a tensor-core kernel
+ * (two items per SM in flight when n_max <= 64, one when n_max <= 128); every
+ * other valid case runs the fp32 SIMT kernel.
+ * Returns TGDN_OK, TGDN_EINVAL, TGDN_ETOOBIG or TGDN_ECUDA. */
 int tgdn_verify(const tgdn_tree* tree, const tgdn_dims* dims, const void* q, const void* k,
                 const void* v, const float* g, const float* b, const float* S0, void* o,
                 void* ws, tgdn_stream_t stream);

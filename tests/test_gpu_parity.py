@@ -63,11 +63,12 @@ def test_cfg4_full_size_sampled():
 
 
 def test_tc_and_simt_paths_agree():
-    """cfg3 through the tensor-core kernel (n_max = 64) and the SIMT kernel (n_max = 65)."""
+    """cfg3 through the 64-node tensor-core kernel (n_max = 64), the 128-node tensor-core
+    kernel (n_max = 65) and the SIMT kernel (n_max = 129)."""
     p = synth.make_problem("cfg3")
     ref = oracle_step(p)
     outs = []
-    for n_max in (64, 65):
+    for n_max in (64, 65, 129):
         tree, dims, dev = upload(p, n_max=n_max)
         got = run_step(tree, dims, dev)
         eo = rel_fro_blocks(got["o"], ref["o"], p.trees.cu_nodes)

@@ -129,11 +129,47 @@ def test_kernel_limits(case):
     run_and_check(p, TOL_BF16)
 
 
+def _relabel(par, new_root):
+    """The same tree with its nodes renumbered so that the root gets index new_root."""
+    N = len(par)
+    perm = np.roll(np.arange(N), new_root)      # new index -> old index, perm[new_root] = 0
+    inv = np.argsort(perm)
+    return np.array([-1 if par[perm[i]] == -1 else inv[par[perm[i]]] for i in range(N)],
+                    np.int32)
+
+
+@pytest.mark.parametrize("case", ["random", "deep", "chain60", "star128", "ragged", "fold129"])
+def test_trees_of_65_to_128_nodes(case):
+    """The 128-node tensor-core kernel: full, deep, chain and star trees, and a ragged batch
+    with empty and invalid sequences."""
+    rng = np.random.default_rng(41)
+    if case == "random":
+        parents = [synth.random_recursive_tree(rng, int(n), 16) for n in (65, 90, 128, 100)]
+    elif case == "deep":       # depth 30, the kernel's bound
+        parents = [synth.random_recursive_tree(rng, 128, 30), synth.chain_tree(31)]
+    elif case == "chain60":    # above the depth bound: SIMT kernel
+        parents = [synth.chain_tree(60), synth.random_recursive_tree(rng, 90, 8)]
+    elif case == "star128":
+        parents = [np.array([-1] + [0] * 127, np.int32), synth.random_recursive_tree(rng, 70, 3)]
+    elif case == "ragged":
+        parents = [synth.random_recursive_tree(rng, 120, 12), np.zeros(0, np.int32),
+                   np.array([-1, 0, 3, 2], np.int32), synth.chain_tree(5),
+                   synth.random_recursive_tree(rng, 128, 20)]
+    else:   # 129 nodes: root first (folded into the state) and root in the middle (SIMT)
+        t129 = synth.top_m_tree(rng, 8, 16)
+        parents = [t129, _relabel(t129, 64), synth.random_recursive_tree(rng, 129, 14),
+                   synth.chain_tree(17), np.array([-1, 0, 3, 2], np.int32)]
+    p = custom(parents, 2, 4, 128, "bf16", 12, n_max=129 if case == "fold129" else 128)
+    got, ref = run_and_check(p, TOL_BF16)
+    if case == "ragged":
+        assert got["status"].tolist() == [0, 0, 4, 0, 0]
+
+
 @pytest.mark.parametrize("io", ["bf16", "f32"])
-def test_non_ancestor_edits_leave_outputs_bitwise(io):
+def test_non_ancestor_edits_leave_outputs_bitwise(io, n_max=None):
     rng = np.random.default_rng(21)
     par = synth.random_recursive_tree(rng, 48, 10)
-    p = custom([par], 2, 4, 128, io, 6)
+    p = custom([par], 2, 4, 128, io, 6, n_max=n_max)
     tree, dims, dev = upload(p)
     base = run_step(tree, dims, dev)
     n = 47
@@ -184,3 +220,7 @@ def test_two_step_rollback_free():
     e = rel_fro_blocks(r2["o"], ref["o"][L:], np.array([0, 20]))
     assert e <= TOL_BF16, e
     assert n_star == path[-1]
+
+
+def test_non_ancestor_edits_on_the_128_node_kernel():
+    test_non_ancestor_edits_leave_outputs_bitwise("bf16", n_max=100)

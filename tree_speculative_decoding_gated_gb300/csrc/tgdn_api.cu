@@ -129,6 +129,16 @@ int tgdn_verify(const tgdn_tree* tree, const tgdn_dims* dims, const void* q, con
     return from_cuda(tgdn::launch_verify_tc(t, d, qmap, kmap, v, g, b, const_cast<float*>(S0), o,
                                             U, G, none, s));
   }
+  if (tgdn::verify_tc128_supported(t, d, q, k, v, S0, o)) {
+    CUtensorMap qmap, kmap;
+    if (!encode_qk_map(&qmap, q, t.T, d.H_qk) || !encode_qk_map(&kmap, k, t.T, d.H_qk))
+      return TGDN_ECUDA;
+    rc = from_cuda(tgdn::launch_verify_tc128(t, d, qmap, kmap, q, k, v, g, b, S0, o, U, G, s));
+    if (rc != TGDN_OK || t.n_max < tgdn::kTc128FoldNodes) return rc;
+    // 129-node trees whose root is not node 0 (the rest of the batch is done)
+    return from_cuda(tgdn::launch_verify_simt(t, d, q, k, v, g, b, S0, o, U, G, s,
+                                              tgdn::kTc128FoldNodes));
+  }
   return from_cuda(tgdn::launch_verify_simt(t, d, q, k, v, g, b, S0, o, U, G, s));
 }
 

@@ -29,9 +29,11 @@ cudaError_t launch_accept(const tgdn_tree& t, const int32_t* draft, const int32_
                           cudaStream_t s);
 
 // fp32 SIMT verify: any valid geometry (d_k, d_v <= 128, n_max <= 256, depth_max <= 64).
+// only_n > 0: just the valid sequences of only_n nodes whose root is not node 0.
 cudaError_t launch_verify_simt(const tgdn_tree& t, const tgdn_dims& d, const void* q,
                                const void* k, const void* v, const float* g, const float* b,
-                               const float* S0, void* o, float* U, float* G, cudaStream_t s);
+                               const float* S0, void* o, float* U, float* G, cudaStream_t s,
+                               int only_n = 0);
 
 // The previous decode step's commit, folded into this step's verify: the
 // accepted root path of every sequence and the factors of that step.
@@ -49,6 +51,18 @@ struct PendingCommit {
 // Tensor-core verify: bf16 io, d_k = d_v = 128, n_max <= 64, depth_max <= 30.
 bool verify_tc_supported(const tgdn_tree& t, const tgdn_dims& d, const void* q, const void* k,
                          const void* v, const float* S0, const void* o);
+// Tensor-core verify for larger trees: bf16 io, d_k = d_v = 128, n_max <= 129,
+// depth_max <= 30; one item per SM at a time, sparse second step on CUDA cores.
+// A 129-node tree is taken when its root is node 0 (the root is folded into the
+// state); otherwise it is left for launch_verify_simt(..., only_n = 129).
+constexpr int kTc128FoldNodes = 129;
+bool verify_tc128_supported(const tgdn_tree& t, const tgdn_dims& d, const void* q,
+                            const void* k, const void* v, const float* S0, const void* o);
+cudaError_t launch_verify_tc128(const tgdn_tree& t, const tgdn_dims& d, const CUtensorMap& qmap,
+                                const CUtensorMap& kmap, const void* q, const void* k,
+                                const void* v, const float* g,
+                                const float* b, const float* S0, void* o, float* U, float* G,
+                                cudaStream_t s);
 // Whether the tensor-core verify can also apply a pending commit of `prev`.
 bool pending_commit_tc_supported(const tgdn_tree& prev, const void* prev_k);
 // With cm.path set, S is first updated in place by the pending commit and the

@@ -10,7 +10,9 @@
 // value columns are independent, only the Gram entries are shared.
 //
 // This is the exact-precision path (fp32 io, the 16x16 toy head) and the
-// general path for shapes the tensor-core kernel does not take.
+// general path for shapes the tensor-core kernels do not take.  In complement
+// mode (only_n > 0) it verifies just the valid sequences of only_n nodes whose
+// root is not node 0: the ones the 128-node tensor-core kernel leaves to it.
 #include "tgdn_device.cuh"
 #include "tgdn_kernels.h"
 
@@ -61,7 +63,7 @@ verify_simt_kernel(int n_max, int depth_max, int H_qk, int H_v, int dk, int dv,
                    const T* __restrict__ k, const T* __restrict__ v,
                    const float* __restrict__ g, const float* __restrict__ bta,
                    const float* __restrict__ S0, T* __restrict__ o, float* __restrict__ Uws,
-                   float* __restrict__ Gws) {
+                   float* __restrict__ Gws, int only_n) {
   extern __shared__ __align__(16) uint8_t smem[];
   const SimtShape sh = simt_shape(n_max, depth_max, dk);
   float* S0s = reinterpret_cast<float*>(smem + sh.s0);
@@ -89,6 +91,7 @@ verify_simt_kernel(int n_max, int depth_max, int H_qk, int H_v, int dk, int dv,
   const int tid = threadIdx.x;
   const int lo = cu[bi], N = cu[bi + 1] - lo;
   if (N <= 0) return;
+  if (only_n > 0 && !(N == only_n && status[bi] == TGDN_SEQ_OK && depth[lo] != 0)) return;
   __shared__ int s_bad;
   if (tid == 0) s_bad = (status[bi] != TGDN_SEQ_OK) || (N > n_max);
   __syncthreads();
@@ -241,7 +244,8 @@ verify_simt_kernel(int n_max, int depth_max, int H_qk, int H_v, int dk, int dv,
 template <typename T>
 static cudaError_t launch_simt_t(const tgdn_tree& t, const tgdn_dims& d, const void* q,
                                  const void* k, const void* v, const float* g, const float* b,
-                                 const float* S0, void* o, float* U, float* G, cudaStream_t s) {
+                                 const float* S0, void* o, float* U, float* G, int only_n,
+                                 cudaStream_t s) {
   const SimtShape sh = simt_shape(t.n_max, t.depth_max, d.d_k);
   const auto kern = verify_simt_kernel<T>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -254,16 +258,17 @@ static cudaError_t launch_simt_t(const tgdn_tree& t, const tgdn_dims& d, const v
   kern<<<(unsigned)grid, kSimtThreads, sh.total, s>>>(
       t.n_max, t.depth_max, d.H_qk, d.H_v, d.d_k, d.d_v, t.cu_nodes, t.parent, t.depth, t.order,
       t.status, static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), g,
-      b, S0, static_cast<T*>(o), U, G);
+      b, S0, static_cast<T*>(o), U, G, only_n);
   return cudaGetLastError();
 }
 
 cudaError_t launch_verify_simt(const tgdn_tree& t, const tgdn_dims& d, const void* q,
                                const void* k, const void* v, const float* g, const float* b,
-                               const float* S0, void* o, float* U, float* G, cudaStream_t s) {
+                               const float* S0, void* o, float* U, float* G, cudaStream_t s,
+                               int only_n) {
   if (d.io == TGDN_BF16)
-    return launch_simt_t<__nv_bfloat16>(t, d, q, k, v, g, b, S0, o, U, G, s);
-  return launch_simt_t<float>(t, d, q, k, v, g, b, S0, o, U, G, s);
+    return launch_simt_t<__nv_bfloat16>(t, d, q, k, v, g, b, S0, o, U, G, only_n, s);
+  return launch_simt_t<float>(t, d, q, k, v, g, b, S0, o, U, G, only_n, s);
 }
 
 }  // namespace tgdn
