@@ -7,12 +7,15 @@
 // ancestor-or-self bitmasks from tree prep.
 //
 // One CTA per (sequence, key/value head, tile of 128 query rows); a query row
-// is (node, query head of the group), row = node * G + g.  128 threads, one per
-// row (= TMEM lane).  Keys come in tiles of 64: first the cached context
+// is (node, query head of the group), row = node * G + g.  256 threads, two per
+// row (= TMEM lane), each taking half of every key tile and half of the output
+// columns; the halves of a row's maximum and normaliser are merged once.  Keys come in tiles of 64: first the cached context
 // (prefix_len[b] positions), then the tree's own nodes.  Two passes over the
 // key tiles: the first finds each row's maximum logit and normaliser, the
 // second forms P = exp(logit - max) / sum as a bf16 operand and accumulates
-// O = P V on the tensor cores, so O never needs rescaling.
+// O = P V on the tensor cores, so O never needs rescaling.  Key and value
+// tiles are double-buffered: the copy of the next tile is in flight while the
+// current one is scored.
 //   S tile = Q K^T: tcgen05.mma, A = Q (TMA, 128-byte swizzle), B = K tile
 //   O     += P V:   A = P (written by the threads), B = V tile (MN-major)
 // Every wait is bounded; on expiry the sequence is marked TGDN_SEQ_TIMEOUT.
@@ -21,17 +24,20 @@
 
 namespace tgdn {
 
-constexpr int kAtThreads = 128;
+constexpr int kAtThreads = 256;
+constexpr int kAtRows = 128;             // query rows per CTA
 constexpr int kAtKeys = 64;              // keys per tile
 constexpr int kAtD = 128;
 constexpr int kAtMaxNodes = 128;         // tree nodes per sequence on this kernel
 constexpr uint32_t kAtTmemCols = 256;    // S tile: cols 0-63; O: cols 64-191
 constexpr int kAtOffQ = 0;               // [2 d halves][128 rows][128 B]     32 KiB
-constexpr int kAtOffK = 32768;           // [2 d halves][64 keys][128 B]      16 KiB
-constexpr int kAtOffV = 49152;           // [2 d atoms][64 keys][128 B]       16 KiB
-constexpr int kAtOffP = 65536;           // [128 rows][64 keys] bf16          16 KiB
-constexpr int kAtOffMask = 81920;        // [kAtMaxNodes][2] uint64          2 KiB
-constexpr int kAtOffBar = kAtOffMask + kAtMaxNodes * 16;
+constexpr int kAtOffK = 32768;           // 2 x [2 d halves][64 keys][128 B]  2 x 16 KiB
+constexpr int kAtOffV = 65536;           // 2 x [2 d atoms][64 keys][128 B]   2 x 16 KiB
+// P [128 rows][64 keys] bf16 (16 KiB) is written over the key tile of its own step,
+// which the score product has finished reading.
+constexpr int kAtOffMask = 98304;        // [kAtMaxNodes][2] uint64          2 KiB
+constexpr int kAtOffStat = kAtOffMask + kAtMaxNodes * 16;  // [2][128] row max, [2][128] sum
+constexpr int kAtOffBar = kAtOffStat + 4 * kAtRows * 4;
 constexpr int kAtSmemBytes = kAtOffBar + 64 + 1024;
 
 __device__ __forceinline__ int at_swz(int row, int chunk) {
@@ -61,8 +67,8 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(at_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* amask = reinterpret_cast<uint64_t*>(smem + kAtOffMask);
-  uint64_t* tma_bar = reinterpret_cast<uint64_t*>(smem + kAtOffBar);
-  uint64_t* mma_bar = tma_bar + 1;
+  uint64_t* tma_bar = reinterpret_cast<uint64_t*>(smem + kAtOffBar);  // [2], one per buffer
+  uint64_t* mma_bar = tma_bar + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_bar + 1);
   int* s_abort = reinterpret_cast<int*>(tmem_slot + 1);
 
@@ -73,22 +79,25 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   const int b = item / (a.mtiles * a.H_kv);
   const int tid = threadIdx.x, warp = tid >> 5;
   const int lo = a.cu[b], N = a.cu[b + 1] - lo;
-  const int npt = kAtThreads / a.G;          // nodes per tile of query rows
+  const int npt = kAtRows / a.G;             // nodes per tile of query rows
   const int node0 = mt * npt;
   if (N <= 0 || node0 >= N) return;          // no rows of this tile exist
-  const int my_node = node0 + tid / a.G, my_g = tid % a.G;
+  const int row = tid & (kAtRows - 1), kh = tid >> 7;  // TMEM lane; key / column half
+  const int my_node = node0 + row / a.G, my_g = row % a.G;
   const bool row_live = my_node < N;
   __nv_bfloat16* orow =
       a.o + ((size_t)(lo + my_node) * a.H_q + hk * a.G + my_g) * kAtD;
   if (a.status[b] != TGDN_SEQ_OK || N > kAtMaxNodes || N > a.n_max) {
     if (row_live)
-      for (int c = 0; c < kAtD / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = make_uint4(0, 0, 0, 0);
+      for (int c = kh * 8; c < kh * 8 + 8; ++c)
+        reinterpret_cast<uint4*>(orow)[c] = make_uint4(0, 0, 0, 0);
     return;
   }
   const int P = max(0, min(a.prefix_len[b], a.P_max));
 
   if (tid == 0) {
-    mbar_init(tma_bar, 1);
+    mbar_init(&tma_bar[0], 1);
+    mbar_init(&tma_bar[1], 1);
     mbar_init(mma_bar, 1);
     fence_mbar_init();
     *s_abort = 0;
@@ -118,41 +127,54 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tS = tmem, tO = tmem + 64;
-  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
   volatile int* abort = s_abort;
 
   const int nt_pre = (P + kAtKeys - 1) / kAtKeys;
   const int nt_tree = (N + kAtKeys - 1) / kAtKeys;
   const int nt = nt_pre + nt_tree;
-  uint32_t tma_phase = 0, mma_phase = 0;
+  uint32_t mma_phase = 0;
   const uint64_t m_lo = row_live ? amask[2 * my_node] : 0;
   const uint64_t m_hi = row_live ? amask[2 * my_node + 1] : 0;
 
-  // thread 0: the key (and value) tile t into shared memory, then S = Q K^T.
-  // Called once every thread is done with the previous tile's S and P.  On an
-  // expired wait it raises *abort and commits nothing (wait_mma then gives up).
-  auto load_and_score = [&](int t, bool with_v, bool first) {
-    if (tid != 0) return;
-    ++tma_phase;
+  // Steps u = 0 .. 2 nt - 1: pass u / nt, key tile u % nt, buffer u & 1.
+  const int steps = 2 * nt;
+  int tma_issued[2] = {0, 0};  // copies issued per buffer (thread 0)
+  // thread 0: the key (and, in the second pass, value) tile of step u into buffer u & 1
+  auto issue_tile = [&](int u) {
+    const int t = u < nt ? u : u - nt, buf = u & 1;
+    const bool with_v = u >= nt;
     const bool pre = t < nt_pre;
     const int row = pre ? b * a.P_max + t * kAtKeys : lo + (t - nt_pre) * kAtKeys;
     const CUtensorMap* km = pre ? &kcmap : &ktmap;
     const CUtensorMap* vm = pre ? &vcmap : &vtmap;
-    uint32_t bytes = 2 * kAtKeys * 128 + (with_v ? 2 * kAtKeys * 128 : 0) + (first ? 32768 : 0);
-    mbar_arrive_expect_tx(tma_bar, bytes);
-    if (first) {
-      tma_load_3d(smem + kAtOffQ, &qmap, tma_bar, 0, hk * a.G, lo + node0);
-      tma_load_3d(smem + kAtOffQ + 16384, &qmap, tma_bar, 64, hk * a.G, lo + node0);
+    uint64_t* bar = &tma_bar[buf];
+    const uint32_t bytes = 2 * kAtKeys * 128 * (with_v ? 2 : 1) + (u == 0 ? 32768 : 0);
+    mbar_arrive_expect_tx(bar, bytes);
+    if (u == 0) {
+      tma_load_3d(smem + kAtOffQ, &qmap, bar, 0, hk * a.G, lo + node0);
+      tma_load_3d(smem + kAtOffQ + 16384, &qmap, bar, 64, hk * a.G, lo + node0);
     }
-    tma_load_3d(smem + kAtOffK, km, tma_bar, 0, hk, row);
-    tma_load_3d(smem + kAtOffK + 8192, km, tma_bar, 64, hk, row);
+    uint8_t* kdst = smem + kAtOffK + buf * 16384;
+    tma_load_3d(kdst, km, bar, 0, hk, row);
+    tma_load_3d(kdst + 8192, km, bar, 64, hk, row);
     if (with_v) {
-      tma_load_3d(smem + kAtOffV, vm, tma_bar, 0, hk, row);
-      tma_load_3d(smem + kAtOffV + 8192, vm, tma_bar, 64, hk, row);
+      uint8_t* vdst = smem + kAtOffV + buf * 16384;
+      tma_load_3d(vdst, vm, bar, 0, hk, row);
+      tma_load_3d(vdst + 8192, vm, bar, 64, hk, row);
     }
-    if (!mbar_wait_suspend(tma_bar, (tma_phase - 1) & 1, abort)) return;
+    tma_issued[buf] += 1;
+  };
+  // thread 0, once every thread is done with the previous step: start the copy of
+  // step u + 1 (its buffer's last readers have completed), then S = Q K^T of step u.
+  // On an expired wait it raises *abort and commits nothing (wait_mma then gives up).
+  auto load_and_score = [&](int u) {
+    if (tid != 0) return;
+    if (u + 1 < steps) issue_tile(u + 1);
+    const int buf = u & 1;
+    if (!mbar_wait_suspend(&tma_bar[buf], (u >> 1) & 1, abort)) return;
     tc_fence_after_sync();
-    const uint32_t sQ = smem_addr(smem + kAtOffQ), sK = smem_addr(smem + kAtOffK);
+    const uint32_t sQ = smem_addr(smem + kAtOffQ), sK = smem_addr(smem + kAtOffK + buf * 16384);
     constexpr uint32_t id_s = idesc_bf16_f32(128, kAtKeys, 0, 0);
 #pragma unroll
     for (int s = 0; s < kAtD / 16; ++s) {
@@ -173,64 +195,73 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
     ++mma_phase;
     return __syncthreads_and(ok) != 0;
   };
-  // this row's 64 logits of tile t, scaled, masked to -inf
-  auto read_logits = [&](int t, float (&x)[kAtKeys]) {
-    float r[32];
+  // this thread's 32 logits of tile t (keys kh * 32 ..), scaled, masked to -inf
+  constexpr int kHalf = kAtKeys / 2;
+  auto read_logits = [&](int t, float (&x)[kHalf]) {
+    tmem_ld32(tS + lane_base + kh * kHalf, x);
+    tmem_ld_wait();
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      tmem_ld32(tS + lane_base + h * 32, r);
-      tmem_ld_wait();
-#pragma unroll
-      for (int c = 0; c < 32; ++c) x[h * 32 + c] = r[c] * a.scale;
-    }
+    for (int c = 0; c < kHalf; ++c) x[c] *= a.scale;
     if (t < nt_pre) {
-      const int lim = P - t * kAtKeys;  // keys t*64 + c with c < lim are cached context
+      const int lim = P - t * kAtKeys - kh * kHalf;  // keys below lim are cached context
 #pragma unroll
-      for (int c = 0; c < kAtKeys; ++c)
+      for (int c = 0; c < kHalf; ++c)
         if (c >= lim || !row_live) x[c] = -INFINITY;
     } else {
-      const int s0 = (t - nt_pre) * kAtKeys;
-      const uint64_t mk = s0 == 0 ? m_lo : m_hi;
+      const int s0 = (t - nt_pre) * kAtKeys + kh * kHalf;
+      const uint64_t mk = (s0 < 64 ? m_lo : m_hi) >> (s0 & 63);
 #pragma unroll
-      for (int c = 0; c < kAtKeys; ++c)
+      for (int c = 0; c < kHalf; ++c)
         if (s0 + c >= N || !((mk >> c) & 1ull)) x[c] = -INFINITY;
     }
   };
 
   bool ok = true;
+  if (tid == 0) issue_tile(0);
   // ---- pass 1: row maximum and normaliser
   float m = -INFINITY, l = 0.f;
   for (int t = 0; t < nt && ok; ++t) {
     tile_sync();
-    load_and_score(t, false, t == 0);
+    load_and_score(t);
     ok = wait_mma();
     if (!ok) break;
     tc_fence_after_sync();
-    float x[kAtKeys];
+    float x[kHalf];
     read_logits(t, x);
     float mt_ = m;
 #pragma unroll
-    for (int c = 0; c < kAtKeys; ++c) mt_ = fmaxf(mt_, x[c]);
+    for (int c = 0; c < kHalf; ++c) mt_ = fmaxf(mt_, x[c]);
     if (mt_ > -INFINITY) {
       float sum = 0.f;
 #pragma unroll
-      for (int c = 0; c < kAtKeys; ++c) sum += __expf(x[c] - mt_);
+      for (int c = 0; c < kHalf; ++c) sum += __expf(x[c] - mt_);
       l = l * __expf(m - mt_) + sum;
       m = mt_;
     }
   }
+  {  // merge the two halves of each row
+    float* st = reinterpret_cast<float*>(smem + kAtOffStat);
+    st[kh * kAtRows + row] = m;
+    st[(2 + kh) * kAtRows + row] = l;
+    __syncthreads();
+    const float m0 = st[row], m1 = st[kAtRows + row];
+    const float l0 = st[2 * kAtRows + row], l1 = st[3 * kAtRows + row];
+    m = fmaxf(m0, m1);
+    l = m > -INFINITY ? l0 * __expf(m0 - m) + l1 * __expf(m1 - m) : 0.f;
+  }
   const float inv_l = l > 0.f ? 1.f / l : 0.f;
   // ---- pass 2: P = exp(logit - m) / l as a bf16 operand, O += P V
   for (int t = 0; t < nt && ok; ++t) {
+    const int u = nt + t;
     tile_sync();
-    load_and_score(t, true, false);
+    load_and_score(u);
     ok = wait_mma();
     if (!ok) break;
     tc_fence_after_sync();
-    float x[kAtKeys];
+    float x[kHalf];
     read_logits(t, x);
 #pragma unroll
-    for (int c8 = 0; c8 < kAtKeys / 8; ++c8) {
+    for (int c8 = 0; c8 < kHalf / 8; ++c8) {
       uint32_t w[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -239,14 +270,16 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
         const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
         w[i] = *reinterpret_cast<const uint32_t*>(&pp);
       }
-      *reinterpret_cast<uint4*>(smem + kAtOffP + at_swz(tid, c8)) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(smem + kAtOffK + (u & 1) * 16384 + at_swz(row, kh * 4 + c8)) =
+          make_uint4(w[0], w[1], w[2], w[3]);
     }
     fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
     if (tid == 0) {
       tc_fence_after_sync();
-      const uint32_t sP = smem_addr(smem + kAtOffP), sV = smem_addr(smem + kAtOffV);
+      const uint32_t sP = smem_addr(smem + kAtOffK + (u & 1) * 16384);
+      const uint32_t sV = smem_addr(smem + kAtOffV + (u & 1) * 16384);
       constexpr uint32_t id_o = idesc_bf16_f32(128, 64, 0, 1);
 #pragma unroll
       for (int s = 0; s < kAtKeys / 16; ++s) {
@@ -265,7 +298,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   if (ok) {
     tc_fence_after_sync();
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 2 * kh; q < 2 * kh + 2; ++q) {  // this thread's 64 output columns
       float r[32];
       tmem_ld32(tO + lane_base + q * 32, r);
       tmem_ld_wait();
@@ -286,7 +319,8 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   } else if (tid == 0) {
     // an expired wait: report it, and let the latest copy and products land (bounded)
     atomicCAS(&a.status[b], TGDN_SEQ_OK, TGDN_SEQ_TIMEOUT);
-    if (tma_phase > 0) (void)mbar_wait(tma_bar, (tma_phase - 1) & 1);
+    for (int bf = 0; bf < 2; ++bf)
+      if (tma_issued[bf] > 0) (void)mbar_wait(&tma_bar[bf], (tma_issued[bf] - 1) & 1);
     if (mma_phase > 0) (void)mbar_wait(mma_bar, (mma_phase - 1) & 1);
   }
   tc_fence_before_sync();
@@ -315,7 +349,7 @@ cudaError_t launch_tree_attn(const tgdn_tree& t, int H_q, int H_kv, int P_max, f
   a.G = H_q / H_kv;
   a.n_max = t.n_max;
   a.P_max = P_max;
-  a.mtiles = (t.n_max * a.G + kAtThreads - 1) / kAtThreads;
+  a.mtiles = (t.n_max * a.G + kAtRows - 1) / kAtRows;
   const long items = (long)t.B * H_kv * a.mtiles;
   if (items == 0) return cudaSuccess;
   if (items > 0x7fffffffL) return cudaErrorInvalidConfiguration;
