@@ -596,6 +596,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             const float y = t_row ? ((jj == dn) ? 1.f : 0.f)
                                   : __expf(Gn - Gj) * GR[qrow * 64 + swz(qrow, cj) * 4 + wj];
             float acc = 0.f;
+#pragma unroll 4
             for (int i = jj + 1; i <= dn; ++i) {
               const int pi = P[i * kTcNodes];
               acc = fmaf(SS[i], GR[pi * 64 + swz(pi, cj) * 4 + wj], acc);

@@ -399,6 +399,7 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
           const float inv_phi = __expf(fmaxf(Gn - Gj, -80.f));
           const float y = t_row ? ((jj == dn) ? 1.f : 0.f) : __expf(Gn - Gj) * GQ[sn * kT8Path + jj];
           float acc = 0.f;
+#pragma unroll 4
           for (int i = jj + 1; i <= dn; ++i)
             acc = fmaf(SS[i], GK[M.anc_at[i][sn] * kT8Path + jj], acc);
           const float rj = y - inv_phi * acc;
