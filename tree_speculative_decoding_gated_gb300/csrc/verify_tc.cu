@@ -12,11 +12,13 @@
 // path of n: it solves a (depth+1)-sized unit triangular system.  So
 // U = T R and O = diag(e^G) Q S0 + W R, both tensor-core products.
 //
-// Persistent, warp-specialised kernel: one CTA per SM, 16 warps, looping over
-// work items (sequence, v-head) that cover all 128 value columns; trees have
-// at most 64 nodes and depth at most 30.  Two items are in flight per SM:
+// Persistent, warp-specialised kernel: one CTA per SM, 16 warps, looping over a
+// contiguous run of work items (sequence, v-head) that cover all 128 value
+// columns; trees have at most 64 nodes and depth at most 30.  Two items are in
+// flight per SM:
 //   producer warps 0-7, item j+1:
-//     tree metadata (prefetched) -> root paths and path-cumulative gates;
+//     tree metadata (prefetched) -> root paths (reused for the next head of the
+//     same sequence) and path-cumulative gates;
 //     S0 (prefetched into registers) -> bf16 hi + lo operands (~16-bit products);
 //     TMA of the item's key and query rows -> A = [K; Q] (128-byte swizzle);
 //     tcgen05.mma into TMEM half (j+1)&1:
@@ -153,7 +155,15 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
   volatile int* abort = &sh.abort;
   const int tid = threadIdx.x, warp = tid >> 5;
   if ((int)blockIdx.x >= n_items) return;
-  const int stride = gridDim.x;
+  // Item order.  With a pending commit the producer warps are the critical path,
+  // so each CTA takes a contiguous run of items: consecutive items are mostly the
+  // heads of one sequence, whose root paths are then reused.  Otherwise the items
+  // are dealt round robin, so that the CTAs work on neighbouring heads of the
+  // same rows at the same time (better DRAM locality for the v, U and o rows).
+  const bool runs = cm.path != nullptr;
+  const int i_begin = runs ? (int)(((long)blockIdx.x * n_items) / gridDim.x) : (int)blockIdx.x;
+  const int i_end = runs ? (int)(((long)(blockIdx.x + 1) * n_items) / gridDim.x) : n_items;
+  const int i_step = runs ? 1 : (int)gridDim.x;
   const int grp = H_v / H_qk;  // v-heads per query/key head
   const bool fused = cm.path != nullptr;
 
@@ -264,12 +274,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         pf.bb = bta[(size_t)(pf.lo + p) * H_v + h];
       }
     };
-    int item = blockIdx.x;
+    int item = i_begin;
     uint32_t mma1_count = 0;  // first products issued so far (thread 0)
     load_seq(item);
     if (p == 0) issue_kq(item, q_lo);
     load_meta(item);
-    if (item + stride < n_items) load_seq(item + stride);
+    if (item + i_step < i_end) load_seq(item + i_step);
     load_s0(item);
     if (fused) {
       if (p < 32) {
@@ -280,7 +290,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       stage_commit(item);
     }
 
-    for (int j = 0; item < n_items; ++j, item += stride) {
+    int prev_bi = -1;  // sequence of the previous item when its tree was valid
+    for (int j = 0; item < i_end; ++j, item += i_step) {
       const int slot = j & 1;
       ItemMeta& M = sh.meta[slot];
       // the consumer has finished item j-2, the previous user of this half and slot
@@ -377,17 +388,30 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       }
       fence_proxy_async_smem();
       // prefetch the next item while this one is finished
-      const int next = item + stride;
-      if (next < n_items) {  // the small loads first: they are not queued behind S0
+      const int next = item + i_step;
+      if (next < i_end) {  // the small loads first: they are not queued behind S0
         load_meta(next);
-        if (next + stride < n_items) load_seq(next + stride);
+        if (next + i_step < i_end) load_seq(next + i_step);
         if (fused && p < 32) load_commit_meta(next);
         load_s0(next);
       }
       ok = named_sync_and(kBarP, kGroup, ok);
       // root paths from the ancestor masks (bits = topological positions,
-      // ascending = root first) and path-cumulative log-gates
-      if (ok && p < N) {
+      // ascending = root first) and path-cumulative log-gates; the same tree as
+      // the previous item (another head) reuses its paths and only sums the gates
+      const bool reuse = prev_bi == bi;
+      if (ok && p < N && reuse) {
+        const int dn = M.dep[p];
+        const ItemMeta& Mp = sh.meta[slot ^ 1];
+        float acc = 0.f;
+#pragma unroll 4
+        for (int i = 0; i <= dn; ++i) {
+          const uint8_t s = Mp.anc_at[i][p];
+          M.anc_at[i][p] = s;
+          acc += M.gg[s];
+        }
+        M.G[p] = acc;
+      } else if (ok && p < N) {
         const int dn = M.dep[p];
         uint64_t mk = my_anc;
         bool pk = __popcll(mk) == dn + 1 && ((mk >> M.pos[p]) & 1ull);
@@ -409,6 +433,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       }
       ok = named_sync_and(kBarP, kGroup, ok);
       if (p == 0) M.good = ok;
+      prev_bi = ok ? bi : -1;
       // first product into TMEM half `slot` (one thread)
       bool step_ok = true;
       if (p == 0) {
@@ -448,11 +473,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         step_ok = tma_ok && (!issued || mbar_wait_suspend(&sh.mma1_bar, mma1_count & 1, abort));
         if (issued) ++mma1_count;
       }
-      if (fused && p < 32 && next < n_items) publish_commit();
+      if (fused && p < 32 && next < i_end) publish_commit();
       if (!named_sync_and(kBarP, kGroup, step_ok && !*abort)) break;
-      if (p == 0 && next < n_items) issue_kq(next, pf.lo);
+      if (p == 0 && next < i_end) issue_kq(next, pf.lo);
       // the S0 operand area is free again: stage the next item's pending commit
-      if (fused && next < n_items) stage_commit(next);
+      if (fused && next < i_end) stage_commit(next);
     }
   } else {
     // =================================================== consumer warps 8-15
@@ -482,20 +507,20 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         for (int i = 0; i < 8; ++i) vreg[i] = __ldg(vp + i);
       }
     };
-    int item = blockIdx.x;
+    int item = i_begin;
     load_vseq(item);
     load_v(item);
-    if (item + stride < n_items) load_vseq(item + stride);
+    if (item + i_step < i_end) load_vseq(item + i_step);
     float* SSbase = reinterpret_cast<float*>(smem + kOffSS);
     uint32_t mma2_count = 0;  // second products issued so far (same in every thread)
-    for (int j = 0; item < n_items; ++j, item += stride) {
+    for (int j = 0; item < i_end; ++j, item += i_step) {
       const int slot = j & 1;
       if (!group_wait(&sh.s1_done[slot], (j >> 1) & 1, kBarC, c == 0, abort)) break;
       tc_fence_after_sync();
       const ItemMeta& M = sh.meta[slot];
       const int lo = M.lo, N = M.N, h = M.h;
       const uint32_t tb = tmem + slot * 256;
-      const int next = item + stride;
+      const int next = item + i_step;
 
       if (!M.good) {  // bad or empty sequence: zero rows
         for (int e = c; e < N * (kTcDV / 4); e += kGroup) {
@@ -505,9 +530,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
           *reinterpret_cast<float4*>(Uws + row) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         for (int n = c; n < N; n += kGroup) Gws[(size_t)(lo + n) * H_v + h] = 0.f;
-        if (next < n_items) {
+        if (next < i_end) {
           load_v(next);
-          if (next + stride < n_items) load_vseq(next + stride);
+          if (next + i_step < i_end) load_vseq(next + i_step);
         }
         named_sync(kBarC, kGroup);
         if (c == 0) mbar_arrive(&sh.tmem_free[slot]);
@@ -562,9 +587,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
           }
         }
       }
-      if (next < n_items) {  // V rows of the next item, ahead of time
+      if (next < i_end) {  // V rows of the next item, ahead of time
         load_v(next);
-        if (next + stride < n_items) load_vseq(next + stride);
+        if (next + i_step < i_end) load_vseq(next + i_step);
       }
 
       // ---- one row of T (sc < 64) or W (64 <= sc < 128), by back substitution on
@@ -697,7 +722,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
   cp_async_wait_all();  // staging copies left by a loop that ended early
   __syncthreads();
   if (sh.abort && tid == 0) {
-    for (int it2 = blockIdx.x; it2 < n_items; it2 += stride)
+    for (int it2 = i_begin; it2 < i_end; it2 += i_step)
       atomicCAS(&status[it2 / H_v], TGDN_SEQ_OK, TGDN_SEQ_TIMEOUT);
     if (sh.tma_issued > 0) (void)mbar_wait(&sh.tma_bar, (sh.tma_issued - 1) & 1);
   }
