@@ -184,6 +184,13 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
+// Non-binding prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
+               "r"(bytes)
+               : "memory");
+}
+
 // 16-byte asynchronous copy global -> shared (both addresses 16-byte aligned);
 // completes for this thread at cp_async_wait_all().
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {

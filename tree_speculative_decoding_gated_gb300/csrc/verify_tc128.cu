@@ -70,6 +70,14 @@ __device__ __forceinline__ int t8_atom_off(int row, int chunk) {
 __device__ __forceinline__ int f_idx(int row, int col) {
   return row * 128 + ((((col >> 2) ^ (row & 31))) << 2) + (col & 3);
 }
+// This thread's part of one item's state: rows r0 + 16 r, float4 column sq.
+__device__ __forceinline__ void load_state_rows(float4 (&sr)[8], const float* src, int r0,
+                                                int sq) {
+#pragma unroll
+  for (int r = 0; r < 8; ++r)
+    sr[r] = __ldg(reinterpret_cast<const float4*>(src + (size_t)(r0 + 16 * r) * kT8D) + sq);
+}
+
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
   const __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&p);
@@ -121,13 +129,45 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
   float* GK = reinterpret_cast<float*>(smem + kO8GK);
   float* GQ = reinterpret_cast<float*>(smem + kO8GQ);
 
+  // One item ahead: the sequence's bounds, status and root depth in registers,
+  // and the item's state, V rows and tree metadata pulled into L2 while the
+  // current item is being finished (16-byte aligned ranges inside the arrays).
+  const int sq = tid & 31, r0 = tid >> 5;
+  int nx_lo = 0, nx_hi = 0, nx_st = 0, nx_d0 = 0;
+  float4 sr[8];
+#define T8_PREFETCH(it)                                                          \
+  if ((it) < n_items) {                                                          \
+    const int b2 = (it) / H_v;                                                   \
+    nx_lo = cu[b2];                                                              \
+    nx_hi = cu[b2 + 1];                                                          \
+    nx_st = status[b2];                                                          \
+    nx_d0 = nx_hi > nx_lo ? depth[nx_lo] : 0;                                    \
+    if (tid == 0) prefetch_l2(S0 + (size_t)(it) * kT8D * kT8D, kT8D * kT8D * 4); \
+    if (tid < nx_hi - nx_lo && tid <= kT8Nodes)                                  \
+      prefetch_l2(v + ((size_t)(nx_lo + tid) * H_v + (it) % H_v) * kT8D, kT8D * 2); \
+    if (tid >= 32 && tid < 35) {                                                 \
+      const int32_t* arr = tid == 32 ? depth : tid == 33 ? pos : order;          \
+      const uintptr_t a0 = reinterpret_cast<uintptr_t>(arr + nx_lo) & ~(uintptr_t)15; \
+      const uintptr_t a1 = reinterpret_cast<uintptr_t>(arr + nx_hi) & ~(uintptr_t)15; \
+      if (a1 > a0) prefetch_l2(reinterpret_cast<const void*>(a0), (uint32_t)(a1 - a0)); \
+    }                                                                            \
+  }
+  T8_PREFETCH((int)blockIdx.x)
+
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
     const int bi = item / H_v, h = item % H_v, qh = h / grp;
-    const int lo = cu[bi], N = cu[bi + 1] - lo;
-    if (N <= 0) continue;  // uniform over the CTA
-    const bool st_ok = status[bi] == TGDN_SEQ_OK;
-    const int fold = (st_ok && N == kT8Nodes + 1 && depth[lo] == 0) ? 1 : 0;
-    if (st_ok && N == kT8Nodes + 1 && !fold) continue;  // root elsewhere: the SIMT kernel's
+    const int lo = nx_lo, N = nx_hi - nx_lo;
+    const bool st_ok = nx_st == TGDN_SEQ_OK;
+    const int d0 = nx_d0;
+    if (N <= 0) {  // uniform over the CTA
+      T8_PREFETCH(item + (int)gridDim.x)
+      continue;
+    }
+    const int fold = (st_ok && N == kT8Nodes + 1 && d0 == 0) ? 1 : 0;
+    if (st_ok && N == kT8Nodes + 1 && !fold) {  // root elsewhere: the SIMT kernel's
+      T8_PREFETCH(item + (int)gridDim.x)
+      continue;
+    }
     const int Nf = N - fold;                             // nodes on the tensor cores
     const size_t obase0 = (size_t)lo * H_v + h;          // row of node 0
     const size_t obase = obase0 + (size_t)fold * H_v;    // row of the first tensor-core node
@@ -149,13 +189,6 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
       M.tma_n += 1;
     }
     // ---- metadata, root paths and path-cumulative gates (one thread per node)
-    uint4 vreg[4];
-    if (ok && my_row < Nf) {  // this thread's V row slice (32 columns), early
-      const uint4* vp =
-          reinterpret_cast<const uint4*>(v + (obase + (size_t)my_row * H_v) * kT8D + cg * 32);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) vreg[i] = __ldg(vp + i);
-    }
     // (with a folded root, node nd = tid + 1 is tensor-core node tid; depths and
     // topological positions drop by one: the root is position 0)
     if (ok && tid < Nf) {
@@ -199,12 +232,7 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
     }
     // ---- S0 -> bf16 hi + lo operand (thread: rows (tid >> 5) + 16 r, float4 column tid & 31)
     {
-      const float* src = S0 + (size_t)item * kT8D * kT8D;
-      const int sq = tid & 31, r0 = tid >> 5;
-      float4 sr[8];
-#pragma unroll
-      for (int r = 0; r < 8; ++r)
-        sr[r] = __ldg(reinterpret_cast<const float4*>(src + (size_t)(r0 + 16 * r) * kT8D) + sq);
+      load_state_rows(sr, S0 + (size_t)item * kT8D * kT8D, r0, sq);
       if (fold) {  // the root's own step: S_r = a_r S0 + k_r u_r^T, o_r = S_r^T q_r
         float* part = reinterpret_cast<float*>(smem + kO8GK);  // [16][128] partial sums
         float* kr = part + 16 * kT8D;
@@ -273,6 +301,13 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
       }
     }
     fence_proxy_async_smem();
+    uint4 vreg[4];  // this thread's V row slice (32 columns), for R after the product
+    if (ok && my_row < Nf) {
+      const uint4* vp =
+          reinterpret_cast<const uint4*>(v + (obase + (size_t)my_row * H_v) * kT8D + cg * 32);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) vreg[i] = __ldg(vp + i);
+    }
     ok = __syncthreads_and(ok) != 0;
     if (!ok) {  // bad sequence: zero rows, and let an issued copy land before reuse
       if (tid == 0 && tma_issued) (void)mbar_wait_suspend(&M.tma_bar, (M.tma_n - 1) & 1, abort);
@@ -284,6 +319,7 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
       }
       for (int n = tid; n < N; n += kT8Threads) Gws[obase0 + (size_t)n * H_v] = 0.f;
       if (__syncthreads_or(*abort)) break;
+      T8_PREFETCH(item + (int)gridDim.x)
       continue;
     }
 
@@ -459,6 +495,7 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
     tc_fence_before_sync();
     __syncthreads();  // TMEM and shared memory are reused by the next item
     tc_fence_after_sync();
+    T8_PREFETCH(item + (int)gridDim.x)  // lands while the next item's metadata is read
   }
 
   // ---- end.  After an expired wait every item still owned by this CTA is
@@ -476,6 +513,8 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
     tmem_dealloc(tmem, 512);
   }
 }
+
+#undef T8_PREFETCH
 
 bool verify_tc128_supported(const tgdn_tree& t, const tgdn_dims& d, const void* q,
                             const void* k, const void* v, const float* S0, const void* o) {
