@@ -10,12 +10,14 @@
 // is (node, query head of the group), row = node * G + g.  256 threads, two per
 // row (= TMEM lane), each taking half of every key tile and half of the output
 // columns; the halves of a row's maximum and normaliser are merged once.  Keys come in tiles of 64: first the cached context
-// (prefix_len[b] positions), then the tree's own nodes.  Two passes over the
-// key tiles: the first finds each row's maximum logit and normaliser, the
-// second forms P = exp(logit - max) / sum as a bf16 operand and accumulates
-// O = P V on the tensor cores, so O never needs rescaling.  Key and value
-// tiles are double-buffered: the copy of the next tile is in flight while the
-// current one is scored.
+// (prefix_len[b] positions), then the tree's own nodes.  One pass over the key
+// tiles with an online softmax: P = exp(logit - m) is formed against a running
+// row maximum m as a bf16 operand and O += P V accumulates in TMEM; m is moved
+// (and O, the running sum rescaled in place) only when a tile's maximum exceeds
+// it by more than kRescaleGap, so P stays below e^kRescaleGap and rescaling is
+// rare.  O is divided by the sum at the end.  Key and value tiles are
+// double-buffered: the copy of the next tile is in flight while the current
+// one is scored.
 //   S tile = Q K^T: tcgen05.mma, A = Q (TMA, 128-byte swizzle), B = K tile
 //   O     += P V:   A = P (written by the threads), B = V tile (MN-major)
 // Every wait is bounded; on expiry the sequence is marked TGDN_SEQ_TIMEOUT.
@@ -26,6 +28,7 @@ namespace tgdn {
 
 constexpr int kAtThreads = 256;
 constexpr int kAtRows = 128;             // query rows per CTA
+constexpr float kRescaleGap = 8.f;       // lazy rescaling threshold (natural log units)
 constexpr int kAtKeys = 64;              // keys per tile
 constexpr int kAtD = 128;
 constexpr int kAtMaxNodes = 128;         // tree nodes per sequence on this kernel
@@ -137,13 +140,13 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   const uint64_t m_lo = row_live ? amask[2 * my_node] : 0;
   const uint64_t m_hi = row_live ? amask[2 * my_node + 1] : 0;
 
-  // Steps u = 0 .. 2 nt - 1: pass u / nt, key tile u % nt, buffer u & 1.
-  const int steps = 2 * nt;
+  // Steps u = 0 .. nt - 1: key and value tile u, buffer u & 1.
+  const int steps = nt;
   int tma_issued[2] = {0, 0};  // copies issued per buffer (thread 0)
-  // thread 0: the key (and, in the second pass, value) tile of step u into buffer u & 1
+  // thread 0: the key and value tiles of step u into buffer u & 1
   auto issue_tile = [&](int u) {
-    const int t = u < nt ? u : u - nt, buf = u & 1;
-    const bool with_v = u >= nt;
+    const int t = u, buf = u & 1;
+    const bool with_v = true;
     const bool pre = t < nt_pre;
     const int row = pre ? b * a.P_max + t * kAtKeys : lo + (t - nt_pre) * kAtKeys;
     const CUtensorMap* km = pre ? &kcmap : &ktmap;
@@ -218,55 +221,49 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
 
   bool ok = true;
   if (tid == 0) issue_tile(0);
-  // ---- pass 1: row maximum and normaliser
-  float m = -INFINITY, l = 0.f;
-  for (int t = 0; t < nt && ok; ++t) {
-    tile_sync();
-    load_and_score(t);
-    ok = wait_mma();
-    if (!ok) break;
-    tc_fence_after_sync();
-    float x[kHalf];
-    read_logits(t, x);
-    float mt_ = m;
-#pragma unroll
-    for (int c = 0; c < kHalf; ++c) mt_ = fmaxf(mt_, x[c]);
-    if (mt_ > -INFINITY) {
-      float sum = 0.f;
-#pragma unroll
-      for (int c = 0; c < kHalf; ++c) sum += __expf(x[c] - mt_);
-      l = l * __expf(m - mt_) + sum;
-      m = mt_;
-    }
-  }
-  {  // merge the two halves of each row
-    float* st = reinterpret_cast<float*>(smem + kAtOffStat);
-    st[kh * kAtRows + row] = m;
-    st[(2 + kh) * kAtRows + row] = l;
-    __syncthreads();
-    const float m0 = st[row], m1 = st[kAtRows + row];
-    const float l0 = st[2 * kAtRows + row], l1 = st[3 * kAtRows + row];
-    m = fmaxf(m0, m1);
-    l = m > -INFINITY ? l0 * __expf(m0 - m) + l1 * __expf(m1 - m) : 0.f;
-  }
-  const float inv_l = l > 0.f ? 1.f / l : 0.f;
-  // ---- pass 2: P = exp(logit - m) / l as a bf16 operand, O += P V
-  for (int t = 0; t < nt && ok; ++t) {
-    const int u = nt + t;
+  float* st = reinterpret_cast<float*>(smem + kAtOffStat);
+  float m = -INFINITY;  // running row maximum (same in both threads of a row)
+  float lsum = 0.f;     // this thread's half of the row's sum of exp(logit - m)
+  for (int u = 0; u < nt && ok; ++u) {
     tile_sync();
     load_and_score(u);
     ok = wait_mma();
     if (!ok) break;
     tc_fence_after_sync();
     float x[kHalf];
-    read_logits(t, x);
+    read_logits(u, x);
+    float lm = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < kHalf; ++c) lm = fmaxf(lm, x[c]);
+    st[kh * kAtRows + row] = lm;
+    __syncthreads();
+    const float mt = fmaxf(st[row], st[kAtRows + row]);
+    const bool need = mt > m + kRescaleGap;  // also the first finite maximum of the row
+    const float alpha = need ? (m == -INFINITY ? 0.f : __expf(m - mt)) : 1.f;
+    if (need) {
+      m = mt;
+      lsum *= alpha;
+    }
+    if (u > 0 && __any_sync(0xffffffffu, need)) {  // O *= alpha (warp-collective)
+#pragma unroll
+      for (int q = 2 * kh; q < 2 * kh + 2; ++q) {
+        float r[32];
+        tmem_ld32(tO + lane_base + q * 32, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) r[c] *= alpha;
+        tmem_st32(tO + lane_base + q * 32, r);
+      }
+      tmem_st_wait();
+    }
 #pragma unroll
     for (int c8 = 0; c8 < kHalf / 8; ++c8) {
       uint32_t w[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float p0 = l > 0.f ? __expf(x[c8 * 8 + 2 * i] - m) * inv_l : 0.f;
-        const float p1 = l > 0.f ? __expf(x[c8 * 8 + 2 * i + 1] - m) * inv_l : 0.f;
+        const float p0 = m == -INFINITY ? 0.f : __expf(x[c8 * 8 + 2 * i] - m);
+        const float p1 = m == -INFINITY ? 0.f : __expf(x[c8 * 8 + 2 * i + 1] - m);
+        lsum += p0 + p1;
         const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
         w[i] = *reinterpret_cast<const uint32_t*>(&pp);
       }
@@ -287,13 +284,18 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
 #pragma unroll
         for (int at = 0; at < 2; ++at) {
           const uint64_t bd = smem_desc(sV + at * 8192 + s * 2048, 1024, 1024, kSwizzle128B);
-          umma_bf16(tO + at * 64, ad, bd, id_o, (t > 0 || s > 0) ? 1u : 0u);
+          umma_bf16(tO + at * 64, ad, bd, id_o, (u > 0 || s > 0) ? 1u : 0u);
         }
       }
       umma_commit(mma_bar);
     }
     ok = wait_mma();
   }
+  // the row's sum from its two halves (both kept against the same maximum)
+  st[(2 + kh) * kAtRows + row] = lsum;
+  __syncthreads();
+  const float l = st[2 * kAtRows + row] + st[3 * kAtRows + row];
+  const float inv_l = l > 0.f ? 1.f / l : 0.f;
   // ---- epilogue: O rows to global (bf16)
   if (ok) {
     tc_fence_after_sync();
@@ -308,8 +310,8 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
           uint32_t w[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const __nv_bfloat162 pp =
-                __floats2bfloat162_rn(r[c8 * 8 + 2 * i], r[c8 * 8 + 2 * i + 1]);
+            const __nv_bfloat162 pp = __floats2bfloat162_rn(r[c8 * 8 + 2 * i] * inv_l,
+                                                            r[c8 * 8 + 2 * i + 1] * inv_l);
             w[i] = *reinterpret_cast<const uint32_t*>(&pp);
           }
           reinterpret_cast<uint4*>(orow)[q * 4 + c8] = make_uint4(w[0], w[1], w[2], w[3]);
