@@ -660,9 +660,12 @@ def run_attention_times(args):
         kc, vc = rnd(B, P, H_kv, 128), rnd(B, P, H_kv, 128)
         pl = torch.full((B,), P, dtype=torch.int32, device=dev)
         o = torch.empty_like(q)
+        nb = tgdn.tree_attention_workspace_bytes(tree, H_q, H_kv, 128, P)
+        ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=dev)
         with torch.cuda.stream(stream):
             tgdn.tree_prep(tree, stream)
-        fn = lambda: tgdn.tree_attention(tree, q, kt, vt, kc, vc, pl, o, 128 ** -0.5, stream)
+        fn = lambda: tgdn.tree_attention(tree, q, kt, vt, kc, vc, pl, o, 128 ** -0.5, ws=ws,
+                                         stream=stream)
         with torch.cuda.stream(stream):
             for _ in range(3):
                 fn()
@@ -674,6 +677,7 @@ def run_attention_times(args):
         node_bytes = T * (2 * H_q + 2 * H_kv) * 128 * 2
         gbs = (cache_bytes + node_bytes) / (t * 1e-6) / 1e9
         out.append({"B": B, "nodes": N, "H_q": H_q, "H_kv": H_kv, "context": P, "us": t,
+                    "context_split": nb > 0,
                     "GB/s": gbs, "frac_hbm": gbs / hbm, "TFLOP/s": flops / (t * 1e-6) / 1e12})
     return {"part": "attention", "metric": "tgdn_tree_attention kernel time per layer, bf16, "
             "d=128, L2 flushed before every launch", "unit": "us", "higher_is_better": False,

@@ -212,6 +212,10 @@ int tgdn_tree_build(int32_t B, int32_t budget, int32_t K, int32_t w, int32_t dep
  *   k_cache, v_cache [B][P_max][H_kv][d]  (cached context; may be NULL if P_max is 0)
  *   prefix_len [B] int32 (device; clamped to [0, P_max])
  *   o       [T][H_q][d] bf16, written
+ *   ws      optional workspace of tgdn_tree_attention_workspace_bytes() bytes
+ *           (NULL, or fewer bytes: no split): with it the cached context of each
+ *           (sequence, key/value head, 128 query rows) is split over several CTAs
+ *           and the parts merged, which keeps every SM busy on small batches
  * tgdn_tree_prep must have run on `tree`; sequences with a bad status get zero
  * outputs.  Tensor-core kernel: d = 128, H_q / H_kv in {1, 2, 4, 8, 16},
  * n_max <= 128; other shapes return TGDN_EUNSUPPORTED.  All pointers 16-byte
@@ -220,7 +224,14 @@ int tgdn_tree_build(int32_t B, int32_t budget, int32_t K, int32_t w, int32_t dep
 int tgdn_tree_attention(const tgdn_tree* tree, int32_t H_q, int32_t H_kv, int32_t d,
                         const void* q, const void* k_tree, const void* v_tree,
                         const void* k_cache, const void* v_cache, const int32_t* prefix_len,
-                        int32_t P_max, float scale, void* o, tgdn_stream_t stream);
+                        int32_t P_max, float scale, void* o, void* ws, size_t ws_bytes,
+                        tgdn_stream_t stream);
+
+/* Workspace bytes that let tgdn_tree_attention split the cached context for this
+ * tree and shape on the current device (0: no split would be used, or invalid
+ * arguments). */
+size_t tgdn_tree_attention_workspace_bytes(const tgdn_tree* tree, int32_t H_q, int32_t H_kv,
+                                           int32_t d, int32_t P_max);
 
 /* Greedy acceptance (Experimentelle Ergebnisse, mean acceptance length).  The
  * root is always accepted; a non-root node is accepted when it and every

@@ -3,7 +3,8 @@
 Each node attends to its sequence's cached context and its own root path.  Checked over
 grouped-query ratios 1-16, context lengths 0 .. P_max including ragged last tiles, trees
 of 1-128 nodes (one or two key tiles of tree nodes), empty and invalid sequences, and
-non-ancestor invariance (bitwise) on the GPU.  Bar: max relative Frobenius error per
+non-ancestor invariance (bitwise) on the GPU; with and without the workspace that splits
+the cached context over several CTAs.  Bar: max relative Frobenius error per
 (sequence, query head) block <= 2e-2 (bf16 io; P is a bf16 operand).
 """
 import numpy as np
@@ -36,7 +37,7 @@ def make_case(parents, H_q, H_kv, P_max, prefix, n_max=None, seed=0, d=128):
                 prefix=np.asarray(prefix, np.int32), scale=1.0 / np.sqrt(d))
 
 
-def run_gpu(c):
+def run_gpu(c, split=False):
     t = c["trees"]
     tree = tgdn.Tree.from_host(t.cu_nodes, t.parent, t.n_max, t.depth_max)
     tgdn.tree_prep(tree)
@@ -45,8 +46,13 @@ def run_gpu(c):
     P_max = c["kc"].shape[1]
     kc = dev(c["kc"]) if P_max > 0 else None
     vc = dev(c["vc"]) if P_max > 0 else None
+    ws = None
+    if split:
+        nb = tgdn.tree_attention_workspace_bytes(tree, c["q"].shape[1], c["kt"].shape[1],
+                                                 c["q"].shape[2], P_max)
+        ws = torch.full((max(nb, 16),), 255, dtype=torch.uint8, device="cuda")  # stale bytes
     tgdn.tree_attention(tree, dev(c["q"]), dev(c["kt"]), dev(c["vt"]), kc, vc,
-                        torch.from_numpy(c["prefix"]).cuda(), o, c["scale"])
+                        torch.from_numpy(c["prefix"]).cuda(), o, c["scale"], ws=ws)
     torch.cuda.synchronize()
     return o.float().cpu().numpy(), tree.status.cpu().numpy()
 
@@ -59,12 +65,24 @@ def run_oracle(c):
 
 
 def check(c):
-    got, status = run_gpu(c)
     ref = run_oracle(c)
-    err = rel_fro_blocks(got, ref, c["trees"].cu_nodes)
-    print(f"tree attention rel-Frobenius {err:.3e}")
-    assert err <= TOL_BF16
+    for split in (False, True):
+        got, status = run_gpu(c, split)
+        err = rel_fro_blocks(got, ref, c["trees"].cu_nodes)
+        print(f"tree attention (split={split}) rel-Frobenius {err:.3e}")
+        assert err <= TOL_BF16
     return got, ref, status
+
+
+def test_small_batches_split_the_context():
+    """Few (sequence, head) items: the workspace lets the context be split."""
+    rng = np.random.default_rng(9)
+    parents = [synth.random_recursive_tree(rng, 40, 8) for _ in range(2)]
+    c = make_case(parents, 8, 2, 2600, [2600, 1333], n_max=64, seed=9)
+    t = c["trees"]
+    tree = tgdn.Tree.from_host(t.cu_nodes, t.parent, t.n_max, t.depth_max)
+    assert tgdn.tree_attention_workspace_bytes(tree, 8, 2, 128, 2600) > 0
+    check(c)
 
 
 @pytest.mark.parametrize("H_q,H_kv", [(16, 4), (8, 8), (16, 8), (16, 2), (16, 1)])
@@ -125,3 +143,17 @@ def test_unsupported_shapes_are_refused():
     c = make_case([np.array([-1, 0], np.int32)], 4, 4, 8, [8], seed=7, d=64)
     with pytest.raises(tgdn.TgdnError):
         run_gpu(c)
+
+
+def test_many_context_splits_with_an_empty_context():
+    """Four splits of a 4096-position context next to a sequence with no context (its
+    context splits are empty and only the last one, with the tree's keys, counts)."""
+    rng = np.random.default_rng(10)
+    parents = [synth.random_recursive_tree(rng, 40, 8), synth.random_recursive_tree(rng, 30, 6),
+               np.array([-1, 0, -1], np.int32)]
+    c = make_case(parents, 8, 8, 4096, [4096, 0, 4096], n_max=64, seed=10)
+    t = c["trees"]
+    tree = tgdn.Tree.from_host(t.cu_nodes, t.parent, t.n_max, t.depth_max)
+    assert tgdn.tree_attention_workspace_bytes(tree, 8, 8, 128, 4096) > 0
+    got, ref, status = check(c)
+    assert status.tolist() == [0, 0, 3]

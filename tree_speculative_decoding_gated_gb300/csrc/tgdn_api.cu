@@ -228,10 +228,19 @@ int tgdn_tree_build(int32_t B, int32_t budget, int32_t K, int32_t w, int32_t dep
                                            rounds, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t tgdn_tree_attention_workspace_bytes(const tgdn_tree* tree, int32_t H_q, int32_t H_kv,
+                                           int32_t d, int32_t P_max) {
+  if (check_tree(tree) != TGDN_OK || H_q < 1 || H_kv < 1 || H_q % H_kv != 0 || P_max < 0)
+    return 0;
+  if (!tgdn::tree_attn_supported(*tree, H_q, H_kv, d)) return 0;
+  return tgdn::tree_attn_workspace_bytes(*tree, H_q, H_kv, P_max);
+}
+
 int tgdn_tree_attention(const tgdn_tree* tree, int32_t H_q, int32_t H_kv, int32_t d,
                         const void* q, const void* k_tree, const void* v_tree,
                         const void* k_cache, const void* v_cache, const int32_t* prefix_len,
-                        int32_t P_max, float scale, void* o, tgdn_stream_t stream) {
+                        int32_t P_max, float scale, void* o, void* ws, size_t ws_bytes,
+                        tgdn_stream_t stream) {
   int rc = check_tree(tree);
   if (rc != TGDN_OK) return rc;
   const tgdn_tree& t = *tree;
@@ -241,7 +250,7 @@ int tgdn_tree_attention(const tgdn_tree* tree, int32_t H_q, int32_t H_kv, int32_
   if (t.T > 0 && (!q || !k_tree || !v_tree || !o)) return TGDN_EINVAL;
   auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) % 16) == 0; };
   if (!al16(q) || !al16(k_tree) || !al16(v_tree) || !al16(k_cache) || !al16(v_cache) ||
-      !al16(o))
+      !al16(o) || !al16(ws))
     return TGDN_EINVAL;
   if (t.B == 0 || t.T == 0) return TGDN_OK;
   const int G = H_q / H_kv;
@@ -257,7 +266,8 @@ int tgdn_tree_attention(const tgdn_tree* tree, int32_t H_q, int32_t H_kv, int32_
       !encode_rows_map(&vcm, vc, crows, H_kv, 1, 64))
     return TGDN_ECUDA;
   return from_cuda(tgdn::launch_tree_attn(t, H_q, H_kv, P_max, scale, qm, ktm, vtm, kcm, vcm,
-                                          prefix_len, o, reinterpret_cast<cudaStream_t>(stream)));
+                                          prefix_len, o, ws, ws ? ws_bytes : 0,
+                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int tgdn_accept(const tgdn_tree* tree, const int32_t* draft_ids, const int32_t* target_ids,

@@ -89,12 +89,15 @@ cudaError_t launch_tree_build(int B, int budget, int K, int w, int depth_max,
 // head, 128 query rows).  Tensor maps: q [T][H_q][128] with box {64, G, 128 / G};
 // k_tree, v_tree [T][H_kv][128] and k_cache, v_cache [B * P_max][H_kv][128] with
 // box {64, 1, 64}; all 128-byte swizzled.
+// With a workspace of tree_attn_workspace_bytes() (0: no split for this shape) the
+// cached context is split over several CTAs and merged by a second kernel.
 bool tree_attn_supported(const tgdn_tree& t, int H_q, int H_kv, int d);
+size_t tree_attn_workspace_bytes(const tgdn_tree& t, int H_q, int H_kv, int P_max);
 cudaError_t launch_tree_attn(const tgdn_tree& t, int H_q, int H_kv, int P_max, float scale,
                              const CUtensorMap& qmap, const CUtensorMap& ktmap,
                              const CUtensorMap& vtmap, const CUtensorMap& kcmap,
                              const CUtensorMap& vcmap, const int32_t* prefix_len, void* o,
-                             cudaStream_t s);
+                             void* ws, size_t ws_bytes, cudaStream_t s);
 
 cudaError_t launch_commit(const tgdn_tree& t, const tgdn_dims& d, const int32_t* accept_node,
                           const void* k, const float* U, const float* G, const float* S_in,

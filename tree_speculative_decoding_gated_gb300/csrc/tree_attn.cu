@@ -18,6 +18,12 @@
 // rare.  O is divided by the sum at the end.  Key and value tiles are
 // double-buffered: the copy of the next tile is in flight while the current
 // one is scored.
+//
+// With a workspace the cached context of each (sequence, head, row tile) is
+// split over several CTAs (the tree's own keys go to the last one); each writes
+// its unnormalised O, row maximum and sum, and tree_attn_combine_kernel merges
+// them (O = sum_s e^{m_s - M} O_s / sum_s e^{m_s - M} l_s).  That keeps every SM
+// busy when there are fewer (sequence, head, row tile) items than SMs.
 //   S tile = Q K^T: tcgen05.mma, A = Q (TMA, 128-byte swizzle), B = K tile
 //   O     += P V:   A = P (written by the threads), B = V tile (MN-major)
 // Every wait is bounded; on expiry the sequence is marked TGDN_SEQ_TIMEOUT.
@@ -31,6 +37,7 @@ constexpr int kAtRows = 128;             // query rows per CTA
 constexpr float kRescaleGap = 8.f;       // lazy rescaling threshold (natural log units)
 constexpr int kAtKeys = 64;              // keys per tile
 constexpr int kAtD = 128;
+constexpr int kPartStride = kAtD + 4;    // workspace row: O (128), m, l, 2 pad (528 B, 16-B aligned)
 constexpr int kAtMaxNodes = 128;         // tree nodes per sequence on this kernel
 constexpr uint32_t kAtTmemCols = 256;    // S tile: cols 0-63; O: cols 64-191
 constexpr int kAtOffQ = 0;               // [2 d halves][128 rows][128 B]     32 KiB
@@ -48,7 +55,8 @@ __device__ __forceinline__ int at_swz(int row, int chunk) {
 }
 
 struct AtArgs {
-  int H_q, H_kv, G, n_max, P_max, mtiles, n_items;
+  int H_q, H_kv, G, n_max, P_max, mtiles, n_items, splits;
+  float* part;  // with splits > 1: [splits][n_items][128 rows][kPartStride] = O, m, l, pad
   float scale;
   const int32_t* cu;
   const int32_t* order;
@@ -75,7 +83,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_bar + 1);
   int* s_abort = reinterpret_cast<int*>(tmem_slot + 1);
 
-  const int item = blockIdx.x;
+  const int item = blockIdx.x / a.splits, sp = blockIdx.x % a.splits;
   if (item >= a.n_items) return;
   const int mt = item % a.mtiles;
   const int hk = (item / a.mtiles) % a.H_kv;
@@ -135,7 +143,12 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
 
   const int nt_pre = (P + kAtKeys - 1) / kAtKeys;
   const int nt_tree = (N + kAtKeys - 1) / kAtKeys;
-  const int nt = nt_pre + nt_tree;
+  // this CTA's key tiles: context tiles [t_begin, t_end), then (last split) the tree's
+  const int t_begin = (int)(((long)sp * nt_pre) / a.splits);
+  const int t_end = (int)(((long)(sp + 1) * nt_pre) / a.splits);
+  const int n_ctx = t_end - t_begin;
+  const int nt = n_ctx + (sp == a.splits - 1 ? nt_tree : 0);  // steps of this CTA
+  auto tile_of = [&](int u) { return u < n_ctx ? t_begin + u : nt_pre + (u - n_ctx); };
   uint32_t mma_phase = 0;
   const uint64_t m_lo = row_live ? amask[2 * my_node] : 0;
   const uint64_t m_hi = row_live ? amask[2 * my_node + 1] : 0;
@@ -145,7 +158,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   int tma_issued[2] = {0, 0};  // copies issued per buffer (thread 0)
   // thread 0: the key and value tiles of step u into buffer u & 1
   auto issue_tile = [&](int u) {
-    const int t = u, buf = u & 1;
+    const int t = tile_of(u), buf = u & 1;
     const bool with_v = true;
     const bool pre = t < nt_pre;
     const int row = pre ? b * a.P_max + t * kAtKeys : lo + (t - nt_pre) * kAtKeys;
@@ -220,7 +233,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   };
 
   bool ok = true;
-  if (tid == 0) issue_tile(0);
+  if (tid == 0 && nt > 0) issue_tile(0);
   float* st = reinterpret_cast<float*>(smem + kAtOffStat);
   float m = -INFINITY;  // running row maximum (same in both threads of a row)
   float lsum = 0.f;     // this thread's half of the row's sum of exp(logit - m)
@@ -231,7 +244,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
     if (!ok) break;
     tc_fence_after_sync();
     float x[kHalf];
-    read_logits(u, x);
+    read_logits(tile_of(u), x);
     float lm = -INFINITY;
 #pragma unroll
     for (int c = 0; c < kHalf; ++c) lm = fmaxf(lm, x[c]);
@@ -296,8 +309,29 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   __syncthreads();
   const float l = st[2 * kAtRows + row] + st[3 * kAtRows + row];
   const float inv_l = l > 0.f ? 1.f / l : 0.f;
-  // ---- epilogue: O rows to global (bf16)
-  if (ok) {
+  // ---- epilogue: O rows to global (bf16), or this split's part to the workspace
+  if (ok && a.splits > 1) {
+    tc_fence_after_sync();
+    float* prow = a.part + (((size_t)sp * a.n_items + item) * kAtRows + row) * kPartStride;
+#pragma unroll
+    for (int q = 2 * kh; q < 2 * kh + 2; ++q) {
+      float r[32];
+      tmem_ld32(tO + lane_base + q * 32, r);
+      tmem_ld_wait();
+      if (nt == 0) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) r[c] = 0.f;
+      }
+#pragma unroll
+      for (int c4 = 0; c4 < 8; ++c4)
+        *reinterpret_cast<float4*>(prow + q * 32 + c4 * 4) =
+            make_float4(r[c4 * 4], r[c4 * 4 + 1], r[c4 * 4 + 2], r[c4 * 4 + 3]);
+    }
+    if (kh == 0) {
+      prow[kAtD] = m;
+      prow[kAtD + 1] = l;
+    }
+  } else if (ok) {
     tc_fence_after_sync();
 #pragma unroll
     for (int q = 2 * kh; q < 2 * kh + 2; ++q) {  // this thread's 64 output columns
@@ -333,6 +367,94 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   }
 }
 
+// Merges the context splits of one (sequence, key/value head, row tile) item:
+// 256 threads, two per row (64 output columns each).
+__global__ void __launch_bounds__(kAtThreads)
+tree_attn_combine_kernel(const AtArgs a) {
+  const int item = blockIdx.x;
+  const int mt = item % a.mtiles;
+  const int hk = (item / a.mtiles) % a.H_kv;
+  const int b = item / (a.mtiles * a.H_kv);
+  const int tid = threadIdx.x;
+  const int lo = a.cu[b], N = a.cu[b + 1] - lo;
+  const int node0 = mt * (kAtRows / a.G);
+  if (N <= 0 || node0 >= N || a.status[b] != TGDN_SEQ_OK) return;  // zeros already written
+  const int row = tid & (kAtRows - 1), kh = tid >> 7;
+  const int my_node = node0 + row / a.G, my_g = row % a.G;
+  if (my_node >= N) return;
+  const size_t stride = (size_t)a.n_items * kAtRows * kPartStride;
+  const float* p0 = a.part + ((size_t)item * kAtRows + row) * kPartStride;
+  float M = -INFINITY;
+  for (int s = 0; s < a.splits; ++s) M = fmaxf(M, p0[s * stride + kAtD]);
+  float L = 0.f, acc[64];
+#pragma unroll
+  for (int c = 0; c < 64; ++c) acc[c] = 0.f;
+  for (int s = 0; s < a.splits; ++s) {
+    const float* ps = p0 + s * stride;
+    const float ms = ps[kAtD];
+    if (ms == -INFINITY) continue;  // no visible key in this split
+    const float w = __expf(ms - M);
+    L = fmaf(w, ps[kAtD + 1], L);
+#pragma unroll
+    for (int c4 = 0; c4 < 16; ++c4) {
+      const float4 x = reinterpret_cast<const float4*>(ps + kh * 64)[c4];
+      acc[c4 * 4] = fmaf(w, x.x, acc[c4 * 4]);
+      acc[c4 * 4 + 1] = fmaf(w, x.y, acc[c4 * 4 + 1]);
+      acc[c4 * 4 + 2] = fmaf(w, x.z, acc[c4 * 4 + 2]);
+      acc[c4 * 4 + 3] = fmaf(w, x.w, acc[c4 * 4 + 3]);
+    }
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  uint4* orow = reinterpret_cast<uint4*>(
+      a.o + ((size_t)(lo + my_node) * a.H_q + hk * a.G + my_g) * kAtD + kh * 64);
+#pragma unroll
+  for (int c8 = 0; c8 < 8; ++c8) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 pp =
+          __floats2bfloat162_rn(acc[c8 * 8 + 2 * i] * inv, acc[c8 * 8 + 2 * i + 1] * inv);
+      w[i] = *reinterpret_cast<const uint32_t*>(&pp);
+    }
+    orow[c8] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+static int at_sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0, c = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && c > 0)
+      n = c;
+    else
+      return 1;
+  }
+  return n;
+}
+
+// Context splits for this launch: enough CTAs for two per SM, at most 8, and at
+// least 16 key tiles (1024 cached positions) per split, below which the merge costs
+// more than the split saves.
+static int attn_splits(const tgdn_tree& t, int H_q, int H_kv, int P_max) {
+  const int G = H_q / H_kv;
+  const long items = (long)t.B * H_kv * ((t.n_max * G + kAtRows - 1) / kAtRows);
+  if (items <= 0) return 1;
+  long s = (2L * at_sm_count()) / items;
+  const long ctx_tiles = (P_max + kAtKeys - 1) / kAtKeys;
+  if (s > 8) s = 8;
+  if (s > ctx_tiles / 16) s = ctx_tiles / 16;
+  return s < 1 ? 1 : (int)s;
+}
+
+size_t tree_attn_workspace_bytes(const tgdn_tree& t, int H_q, int H_kv, int P_max) {
+  const int splits = attn_splits(t, H_q, H_kv, P_max);
+  if (splits <= 1) return 0;
+  const int G = H_q / H_kv;
+  const size_t items = (size_t)t.B * H_kv * ((t.n_max * G + kAtRows - 1) / kAtRows);
+  return (size_t)splits * items * kAtRows * kPartStride * sizeof(float);
+}
+
 bool tree_attn_supported(const tgdn_tree& t, int H_q, int H_kv, int d) {
   const int G = H_kv > 0 ? H_q / H_kv : 0;
   return d == kAtD && H_kv > 0 && H_q % H_kv == 0 && (G == 1 || G == 2 || G == 4 || G == 8 ||
@@ -344,7 +466,7 @@ cudaError_t launch_tree_attn(const tgdn_tree& t, int H_q, int H_kv, int P_max, f
                              const CUtensorMap& qmap, const CUtensorMap& ktmap,
                              const CUtensorMap& vtmap, const CUtensorMap& kcmap,
                              const CUtensorMap& vcmap, const int32_t* prefix_len, void* o,
-                             cudaStream_t s) {
+                             void* ws, size_t ws_bytes, cudaStream_t s) {
   AtArgs a;
   a.H_q = H_q;
   a.H_kv = H_kv;
@@ -365,11 +487,19 @@ cudaError_t launch_tree_attn(const tgdn_tree& t, int H_q, int H_kv, int P_max, f
   a.status = t.status;
   a.prefix_len = prefix_len;
   a.o = static_cast<__nv_bfloat16*>(o);
+  const size_t need = tree_attn_workspace_bytes(t, H_q, H_kv, P_max);
+  a.splits = (need > 0 && ws != nullptr && ws_bytes >= need) ? attn_splits(t, H_q, H_kv, P_max)
+                                                              : 1;
+  a.part = a.splits > 1 ? static_cast<float*>(ws) : nullptr;
+  if ((long)a.n_items * a.splits > 0x7fffffffL) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(tree_attn_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kAtSmemBytes);
   if (e != cudaSuccess) return e;
-  tree_attn_kernel<<<(unsigned)items, kAtThreads, kAtSmemBytes, s>>>(qmap, ktmap, vtmap, kcmap,
-                                                                     vcmap, a);
+  tree_attn_kernel<<<(unsigned)(items * a.splits), kAtThreads, kAtSmemBytes, s>>>(
+      qmap, ktmap, vtmap, kcmap, vcmap, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || a.splits == 1) return e;
+  tree_attn_combine_kernel<<<(unsigned)items, kAtThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

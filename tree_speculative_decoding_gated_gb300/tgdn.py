@@ -79,8 +79,10 @@ def lib() -> ctypes.CDLL:
                                       vp, st]
         L.tgdn_tree_build.restype = ctypes.c_int
         L.tgdn_tree_attention.argtypes = [P(CTree), i32, i32, i32, vp, vp, vp, vp, vp, vp, i32,
-                                          ctypes.c_float, vp, st]
+                                          ctypes.c_float, vp, vp, ctypes.c_size_t, st]
         L.tgdn_tree_attention.restype = ctypes.c_int
+        L.tgdn_tree_attention_workspace_bytes.argtypes = [P(CTree), i32, i32, i32, i32]
+        L.tgdn_tree_attention_workspace_bytes.restype = ctypes.c_size_t
         L.tgdn_status_string.argtypes = [i32]
         L.tgdn_status_string.restype = ctypes.c_char_p
         L.tgdn_version.argtypes = []
@@ -277,11 +279,17 @@ def tree_build(root_token, child_logp, child_token, budget: int, w: int, depth_m
     return out
 
 
+def tree_attention_workspace_bytes(tree: Tree, H_q: int, H_kv: int, d: int, P_max: int) -> int:
+    return int(lib().tgdn_tree_attention_workspace_bytes(ctypes.byref(tree.c()), H_q, H_kv, d,
+                                                         P_max))
+
+
 def tree_attention(tree: Tree, q, k_tree, v_tree, k_cache, v_cache, prefix_len, o,
-                   scale: float, stream=None) -> None:
+                   scale: float, ws=None, stream=None) -> None:
     """tgdn_tree_attention: each node attends to its sequence's cached context and its
     own root path.  q/o [T][H_q][d], k_tree/v_tree [T][H_kv][d], k_cache/v_cache
-    [B][P_max][H_kv][d] (bf16), prefix_len [B] int32."""
+    [B][P_max][H_kv][d] (bf16), prefix_len [B] int32.  ws: optional uint8 workspace of
+    tree_attention_workspace_bytes() bytes (splits the cached context over more CTAs)."""
     T, B = tree.T, tree.B
     H_q, d = q.shape[1], q.shape[2]
     H_kv = k_tree.shape[1]
@@ -293,8 +301,12 @@ def tree_attention(tree: Tree, q, k_tree, v_tree, k_cache, v_cache, prefix_len, 
             _dev(k_cache, bf, ncache, "k_cache") if P_max > 0 else None,
             _dev(v_cache, bf, ncache, "v_cache") if P_max > 0 else None,
             _dev(prefix_len, torch.int32, B, "prefix_len"))
+    wsp, wsn = None, 0
+    if ws is not None:
+        wsn = ws.numel() * ws.element_size()
+        wsp = _dev(ws, ws.dtype, ws.numel(), "ws") if wsn > 0 else None
     _check(lib().tgdn_tree_attention(ctypes.byref(tree.c()), H_q, H_kv, d, *args, P_max,
-                                     float(scale), _dev(o, bf, T * H_q * d, "o"),
+                                     float(scale), _dev(o, bf, T * H_q * d, "o"), wsp, wsn,
                                      _stream(stream)), "tgdn_tree_attention")
 
 
