@@ -122,12 +122,13 @@ int tgdn_verify(const tgdn_tree* tree, const tgdn_dims* dims, const void* q, con
   float* G = reinterpret_cast<float*>(static_cast<char*>(ws) + L.g_off);
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (tgdn::verify_tc_supported(t, d, q, k, v, S0, o)) {
-    CUtensorMap qmap, kmap;
-    if (!encode_qk_map(&qmap, q, t.T, d.H_qk) || !encode_qk_map(&kmap, k, t.T, d.H_qk))
-      return TGDN_ECUDA;  // the driver could not describe q/k for TMA
+    CUtensorMap qmap, kmap, vmap;
+    if (!encode_qk_map(&qmap, q, t.T, d.H_qk) || !encode_qk_map(&kmap, k, t.T, d.H_qk) ||
+        !encode_rows_map(&vmap, v, t.T, d.H_v, 1, 64))
+      return TGDN_ECUDA;  // the driver could not describe q/k/v for TMA
     const tgdn::PendingCommit none{};
-    return from_cuda(tgdn::launch_verify_tc(t, d, qmap, kmap, v, g, b, const_cast<float*>(S0), o,
-                                            U, G, none, s));
+    return from_cuda(tgdn::launch_verify_tc(t, d, qmap, kmap, vmap, g, b, const_cast<float*>(S0),
+                                            o, U, G, none, s));
   }
   if (tgdn::verify_tc128_supported(t, d, q, k, v, S0, o)) {
     CUtensorMap qmap, kmap;
@@ -180,14 +181,15 @@ int tgdn_verify_fused(const tgdn_tree* tree, const tgdn_dims* dims, const void* 
                              : nullptr;
   if (t.T > 0 && pt.T > 0 && tgdn::verify_tc_supported(t, d, q, k, v, S, o) &&
       tgdn::pending_commit_tc_supported(pt, prev_k)) {
-    CUtensorMap qmap, kmap;
-    if (!encode_qk_map(&qmap, q, t.T, d.H_qk) || !encode_qk_map(&kmap, k, t.T, d.H_qk))
+    CUtensorMap qmap, kmap, vmap;
+    if (!encode_qk_map(&qmap, q, t.T, d.H_qk) || !encode_qk_map(&kmap, k, t.T, d.H_qk) ||
+        !encode_rows_map(&vmap, v, t.T, d.H_v, 1, 64))
       return TGDN_ECUDA;
     float* U = reinterpret_cast<float*>(static_cast<char*>(ws) + L.u_off);
     float* G = reinterpret_cast<float*>(static_cast<char*>(ws) + L.g_off);
     const tgdn::PendingCommit cm{pt.cu_nodes, pt.status, prev_path, pt.depth_max + 1,
                                  prev_k,      pU,        pG};
-    return from_cuda(tgdn::launch_verify_tc(t, d, qmap, kmap, v, g, b, S, o, U, G, cm, s));
+    return from_cuda(tgdn::launch_verify_tc(t, d, qmap, kmap, vmap, g, b, S, o, U, G, cm, s));
   }
   // any other case: the commit as its own pass, then the verify
   if (pt.T > 0) {

@@ -191,6 +191,26 @@ __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
                : "memory");
 }
 
+// Untiled bulk copy shared -> global of `bytes` (a multiple of 16; both
+// addresses 16-byte aligned), tracked in this thread's bulk async-group.
+__device__ __forceinline__ void bulk_copy_s2g(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                   reinterpret_cast<uint64_t>(dst)),
+               "r"(smem_addr(src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Until this thread's bulk copies have read their shared-memory source.
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Until this thread's bulk copies are complete.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // 16-byte asynchronous copy global -> shared (both addresses 16-byte aligned);
 // completes for this thread at cp_async_wait_all().
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {

@@ -68,7 +68,7 @@ bool pending_commit_tc_supported(const tgdn_tree& prev, const void* prev_k);
 // With cm.path set, S is first updated in place by the pending commit and the
 // committed state is verified; otherwise S is only read.
 cudaError_t launch_verify_tc(const tgdn_tree& t, const tgdn_dims& d, const CUtensorMap& qmap,
-                             const CUtensorMap& kmap, const void* v, const float* g,
+                             const CUtensorMap& kmap, const CUtensorMap& vmap, const float* g,
                              const float* b, float* S, void* o, float* U, float* G,
                              const PendingCommit& cm, cudaStream_t s);
 

@@ -19,15 +19,18 @@
 //   producer warps 0-7, item j+1:
 //     tree metadata (prefetched) -> root paths (reused for the next head of the
 //     same sequence) and path-cumulative gates;
-//     S0 (prefetched into registers) -> bf16 hi + lo operands (~16-bit products);
+//     S0 (prefetched into registers; warp w holds rows 16 w .. 16 w + 15) ->
+//     bf16 hi + lo operands (~16-bit products);
 //     TMA of the item's key and query rows -> A = [K; Q] (128-byte swizzle);
 //     tcgen05.mma into TMEM half (j+1)&1:
 //        D[:, 0:128] = A (S0_hi + S0_lo),  D[:, 128:192] = A K^T;
-//     prefetch of the next item's metadata and S0.
+//     the product's completion is awaited one item later, just before its
+//     operands are overwritten; prefetch of the next item's metadata and S0.
 //   consumer warps 8-15, item j:
 //     Gram rows -> shared memory; R = diag(b)(V - e^G K S0) -> bf16 hi/lo operand;
-//     one thread per row of T (key lanes) or W (query lanes): back substitution
-//     along the node's root path, written straight into the [T; W] operand;
+//     one thread per row of T (key lanes) or W (query lanes): substitution
+//     along the node's root path with the partial sums in registers, written
+//     straight into the [T; W] operand;
 //     tcgen05.mma: D[:, 128:256] = [T; W] R;
 //     key lanes store U (workspace), query lanes O = e^G Q S0 + W R (bf16).
 // The halves hand over through mbarriers: "stage 1 done" (the first product's
@@ -36,9 +39,9 @@
 // Deferred commit folded into the next verify (Methodik 3, last bullet: the
 // state is committed once the accepted branch is known, in the following
 // decode iteration).  When the previous step left a commit pending, the
-// producer stages that step's accepted path for the item (u_s rows and k_s
-// rows by bulk copy, coefficients e^{G*-G_s}) while the item's state is being
-// prefetched, then forms
+// producer stages that step's accepted path for the item (u_s rows, k_s rows
+// and G_s by 16-byte asynchronous copies, one item ahead, into an area of
+// their own) and forms
 //   S = e^{G*} S_prev + sum_{s on the path} e^{G*-G_s} k_s u_s^T
 // in registers, writes it back in place (the committed state) and verifies
 // from it.  The state then crosses HBM once in each direction per step.
@@ -54,7 +57,8 @@ constexpr int kTcNodes = 64;   // nodes per tree on this kernel
 constexpr int kTcDK = 128;
 constexpr int kTcDV = 128;
 constexpr int kTcDepth = 30;   // depth bound on this kernel
-constexpr int kTcPath = kTcDepth + 1;  // entries of a root path (odd: conflict-free stride)
+constexpr int kTcPath = kTcDepth + 1;  // entries of a root path
+constexpr int kPathBytes = 32;         // one root path: a byte per depth, zero past the node
 constexpr uint32_t kTmemCols = 512;    // two halves of 256 columns
 constexpr int kGramCol = 128;          // within a half: Gram rows, then [T; W] R
 
@@ -67,14 +71,22 @@ constexpr int kOffRhi = 131072;   // R operand, MN-major [2 col atoms][8 node gr
 constexpr int kOffRlo = 147456;
 constexpr int kOffA2hi = 163840;  // [T; W] operand, K-major [16 row groups][8][128 B]     16 KiB
 constexpr int kOffA2lo = 180224;
-constexpr int kOffSS = 196608;    // path-solve scratch [128 rows][kTcPath] fp32
-// Pending-commit staging, inside the S0 operand area (free between items):
-constexpr int kOffUP = kOffS0hi;          // u_s rows [kTcPath][128] fp32        15.5 KiB
-constexpr int kOffKP = kOffS0hi + 16384;  // k_s rows [kTcPath][128] bf16        7.75 KiB
-constexpr int kOffGP = kOffS0hi + 24576;  // 16-byte chunks holding G_s [kTcPath][4] fp32
-constexpr int kOffMeta = kOffSS + 128 * kTcPath * 4;
+// Pending-commit staging, an area of its own so that the next item's rows are in
+// flight while this item's operands are still being read:
+constexpr int kOffUP = 196608;                        // u_s rows [kTcPath][128] fp32   15.5 KiB
+constexpr int kOffKP = kOffUP + kTcPath * kTcDV * 4;  // k_s rows [kTcPath][128] bf16   7.75 KiB
+constexpr int kOffGP = kOffKP + kTcPath * kTcDK * 2;  // 16-byte chunks holding G_s [kTcPath]
+constexpr int kOffMeta = (kOffGP + kTcPath * 16 + 127) & ~127;
+// Output staging after the second product (its operand areas are free then):
+constexpr int kOffUst = kOffGR;     // U rows [64][528 B] fp32 (GR and the start of R hi)
+constexpr int kUstRow = 528;        // 512 B + 16: rows 8 apart share banks, no more
+constexpr int kOffOst = kOffA2hi;   // O rows [64][272 B] bf16 (the [T; W] operand area)
+constexpr int kOstRow = 272;
+static_assert(kOffUst + 64 * kUstRow <= kOffRlo, "U staging stays clear of the V rows");
+static_assert(kOffOst + 64 * kOstRow <= kOffUP, "O staging stays in the [T; W] area");
 
-struct ItemMeta {
+struct alignas(16) ItemMeta {
+  uint8_t path[kTcNodes][kPathBytes];  // [node][depth]: the node's ancestor at that depth
   int lo, N, bi, h, good;
   int dep[kTcNodes];
   int ord[kTcNodes];
@@ -82,18 +94,18 @@ struct ItemMeta {
   float gg[kTcNodes];
   float G[kTcNodes];
   float bb[kTcNodes];
-  uint8_t anc_at[kTcPath + 1][kTcNodes];  // [depth index][node]: node's ancestor at that depth
 };
 struct TcShared {
-  uint64_t tma_bar, mma1_bar, mma2_bar;
+  uint64_t tma_bar, mma1_bar, mma2_bar, v_bar;
   uint64_t s1_done[2];    // consumer waits: first product done + metadata written
   uint64_t tmem_free[2];  // producer waits: consumer finished the item in this half
   uint32_t tmem_slot;
   int abort;
   int tma_issued;
-  int c_L;                // staged path length (0: nothing to commit)
-  int c_row[kTcPath];     // previous-step node rows of the staged path
-  int c_gi[kTcPath];      // index of G_s within its staged 16-byte chunk
+  int v_issued;
+  int c_L[2];             // staged path length per item parity (0: nothing to commit)
+  int c_row[2][kTcPath];  // previous-step node rows of the staged path
+  int c_gi[2][kTcPath];   // index of G_s within its staged 16-byte chunk
   ItemMeta meta[2];
 };
 constexpr int kTcSmemBytes = kOffMeta + (int)sizeof(TcShared) + 1024;  // + alignment slack
@@ -139,12 +151,103 @@ struct Prefetch {
   float gg, bb;
 };
 
+// v[k] for a run-time k in [0, N), N a power of two: a binary multiplexer over
+// the bits of k (fixed register indices, log2 N dependent selects).
+template <int N>
+__device__ __forceinline__ float pick(const float (&v)[N], int k) {
+  float t[N];
+#pragma unroll
+  for (int m = 0; m < N; ++m) t[m] = v[m];
+#pragma unroll
+  for (int w = N / 2, bit = 0; w >= 1; w /= 2, ++bit) {
+    const bool hi = (k >> bit) & 1;
+#pragma unroll
+    for (int m = 0; m < w; ++m) t[m] = hi ? t[2 * m + 1] : t[2 * m];
+  }
+  return t[0];
+}
+
+// acc[j] += s * row[p_j ^ x] for j < W and j < lim (p_j: byte j of the path).
+template <int W, int N>
+__device__ __forceinline__ void path_update(float (&acc)[N], const uint32_t (&pw)[8], float s,
+                                            const float* row, int x, int lim) {
+#pragma unroll
+  for (int j = 0; j < W; ++j)
+    if (j < lim)
+      acc[j] = fmaf(s, row[static_cast<int>((pw[j >> 2] >> (8 * (j & 3))) & 0xffu) ^ x], acc[j]);
+}
+
+// One row of T (t_row) or W of the node sn at depth dn, by substitution along
+// its root path P = (p_0 = root, ..., p_dn = sn):
+//   r (I + X_P) = y,  X_P[i][j] = b_{p_i} e^{G_{p_i} - G_{p_j}} k_{p_i}.k_{p_j} (i > j),
+//   y = e_dn for T;  y_j = e^{G_n - G_{p_j}} q_n.k_{p_j} for W.
+// With phi_i = e^{G_{p_i} - G_n} >= 1 and s_i = r_i b_{p_i} phi_i:
+//   r_j = y_j - (1 / phi_j) acc_j,  acc_j = sum_{i>j} s_i k_{p_i}.k_{p_j}.
+// Entries are settled from the node towards the root; once s_i is known it is
+// added into every acc_j (j < i) at once.  acc lives in registers; the loop
+// runs from the warp's deepest row, so the step index i is the same in every
+// lane.  The next entry's sum is taken out of acc before the update and only
+// its own term is added, so the chain from one entry to the next is a few
+// dependent operations; the Gram reads and the other updates are off it.
+// (phi is capped at e^80; the capped terms are below fp32 resolution.)  r_j is
+// written as bf16 hi + lo at column p_j of the [T; W] operand row.
+template <int D>
+__device__ __forceinline__ void solve_path_row(const ItemMeta& M, const float* GR,
+                                               uint8_t* smem, int sn, int dn, int wmax,
+                                               bool t_row) {
+  constexpr int NA = D <= 16 ? 16 : 32;  // partial sums held (entries 0 .. NA-1)
+  static_assert(D <= NA, "path fits the partial sums");
+  const uint8_t* prow = M.path[sn];  // entries past the node are 0 (a valid node)
+  const uint4* pr = reinterpret_cast<const uint4*>(prow);
+  const uint4 pa = pr[0], pb = pr[1];
+  const uint32_t pw[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+  const float Gn = M.G[sn];
+  const int a2row = t_row ? sn : 64 + sn;
+  const float* GRq = GR + (64 + sn) * 64;  // q_n . k_s, row 64 + sn (same swizzle phase)
+  const int xq = (sn & 7) << 2;
+  float acc[NA];
+#pragma unroll
+  for (int k = 0; k < NA; ++k) acc[k] = 0.f;
+  float ai = 0.f;  // acc_i of the current step
+  for (int i = wmax; i >= 0; --i) {
+    const int pi = prow[i];
+    const int pn = i > 0 ? prow[i - 1] : 0;  // the next entry's node
+    const float Gi = M.G[pi];
+    const float y = t_row ? (i == dn ? 1.f : 0.f) : __expf(Gn - Gi) * GRq[pi ^ xq];
+    const float r = y - __expf(fmaxf(Gn - Gi, -80.f)) * ai;
+    const bool own = i <= dn;
+    const float s = own ? r * M.bb[pi] * __expf(fminf(Gi - Gn, 80.f)) : 0.f;
+    if (own) {
+      const __nv_bfloat16 hi = __float2bfloat16_rn(r);
+      const __nv_bfloat16 lw = __float2bfloat16_rn(r - __bfloat162float(hi));
+      const int off = atom_off(a2row, pi >> 3) + (pi & 7) * 2;
+      *reinterpret_cast<__nv_bfloat16*>(smem + kOffA2hi + off) = hi;
+      *reinterpret_cast<__nv_bfloat16*>(smem + kOffA2lo + off) = lw;
+    }
+    // Gram row p_i: element (p_i, c) sits at p_i * 64 + (c ^ ((p_i & 7) << 2))
+    const float* GRi = GR + pi * 64;
+    const int xi = (pi & 7) << 2;
+    const float base = pick<NA>(acc, i - 1);  // acc_{i-1} before this step's term
+    const int lim = i - 1;                     // entries 0 .. i-2 take their terms here
+    if (lim <= 8) {
+      path_update<8>(acc, pw, s, GRi, xi, lim);
+    } else if (lim <= 16) {
+      path_update<16>(acc, pw, s, GRi, xi, lim);
+    } else {
+      path_update<(D < 31 ? D : 31)>(acc, pw, s, GRi, xi, lim);
+    }
+    ai = fmaf(s, GRi[pn ^ xi], base);
+  }
+}
+
+template <int kSolveD>
 __global__ void __launch_bounds__(kTcThreads, 1)
 verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                 const __grid_constant__ CUtensorMap vmap,
                  int n_items, int H_qk, int H_v, int depth_max, const int32_t* __restrict__ cu,
                  const int32_t* __restrict__ depth, const int32_t* __restrict__ order,
                  const int32_t* __restrict__ pos, const uint64_t* __restrict__ anc,
-                 int32_t* __restrict__ status, const __nv_bfloat16* __restrict__ v,
+                 int32_t* __restrict__ status,
                  const float* __restrict__ g, const float* __restrict__ bta, float* S,
                  __nv_bfloat16* __restrict__ o, float* __restrict__ Uws,
                  float* __restrict__ Gws, const PendingCommit cm) {
@@ -171,6 +274,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     mbar_init(&sh.tma_bar, 1);
     mbar_init(&sh.mma1_bar, 1);
     mbar_init(&sh.mma2_bar, 1);
+    mbar_init(&sh.v_bar, 1);
     mbar_init(&sh.s1_done[0], 2);
     mbar_init(&sh.s1_done[1], 2);
     mbar_init(&sh.tmem_free[0], 1);
@@ -179,6 +283,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     fence_proxy_async_smem();
     sh.abort = 0;
     sh.tma_issued = 0;
+    sh.v_issued = 0;
   }
   if (warp == 0) tmem_alloc(&sh.tmem_slot, kTmemCols);
   tc_fence_before_sync();
@@ -199,18 +304,19 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       tma_load_3d(smem + kOffA + 24576, &qmap, &sh.tma_bar, 64, qh, row0);
       sh.tma_issued += 1;
     };
-    // S0 of one item: thread p holds rows (p >> 5) + 8 r, float4 column p & 31
-    // (plain loads: with a pending commit the kernel writes these rows back)
-    const int srow0 = p >> 5, sq = p & 31;
+    // S0 of one item: warp w holds rows 16 w .. 16 w + 15, lane p & 31 float4
+    // column p & 31 (plain loads: with a pending commit the kernel writes these
+    // rows back)
+    const int srow0 = (p >> 5) * 16, sq = p & 31;
     float4 sreg[16];
     auto load_s0 = [&](int item) {
       const float* src = S + (size_t)item * kTcDK * kTcDV;  // item = bi * H_v + h
 #pragma unroll
       for (int r = 0; r < 16; ++r)
-        sreg[r] = reinterpret_cast<const float4*>(src + (size_t)(srow0 + 8 * r) * kTcDV)[sq];
+        sreg[r] = reinterpret_cast<const float4*>(src + (size_t)(srow0 + r) * kTcDV)[sq];
     };
-    // Warp 0, one item ahead: the item's accepted path in the previous tree
-    // (lane l holds entry l) and that sequence's bounds and status.
+    // Warp 0, two items ahead of its staging: the item's accepted path in the
+    // previous tree (lane l holds entry l) and that sequence's bounds and status.
     int c_node = -1, c_plo = 0, c_pN = 0, c_st = TGDN_SEQ_OK;
     auto load_commit_meta = [&](int it) {
       const int bi = it / H_v;
@@ -220,22 +326,22 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       c_node = p < cm.path_len ? cm.path[(size_t)bi * cm.path_len + p] : -1;
     };
     // Warp 0: the item's staged path (entries after the first invalid one are
-    // ignored) -> c_L, c_row.
-    auto publish_commit = [&]() {
+    // ignored) -> c_L[cb], c_row[cb].
+    auto publish_commit = [&](int cb) {
       const bool valid =
           c_st == TGDN_SEQ_OK && p < cm.path_len && c_node >= 0 && c_node < c_pN;
       const int L = __ffs(__ballot_sync(0xffffffffu, !valid)) - 1;  // path_len <= 31
-      if (p == 0) sh.c_L = L;
-      if (p < L) sh.c_row[p] = c_plo + c_node;
+      if (p == 0) sh.c_L[cb] = L;
+      if (p < L) sh.c_row[cb][p] = c_plo + c_node;
     };
     // All producer threads: 16-byte asynchronous copies of the published path's
     // u_s rows, k_s rows and the chunks holding G_s (49 chunks per path node).
-    auto stage_commit = [&](int it) {
+    auto stage_commit = [&](int it, int cb) {
       const int h = it % H_v, qh = h / grp;
-      const int L = sh.c_L;
+      const int L = sh.c_L[cb];
       for (int e = p; e < L * 49; e += kGroup) {
         const int l = e / 49, w = e - l * 49;
-        const size_t row = static_cast<size_t>(sh.c_row[l]);
+        const size_t row = static_cast<size_t>(sh.c_row[cb][l]);
         if (w < 32) {
           cp_async16(smem + kOffUP + l * (kTcDV * 4) + w * 16,
                      cm.U + (row * H_v + h) * kTcDV + w * 4);
@@ -245,7 +351,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                          (w - 32) * 8);
         } else {
           const size_t ge = row * H_v + h;  // the workspace base is 256-byte aligned
-          sh.c_gi[l] = static_cast<int>(ge & 3);
+          sh.c_gi[cb][l] = static_cast<int>(ge & 3);
           cp_async16(smem + kOffGP + l * 16, cm.G + (ge & ~static_cast<size_t>(3)));
         }
       }
@@ -275,22 +381,23 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       }
     };
     int item = i_begin;
-    uint32_t mma1_count = 0;  // first products issued so far (thread 0)
     load_seq(item);
-    if (p == 0) issue_kq(item, q_lo);
     load_meta(item);
     if (item + i_step < i_end) load_seq(item + i_step);
     load_s0(item);
     if (fused) {
       if (p < 32) {
         load_commit_meta(item);
-        publish_commit();
+        publish_commit(0);
       }
       named_sync(kBarP, kGroup);
-      stage_commit(item);
+      stage_commit(item, 0);
+      if (p < 32 && item + i_step < i_end) load_commit_meta(item + i_step);
     }
 
-    int prev_bi = -1;  // sequence of the previous item when its tree was valid
+    int prev_bi = -1;           // sequence of the previous item when its tree was valid
+    bool mma1_pending = false;  // thread 0: a first product not yet seen complete
+    uint32_t mma1_seen = 0;     // thread 0: first products seen complete
     for (int j = 0; item < i_end; ++j, item += i_step) {
       const int slot = j & 1;
       ItemMeta& M = sh.meta[slot];
@@ -300,6 +407,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         break;
       const int bi = item / H_v, h = item % H_v;
       const int lo = pf.lo, N = pf.N;
+      const int next = item + i_step;
       bool ok = (pf.st == TGDN_SEQ_OK) && N > 0 && N <= kTcNodes;
       uint64_t my_anc = 0;
       if (p == 0) {
@@ -323,23 +431,15 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         // the previous step's commit: S = e^{G*} S + sum_l e^{G*-G_l} k_l u_l^T,
         // written back in place; the committed state is what gets verified
         cp_async_wait_all();
+        if (p < 32 && next < i_end) publish_commit(slot ^ 1);  // the next item's path
         named_sync(kBarP, kGroup);
-        const int L = sh.c_L;
+        const int L = sh.c_L[slot];
         if (L > 0) {
-          const float* UP = reinterpret_cast<const float*>(smem + kOffUP);
-          const __nv_bfloat16* KP = reinterpret_cast<const __nv_bfloat16*>(smem + kOffKP);
+          const float4* UP = reinterpret_cast<const float4*>(smem + kOffUP);
+          const uint4* KP = reinterpret_cast<const uint4*>(smem + kOffKP);
           const float* GP = reinterpret_cast<const float*>(smem + kOffGP);
-          const float Gstar = GP[(L - 1) * 4 + sh.c_gi[L - 1]];
+          const float Gstar = GP[(L - 1) * 4 + sh.c_gi[slot][L - 1]];
           const float decay = __expf(Gstar);
-          // CK[l][s][r] = e^{G*-G_l} k_l[8 r + s], in the (free) S0 lo operand area: the
-          // 16 rows a thread owns become four 16-byte loads per path node
-          float* CK = reinterpret_cast<float*>(smem + kOffS0lo);
-          for (int e = p; e < L * kTcDK; e += kGroup) {
-            const int l = e >> 7, row = e & 127;
-            CK[l * kTcDK + (row & 7) * 16 + (row >> 3)] =
-                __expf(Gstar - GP[l * 4 + sh.c_gi[l]]) * __bfloat162float(KP[l * kTcDK + row]);
-          }
-          named_sync(kBarP, kGroup);
 #pragma unroll
           for (int r = 0; r < 16; ++r) {
             sreg[r].x *= decay;
@@ -348,33 +448,56 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             sreg[r].w *= decay;
           }
           for (int l = 0; l < L; ++l) {
-            const float4 u = reinterpret_cast<const float4*>(UP + l * kTcDV)[sq];
-            const float4* c4 = reinterpret_cast<const float4*>(CK + l * kTcDK + srow0 * 16);
+            const float cl = __expf(Gstar - GP[l * 4 + sh.c_gi[slot][l]]);
+            float4 u = UP[l * (kTcDV / 4) + sq];
+            u.x *= cl;
+            u.y *= cl;
+            u.z *= cl;
+            u.w *= cl;
+            // k_l at this warp's 16 rows: 32 bytes, the same for the whole warp
+            const uint4 ka = KP[l * (kTcDK / 8) + (srow0 >> 3)];
+            const uint4 kb = KP[l * (kTcDK / 8) + (srow0 >> 3) + 1];
+            const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {  // rows srow0 + 8 (4 i + t), t = 0..3
-              const float4 x = c4[i];
-              const float kv[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-              for (int t = 0; t < 4; ++t) {
-                float4& a = sreg[4 * i + t];
-                a.x = fmaf(kv[t], u.x, a.x);
-                a.y = fmaf(kv[t], u.y, a.y);
-                a.z = fmaf(kv[t], u.z, a.z);
-                a.w = fmaf(kv[t], u.w, a.w);
-              }
+            for (int i = 0; i < 8; ++i) {  // bf16 pair -> rows srow0 + 2 i, + 2 i + 1
+              const float k0 = __uint_as_float(kw[i] << 16);
+              const float k1 = __uint_as_float(kw[i] & 0xffff0000u);
+              float4& a0 = sreg[2 * i];
+              float4& a1 = sreg[2 * i + 1];
+              a0.x = fmaf(k0, u.x, a0.x);
+              a0.y = fmaf(k0, u.y, a0.y);
+              a0.z = fmaf(k0, u.z, a0.z);
+              a0.w = fmaf(k0, u.w, a0.w);
+              a1.x = fmaf(k1, u.x, a1.x);
+              a1.y = fmaf(k1, u.y, a1.y);
+              a1.z = fmaf(k1, u.z, a1.z);
+              a1.w = fmaf(k1, u.w, a1.w);
             }
           }
           float* dst = S + (size_t)item * kTcDK * kTcDV;
 #pragma unroll
           for (int r = 0; r < 16; ++r)
-            reinterpret_cast<float4*>(dst + (size_t)(srow0 + 8 * r) * kTcDV)[sq] = sreg[r];
+            reinterpret_cast<float4*>(dst + (size_t)(srow0 + r) * kTcDV)[sq] = sreg[r];
         }
-        named_sync(kBarP, kGroup);  // staging read; the operand may overwrite it
       }
-      // S0 registers -> bf16 hi/lo operand (the previous product has completed)
+      // Thread 0: the previous first product has completed, so its operands (the
+      // [K; Q] and S0 areas) are free; this item's key and query rows go out.
+      bool step_ok = true;
+      if (p == 0) {
+        if (mma1_pending) {
+          step_ok = mbar_wait_suspend(&sh.mma1_bar, mma1_seen & 1, abort);
+          ++mma1_seen;
+          mma1_pending = false;
+        }
+        if (step_ok) issue_kq(item, lo);
+      }
+      // (also: every thread has finished reading this item's staged commit)
+      if (!named_sync_and(kBarP, kGroup, step_ok && !*abort)) break;
+      if (fused && next < i_end) stage_commit(next, slot ^ 1);
+      // S0 registers -> bf16 hi/lo operand
 #pragma unroll
       for (int r = 0; r < 16; ++r) {
-        const int kr = srow0 + 8 * r;
+        const int kr = srow0 + r;
         const float4 xv = sreg[r];
         const float h0 = __bfloat162float(__float2bfloat16_rn(xv.x));
         const float h1 = __bfloat162float(__float2bfloat16_rn(xv.y));
@@ -388,11 +511,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       }
       fence_proxy_async_smem();
       // prefetch the next item while this one is finished
-      const int next = item + i_step;
       if (next < i_end) {  // the small loads first: they are not queued behind S0
         load_meta(next);
-        if (next + i_step < i_end) load_seq(next + i_step);
-        if (fused && p < 32) load_commit_meta(next);
+        if (next + i_step < i_end) {
+          load_seq(next + i_step);
+          if (fused && p < 32) load_commit_meta(next + i_step);
+        }
         load_s0(next);
       }
       ok = named_sync_and(kBarP, kGroup, ok);
@@ -402,20 +526,23 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       const bool reuse = prev_bi == bi;
       if (ok && p < N && reuse) {
         const int dn = M.dep[p];
-        const ItemMeta& Mp = sh.meta[slot ^ 1];
+        const uint8_t* srow = sh.meta[slot ^ 1].path[p];
+        const uint4* src = reinterpret_cast<const uint4*>(srow);
+        uint4* dst = reinterpret_cast<uint4*>(M.path[p]);
+        dst[0] = src[0];
+        dst[1] = src[1];
         float acc = 0.f;
-#pragma unroll 4
-        for (int i = 0; i <= dn; ++i) {
-          const uint8_t s = Mp.anc_at[i][p];
-          M.anc_at[i][p] = s;
-          acc += M.gg[s];
-        }
+        for (int i = 0; i <= dn; ++i) acc += M.gg[srow[i]];
         M.G[p] = acc;
       } else if (ok && p < N) {
         const int dn = M.dep[p];
         uint64_t mk = my_anc;
         bool pk = __popcll(mk) == dn + 1 && ((mk >> M.pos[p]) & 1ull);
+        uint8_t* prow = M.path[p];
+        reinterpret_cast<uint4*>(prow)[0] = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4*>(prow)[1] = make_uint4(0u, 0u, 0u, 0u);
         float acc = 0.f;
+        int last = -1;
         for (int i = 0; pk && i <= dn; ++i) {
           const int b = __ffsll(static_cast<long long>(mk)) - 1;
           mk &= mk - 1;
@@ -425,60 +552,51 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
           }
           const int s = M.ord[b];
           pk = M.dep[s] == i;
-          M.anc_at[i][p] = static_cast<uint8_t>(s);
+          prow[i] = static_cast<uint8_t>(s);
           acc += M.gg[s];
+          last = s;
         }
-        if (!pk || M.anc_at[dn][p] != p) ok = false;
+        if (!pk || last != p) ok = false;
         M.G[p] = acc;
       }
       ok = named_sync_and(kBarP, kGroup, ok);
       if (p == 0) M.good = ok;
       prev_bi = ok ? bi : -1;
-      // first product into TMEM half `slot` (one thread)
-      bool step_ok = true;
+      // first product into TMEM half `slot` (one thread); its completion is
+      // awaited in the next iteration
       if (p == 0) {
         const bool tma_ok = mbar_wait_suspend(&sh.tma_bar, j & 1, abort);
-        bool issued = false;
         if (tma_ok && ok) {
           tc_fence_after_sync();
           const uint32_t tb = tmem + slot * 256;
           const uint32_t sA = smem_addr(smem + kOffA);
           const uint32_t sHi = smem_addr(smem + kOffS0hi);
           const uint32_t sLo = smem_addr(smem + kOffS0lo);
-          constexpr uint32_t id_s0 = idesc_bf16_f32(128, 64, 0, 1);
+          constexpr uint32_t id_s0 = idesc_bf16_f32(128, 128, 0, 1);
           constexpr uint32_t id_gram = idesc_bf16_f32(128, kTcNodes, 0, 0);
 #pragma unroll
           for (int s = 0; s < kTcDK / 16; ++s) {
             const uint64_t ad = smem_desc(sA + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024,
                                           kSwizzle128B);
-#pragma unroll
-            for (int at = 0; at < 2; ++at) {  // value-column atoms 0-63, 64-127
-              const uint64_t hd =
-                  smem_desc(sHi + at * 16384 + s * 2048, 1024, 1024, kSwizzle128B);
-              const uint64_t ld =
-                  smem_desc(sLo + at * 16384 + s * 2048, 1024, 1024, kSwizzle128B);
-              umma_bf16(tb + at * 64, ad, hd, id_s0, s > 0);
-              umma_bf16(tb + at * 64, ad, ld, id_s0, 1);
-            }
+            // MN-major S0: value-column atoms 16 KiB apart (leading byte offset),
+            // 8-row k groups 1 KiB apart (stride byte offset)
+            const uint64_t hd = smem_desc(sHi + s * 2048, 16384, 1024, kSwizzle128B);
+            const uint64_t ld = smem_desc(sLo + s * 2048, 16384, 1024, kSwizzle128B);
+            umma_bf16(tb, ad, hd, id_s0, s > 0);
+            umma_bf16(tb, ad, ld, id_s0, 1);
             umma_bf16(tb + kGramCol, ad, ad, id_gram, s > 0);  // B = the key rows of A
           }
           umma_commit(&sh.mma1_bar);
           umma_commit(&sh.s1_done[slot]);
-          issued = true;
+          mma1_pending = true;
         } else {
           mbar_arrive(&sh.s1_done[slot]);  // no product: the consumer zero-fills
         }
         mbar_arrive(&sh.s1_done[slot]);  // the metadata above is written
-        // operands are reusable once the product has completed
-        step_ok = tma_ok && (!issued || mbar_wait_suspend(&sh.mma1_bar, mma1_count & 1, abort));
-        if (issued) ++mma1_count;
       }
-      if (fused && p < 32 && next < i_end) publish_commit();
-      if (!named_sync_and(kBarP, kGroup, step_ok && !*abort)) break;
-      if (p == 0 && next < i_end) issue_kq(next, pf.lo);
-      // the S0 operand area is free again: stage the next item's pending commit
-      if (fused && next < i_end) stage_commit(next);
     }
+    // the last first product, before TMEM and the operands are released (bounded)
+    if (p == 0 && mma1_pending) (void)mbar_wait_suspend(&sh.mma1_bar, mma1_seen & 1, abort);
   } else {
     // =================================================== consumer warps 8-15
     const int c = tid - kGroup;
@@ -489,32 +607,26 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     const int lane_row = lq * 32 + (c & 31);
     const bool key_lane = lq < 2;
     const int lane_node = key_lane ? lane_row : lane_row - 64;
-    uint4 vreg[8];
-    int cv_lo = 0, cv_N = 0;  // bounds of the sequence load_v reads next (one item ahead)
-    auto load_vseq = [&](int item) {
-      const int bi = item / H_v;
-      cv_lo = cu[bi];
-      cv_N = cu[bi + 1] - cv_lo;
-    };
-    auto load_v = [&](int item) {  // this thread's V row, 64 value columns
-      if (!key_lane) return;
-      const int h = item % H_v;
-      const int lo = cv_lo, N = cv_N;
-      if (lane_node < N && N <= kTcNodes) {
-        const uint4* vp = reinterpret_cast<const uint4*>(
-            v + ((size_t)(lo + lane_node) * H_v + h) * kTcDV + chalf * 64);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) vreg[i] = __ldg(vp + i);
-      }
+    // Thread 0, one item ahead: the V rows of an item go by TMA into the R lo
+    // operand area (the same swizzled layout), where R is then formed in place.
+    int cv_lo = 0;  // first node row of the item whose V rows go out next
+    auto load_vseq = [&](int item) { cv_lo = cu[item / H_v]; };
+    auto issue_v = [&](int item) {
+      mbar_arrive_expect_tx(&sh.v_bar, 2 * 64 * 128);
+      tma_load_3d(smem + kOffRlo, &vmap, &sh.v_bar, 0, item % H_v, cv_lo);
+      tma_load_3d(smem + kOffRlo + 8192, &vmap, &sh.v_bar, 64, item % H_v, cv_lo);
+      sh.v_issued += 1;
     };
     int item = i_begin;
-    load_vseq(item);
-    load_v(item);
-    if (item + i_step < i_end) load_vseq(item + i_step);
-    float* SSbase = reinterpret_cast<float*>(smem + kOffSS);
+    if (c == 0) {
+      load_vseq(item);
+      issue_v(item);
+      if (item + i_step < i_end) load_vseq(item + i_step);
+    }
     uint32_t mma2_count = 0;  // second products issued so far (same in every thread)
     for (int j = 0; item < i_end; ++j, item += i_step) {
       const int slot = j & 1;
+      bulk_wait_read();  // the previous item's output rows have left shared memory
       if (!group_wait(&sh.s1_done[slot], (j >> 1) & 1, kBarC, c == 0, abort)) break;
       tc_fence_after_sync();
       const ItemMeta& M = sh.meta[slot];
@@ -530,11 +642,15 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
           *reinterpret_cast<float4*>(Uws + row) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         for (int n = c; n < N; n += kGroup) Gws[(size_t)(lo + n) * H_v + h] = 0.f;
-        if (next < i_end) {
-          load_v(next);
-          if (next + i_step < i_end) load_vseq(next + i_step);
+        bool v_ok = true;
+        if (c == 0) {  // this item's V rows have landed: the area is free for the next
+          v_ok = mbar_wait_suspend(&sh.v_bar, j & 1, abort);
+          if (v_ok && next < i_end) {
+            issue_v(next);
+            if (next + i_step < i_end) load_vseq(next + i_step);
+          }
         }
-        named_sync(kBarC, kGroup);
+        if (!named_sync_and(kBarC, kGroup, v_ok)) break;
         if (c == 0) mbar_arrive(&sh.tmem_free[slot]);
         continue;
       }
@@ -559,7 +675,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       // Key-lane warps form R while the query-lane warps solve for T and W (the
       // solve needs only the Gram rows and the metadata).
       // ---- R = diag(b)(V - e^G K S0) as a bf16 hi/lo operand (key lanes)
+      bool v_ok = true;
       if (key_lane) {
+        v_ok = mbar_wait_suspend(&sh.v_bar, j & 1, abort);
         const bool live = lane_node < N;
         const float eG = live ? __expf(M.G[lane_node]) : 0.f;
         const float bn = live ? M.bb[lane_node] : 0.f;
@@ -570,8 +688,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
           tmem_ld_wait();
 #pragma unroll
           for (int c8 = 0; c8 < 4; ++c8) {  // 8 columns per 16-byte bf16 chunk
-            const __nv_bfloat162* vb =
-                reinterpret_cast<const __nv_bfloat162*>(&vreg[q * 4 + c8]);
+            const int off = chalf * 8192 + atom_off(lane_node, q * 4 + c8);
+            const uint4 vv = *reinterpret_cast<const uint4*>(smem + kOffRlo + off);
+            const __nv_bfloat162* vb = reinterpret_cast<const __nv_bfloat162*>(&vv);
             float xr[8];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -581,64 +700,28 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             }
             uint4 hi, lw;
             split8(xr, hi, lw);  // rows of R beyond the tree are exact zeros
-            const int off = chalf * 8192 + atom_off(lane_node, q * 4 + c8);
             *reinterpret_cast<uint4*>(smem + kOffRhi + off) = hi;
             *reinterpret_cast<uint4*>(smem + kOffRlo + off) = lw;
           }
         }
       }
-      if (next < i_end) {  // V rows of the next item, ahead of time
-        load_v(next);
-        if (next + i_step < i_end) load_vseq(next + i_step);
-      }
 
-      // ---- one row of T (sc < 64) or W (64 <= sc < 128), by back substitution on
-      // the root path P = (p_0 = root, ..., p_d = n):
-      //   r (I + X_P) = y,  X_P[i][j] = b_{p_i} e^{G_{p_i} - G_{p_j}} k_{p_i}.k_{p_j} (i > j),
-      //   y = e_d for T;  y_j = e^{G_n - G_{p_j}} q_n.k_{p_j} for W.
-      // With phi_i = e^{G_{p_i} - G_n} >= 1 and s_i = r_i b_{p_i} phi_i:
-      //   r_j = y_j - (1 / phi_j) sum_{i>j} s_i k_{p_i}.k_{p_j}.
-      // (phi is capped at e^80; the capped terms are below fp32 resolution.)
-      // Rows are handed out in topological order so that a warp sees similar depths.
+      // ---- one row of T (sc < 64) or W (64 <= sc < 128) per query-lane thread
+      // (solve_path_row).  Rows are handed out in topological order so that a
+      // warp sees similar depths.
       if (!key_lane) {
         const int sc = (lq - 2) * 64 + chalf * 32 + (c & 31);  // solver index 0..127
-        const bool t_row = sc < 64;
         const int spos = sc & 63;
-        if (spos < N) {
-          const int sn = M.ord[spos];
-          const int a2row = t_row ? sn : 64 + sn;
-          const int dn = M.dep[sn];
-          const uint8_t* P = &M.anc_at[0][sn];  // P[i * kTcNodes]: ancestor at depth i
-          float* SS = SSbase + sc * kTcPath;
-          const float* GR = reinterpret_cast<const float*>(smem + kOffGR);
-          const float Gn = M.G[sn];
-          const int qrow = 64 + sn;
-          for (int jj = dn; jj >= 0; --jj) {
-            const int pj = P[jj * kTcNodes];
-            const float Gj = M.G[pj];
-            const int cj = pj >> 2, wj = pj & 3;
-            const float inv_phi = __expf(fmaxf(Gn - Gj, -80.f));
-            const float y = t_row ? ((jj == dn) ? 1.f : 0.f)
-                                  : __expf(Gn - Gj) * GR[qrow * 64 + swz(qrow, cj) * 4 + wj];
-            float acc = 0.f;
-#pragma unroll 4
-            for (int i = jj + 1; i <= dn; ++i) {
-              const int pi = P[i * kTcNodes];
-              acc = fmaf(SS[i], GR[pi * 64 + swz(pi, cj) * 4 + wj], acc);
-            }
-            const float rj = y - inv_phi * acc;
-            SS[jj] = rj * M.bb[pj] * __expf(fminf(Gj - Gn, 80.f));
-            const __nv_bfloat16 hi = __float2bfloat16_rn(rj);
-            const __nv_bfloat16 lw = __float2bfloat16_rn(rj - __bfloat162float(hi));
-            const int off = atom_off(a2row, pj >> 3) + (pj & 7) * 2;
-            *reinterpret_cast<__nv_bfloat16*>(smem + kOffA2hi + off) = hi;
-            *reinterpret_cast<__nv_bfloat16*>(smem + kOffA2lo + off) = lw;
-          }
-        }
+        const bool act = spos < N;
+        const int sn = act ? M.ord[spos] : 0;
+        const int dn = act ? M.dep[sn] : -1;
+        const int wmax = __reduce_max_sync(0xffffffffu, dn);
+        solve_path_row<kSolveD>(M, reinterpret_cast<const float*>(smem + kOffGR), smem, sn, dn,
+                                wmax, sc < 64);
       }
       fence_proxy_async_smem();
       tc_fence_before_sync();
-      named_sync(kBarC, kGroup);
+      if (!named_sync_and(kBarC, kGroup, v_ok)) break;
       tc_fence_after_sync();
 
       // ---- second product: D[:, 128:256] = [T; W] R  (hi.hi + hi.lo + lo.hi)
@@ -647,20 +730,18 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         const uint32_t sA2lo = smem_addr(smem + kOffA2lo);
         const uint32_t sRhi = smem_addr(smem + kOffRhi);
         const uint32_t sRlo = smem_addr(smem + kOffRlo);
-        constexpr uint32_t id_r = idesc_bf16_f32(128, 64, 0, 1);
+        constexpr uint32_t id_r = idesc_bf16_f32(128, 128, 0, 1);
 #pragma unroll
         for (int s = 0; s < kTcNodes / 16; ++s) {
           const uint64_t ah = smem_desc(sA2hi + s * 32, 16, 1024, kSwizzle128B);
           const uint64_t al = smem_desc(sA2lo + s * 32, 16, 1024, kSwizzle128B);
-#pragma unroll
-          for (int at = 0; at < 2; ++at) {
-            const uint64_t bh = smem_desc(sRhi + at * 8192 + s * 2048, 1024, 1024, kSwizzle128B);
-            const uint64_t bl = smem_desc(sRlo + at * 8192 + s * 2048, 1024, 1024, kSwizzle128B);
-            const uint32_t d = tb + kGramCol + at * 64;
-            umma_bf16(d, ah, bh, id_r, s > 0);
-            umma_bf16(d, ah, bl, id_r, 1);
-            umma_bf16(d, al, bh, id_r, 1);
-          }
+          // MN-major R: value-column atoms 8 KiB apart, 8-node groups 1 KiB apart
+          const uint64_t bh = smem_desc(sRhi + s * 2048, 8192, 1024, kSwizzle128B);
+          const uint64_t bl = smem_desc(sRlo + s * 2048, 8192, 1024, kSwizzle128B);
+          const uint32_t d = tb + kGramCol;
+          umma_bf16(d, ah, bh, id_r, s > 0);
+          umma_bf16(d, ah, bl, id_r, 1);
+          umma_bf16(d, al, bh, id_r, 1);
         }
         umma_commit(&sh.mma2_bar);
       }
@@ -668,26 +749,37 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       ++mma2_count;
       if (!done2) break;
       tc_fence_after_sync();
+      // the operand areas are free: the next item's V rows go out now
+      if (c == 0 && next < i_end) {
+        issue_v(next);
+        if (next + i_step < i_end) load_vseq(next + i_step);
+      }
 
-      // ---- key lanes: U rows to the workspace; query lanes: O = e^G Q S0 + W R
+      // ---- key lanes: U rows; query lanes: O = e^G Q S0 + W R (bf16).  Each
+      // thread stages its half row in shared memory (padded rows: conflict-free)
+      // and sends it to global memory with one bulk copy.
       {
         const bool live = lane_node < N;
         if (key_lane) {
+          float4* stg = reinterpret_cast<float4*>(smem + kOffUst + lane_node * kUstRow + chalf * 256);
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             float r[32];
             tmem_ld32(tb + lane_base + kGramCol + chalf * 64 + q * 32, r);
             tmem_ld_wait();
-            if (live) {
-              float4* dst = reinterpret_cast<float4*>(
-                  Uws + ((size_t)(lo + lane_node) * H_v + h) * kTcDV + chalf * 64 + q * 32);
 #pragma unroll
-              for (int i = 0; i < 8; ++i)
-                dst[i] = make_float4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
-            }
+            for (int i = 0; i < 8; ++i)
+              stg[q * 8 + i] = make_float4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
           }
-          if (live && chalf == 0) Gws[(size_t)(lo + lane_node) * H_v + h] = M.G[lane_node];
+          if (live) {
+            fence_proxy_async_smem();
+            bulk_copy_s2g(Uws + ((size_t)(lo + lane_node) * H_v + h) * kTcDV + chalf * 64, stg,
+                          256);
+            bulk_commit();
+            if (chalf == 0) Gws[(size_t)(lo + lane_node) * H_v + h] = M.G[lane_node];
+          }
         } else {
+          uint4* stg = reinterpret_cast<uint4*>(smem + kOffOst + lane_node * kOstRow + chalf * 128);
           const float eG = live ? __expf(M.G[lane_node]) : 0.f;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {  // 16 value columns at a time
@@ -695,19 +787,21 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             tmem_ld16(tb + lane_base + chalf * 64 + q * 16, a);
             tmem_ld16(tb + lane_base + kGramCol + chalf * 64 + q * 16, w);
             tmem_ld_wait();
-            if (live) {
-              uint4* dst = reinterpret_cast<uint4*>(
-                  o + ((size_t)(lo + lane_node) * H_v + h) * kTcDV + chalf * 64 + q * 16);
 #pragma unroll
-              for (int i = 0; i < 2; ++i) {
-                const float* aa = a + 8 * i;
-                const float* ww = w + 8 * i;
-                dst[i] = make_uint4(pack_bf16x2(fmaf(eG, aa[0], ww[0]), fmaf(eG, aa[1], ww[1])),
-                                    pack_bf16x2(fmaf(eG, aa[2], ww[2]), fmaf(eG, aa[3], ww[3])),
-                                    pack_bf16x2(fmaf(eG, aa[4], ww[4]), fmaf(eG, aa[5], ww[5])),
-                                    pack_bf16x2(fmaf(eG, aa[6], ww[6]), fmaf(eG, aa[7], ww[7])));
-              }
+            for (int i = 0; i < 2; ++i) {
+              const float* aa = a + 8 * i;
+              const float* ww = w + 8 * i;
+              stg[q * 2 + i] =
+                  make_uint4(pack_bf16x2(fmaf(eG, aa[0], ww[0]), fmaf(eG, aa[1], ww[1])),
+                             pack_bf16x2(fmaf(eG, aa[2], ww[2]), fmaf(eG, aa[3], ww[3])),
+                             pack_bf16x2(fmaf(eG, aa[4], ww[4]), fmaf(eG, aa[5], ww[5])),
+                             pack_bf16x2(fmaf(eG, aa[6], ww[6]), fmaf(eG, aa[7], ww[7])));
             }
+          }
+          if (live) {
+            fence_proxy_async_smem();
+            bulk_copy_s2g(o + ((size_t)(lo + lane_node) * H_v + h) * kTcDV + chalf * 64, stg, 128);
+            bulk_commit();
           }
         }
       }
@@ -715,16 +809,18 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       named_sync(kBarC, kGroup);
       if (c == 0) mbar_arrive(&sh.tmem_free[slot]);  // this half is free again
     }
+    bulk_wait_all();  // this thread's output rows are written
   }
 
   // ---- end.  After an expired wait every item still owned by this CTA is
-  // reported as timed out, and the latest copy and products are drained (bounded).
+  // reported as timed out, and the latest copies and products are drained (bounded).
   cp_async_wait_all();  // staging copies left by a loop that ended early
   __syncthreads();
   if (sh.abort && tid == 0) {
     for (int it2 = i_begin; it2 < i_end; it2 += i_step)
       atomicCAS(&status[it2 / H_v], TGDN_SEQ_OK, TGDN_SEQ_TIMEOUT);
     if (sh.tma_issued > 0) (void)mbar_wait(&sh.tma_bar, (sh.tma_issued - 1) & 1);
+    if (sh.v_issued > 0) (void)mbar_wait(&sh.v_bar, (sh.v_issued - 1) & 1);
   }
   __syncthreads();
   if (warp == 0) {
@@ -759,20 +855,22 @@ static int sm_count() {
 }
 
 cudaError_t launch_verify_tc(const tgdn_tree& t, const tgdn_dims& d, const CUtensorMap& qmap,
-                             const CUtensorMap& kmap, const void* v, const float* g,
+                             const CUtensorMap& kmap, const CUtensorMap& vmap, const float* g,
                              const float* b, float* S, void* o, float* U, float* G,
                              const PendingCommit& cm, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(verify_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
+  // the path solve keeps depth_max + 1 partial sums in registers
+  auto kern = t.depth_max <= 16 ? verify_tc_kernel<16> : verify_tc_kernel<kTcDepth>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
   if (e != cudaSuccess) return e;
   const long items = (long)t.B * d.H_v;
   if (items == 0) return cudaSuccess;
   if (items > 0x7fffffffL) return cudaErrorInvalidConfiguration;
   const int sms = sm_count();
   const int grid = (int)(items < sms ? items : sms);
-  verify_tc_kernel<<<grid, kTcThreads, kTcSmemBytes, s>>>(
-      qmap, kmap, (int)items, d.H_qk, d.H_v, t.depth_max, t.cu_nodes, t.depth, t.order, t.pos,
-      t.anc, t.status, static_cast<const __nv_bfloat16*>(v), g, b, S,
+  kern<<<grid, kTcThreads, kTcSmemBytes, s>>>(
+      qmap, kmap, vmap, (int)items, d.H_qk, d.H_v, t.depth_max, t.cu_nodes, t.depth, t.order,
+      t.pos, t.anc, t.status, g, b, S,
       static_cast<__nv_bfloat16*>(o), U, G, cm);
   return cudaGetLastError();
 }
