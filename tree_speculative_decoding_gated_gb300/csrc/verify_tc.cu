@@ -103,6 +103,7 @@ struct TcShared {
   int abort;
   int tma_issued;
   int v_issued;
+  int mma1_issued;
   int c_L[2];             // staged path length per item parity (0: nothing to commit)
   int c_row[2][kTcPath];  // previous-step node rows of the staged path
   int c_gi[2][kTcPath];   // index of G_s within its staged 16-byte chunk
@@ -167,14 +168,34 @@ __device__ __forceinline__ float pick(const float (&v)[N], int k) {
   return t[0];
 }
 
-// acc[j] += s * row[p_j ^ x] for j < W and j < lim (p_j: byte j of the path).
+// Byte j of the packed root path (a node index).
+__device__ __forceinline__ int path_at(const uint32_t (&pw)[8], int j) {
+  return static_cast<int>((pw[j >> 2] >> (8 * (j & 3))) & 0xffu);
+}
+
+// acc[j] += s * row[p_j ^ x] for j < W.  Only j < i - 1 matter at step i; the
+// other entries are either the next one (taken out before) or settled ones,
+// never read again, so the width only has to cover i - 1 (no per-entry test).
 template <int W, int N>
 __device__ __forceinline__ void path_update(float (&acc)[N], const uint32_t (&pw)[8], float s,
-                                            const float* row, int x, int lim) {
+                                            const float* row, int x) {
+  static_assert(W <= N, "width within the partial sums");
 #pragma unroll
-  for (int j = 0; j < W; ++j)
-    if (j < lim)
-      acc[j] = fmaf(s, row[static_cast<int>((pw[j >> 2] >> (8 * (j & 3))) & 0xffu) ^ x], acc[j]);
+  for (int j = 0; j < W; ++j) acc[j] = fmaf(s, row[path_at(pw, j) ^ x], acc[j]);
+}
+
+// The same for the T and W rows of one node (one Gram read, two sums).
+template <int W, int N>
+__device__ __forceinline__ void path_update2(float (&accT)[N], float (&accW)[N],
+                                             const uint32_t (&pw)[8], float sT, float sW,
+                                             const float* row, int x) {
+  static_assert(W <= N, "width within the partial sums");
+#pragma unroll
+  for (int j = 0; j < W; ++j) {
+    const float gk = row[path_at(pw, j) ^ x];
+    accT[j] = fmaf(sT, gk, accT[j]);
+    accW[j] = fmaf(sW, gk, accW[j]);
+  }
 }
 
 // One row of T (t_row) or W of the node sn at depth dn, by substitution along
@@ -209,14 +230,27 @@ __device__ __forceinline__ void solve_path_row(const ItemMeta& M, const float* G
 #pragma unroll
   for (int k = 0; k < NA; ++k) acc[k] = 0.f;
   float ai = 0.f;  // acc_i of the current step
+  // Software pipeline: the path entry two steps ahead and the gate, beta and
+  // query-Gram value one step ahead are loaded before they are needed.
+  int pi = prow[wmax];
+  int pn = wmax > 0 ? prow[wmax - 1] : 0;  // the next entry's node
+  float Gi = M.G[pi], bi = M.bb[pi];
+  float qi = t_row ? 0.f : GRq[pi ^ xq];
   for (int i = wmax; i >= 0; --i) {
-    const int pi = prow[i];
-    const int pn = i > 0 ? prow[i - 1] : 0;  // the next entry's node
-    const float Gi = M.G[pi];
-    const float y = t_row ? (i == dn ? 1.f : 0.f) : __expf(Gn - Gi) * GRq[pi ^ xq];
-    const float r = y - __expf(fmaxf(Gn - Gi, -80.f)) * ai;
+    const int pnn = i > 1 ? prow[i - 2] : 0;
+    const float Gnx = M.G[pn], bnx = M.bb[pn];
+    const float qnx = t_row ? 0.f : GRq[pn ^ xq];
+    // Gram row p_i: element (p_i, c) sits at p_i * 64 + (c ^ ((p_i & 7) << 2))
+    const float* GRi = GR + pi * 64;
+    const int xi = (pi & 7) << 2;
+    const float kn = GRi[pn ^ xi];  // k_{p_i}.k_{p_{i-1}}
+    const float y = t_row ? (i == dn ? 1.f : 0.f) : __expf(Gn - Gi) * qi;
+    const float inv_phi = __expf(fmaxf(Gn - Gi, -80.f));
+    const float f = bi * __expf(fminf(Gi - Gn, 80.f));
+    const float base = pick<NA>(acc, i - 1);  // acc_{i-1} before this step's term
+    const float r = y - inv_phi * ai;
     const bool own = i <= dn;
-    const float s = own ? r * M.bb[pi] * __expf(fminf(Gi - Gn, 80.f)) : 0.f;
+    const float s = own ? r * f : 0.f;
     if (own) {
       const __nv_bfloat16 hi = __float2bfloat16_rn(r);
       const __nv_bfloat16 lw = __float2bfloat16_rn(r - __bfloat162float(hi));
@@ -224,19 +258,96 @@ __device__ __forceinline__ void solve_path_row(const ItemMeta& M, const float* G
       *reinterpret_cast<__nv_bfloat16*>(smem + kOffA2hi + off) = hi;
       *reinterpret_cast<__nv_bfloat16*>(smem + kOffA2lo + off) = lw;
     }
-    // Gram row p_i: element (p_i, c) sits at p_i * 64 + (c ^ ((p_i & 7) << 2))
+    const int lim = i - 1;  // entries 0 .. i-2 take their terms here
+    if (lim <= 8) {
+      path_update<8>(acc, pw, s, GRi, xi);
+    } else if (lim <= 16) {
+      path_update<16>(acc, pw, s, GRi, xi);
+    } else if (lim <= 24) {
+      path_update<(NA < 24 ? NA : 24)>(acc, pw, s, GRi, xi);
+    } else {
+      path_update<NA>(acc, pw, s, GRi, xi);
+    }
+    ai = fmaf(s, kn, base);
+    pi = pn;
+    pn = pnn;
+    Gi = Gnx;
+    bi = bnx;
+    qi = qnx;
+  }
+}
+
+// The T row and the W row of node sn together (trees of depth <= 16): one path
+// walk, one Gram read per entry for both sums, the gate factors shared.
+template <int D>
+__device__ __forceinline__ void solve_path_pair(const ItemMeta& M, const float* GR,
+                                                uint8_t* smem, int sn, int dn, int wmax) {
+  static_assert(D <= 16, "paired rows keep 2 x 16 partial sums");
+  constexpr int NA = 16;
+  const uint8_t* prow = M.path[sn];  // entries past the node are 0 (a valid node)
+  const uint4* pr = reinterpret_cast<const uint4*>(prow);
+  const uint4 pa = pr[0], pb = pr[1];
+  const uint32_t pw[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+  const float Gn = M.G[sn];
+  const float* GRq = GR + (64 + sn) * 64;  // q_n . k_s, row 64 + sn (same swizzle phase)
+  const int xq = (sn & 7) << 2;
+  float accT[NA], accW[NA];
+#pragma unroll
+  for (int k = 0; k < NA; ++k) {
+    accT[k] = 0.f;
+    accW[k] = 0.f;
+  }
+  float aiT = 0.f, aiW = 0.f;
+  int pi = prow[wmax];
+  int pn = wmax > 0 ? prow[wmax - 1] : 0;
+  float Gi = M.G[pi], bi = M.bb[pi], qi = GRq[pi ^ xq];
+  for (int i = wmax; i >= 0; --i) {
+    const int pnn = i > 1 ? prow[i - 2] : 0;
+    const float Gnx = M.G[pn], bnx = M.bb[pn], qnx = GRq[pn ^ xq];
     const float* GRi = GR + pi * 64;
     const int xi = (pi & 7) << 2;
-    const float base = pick<NA>(acc, i - 1);  // acc_{i-1} before this step's term
-    const int lim = i - 1;                     // entries 0 .. i-2 take their terms here
-    if (lim <= 8) {
-      path_update<8>(acc, pw, s, GRi, xi, lim);
-    } else if (lim <= 16) {
-      path_update<16>(acc, pw, s, GRi, xi, lim);
-    } else {
-      path_update<(D < 31 ? D : 31)>(acc, pw, s, GRi, xi, lim);
+    const float kn = GRi[pn ^ xi];
+    const float yW = __expf(Gn - Gi) * qi;
+    const float inv_phi = __expf(fmaxf(Gn - Gi, -80.f));
+    const float f = bi * __expf(fminf(Gi - Gn, 80.f));
+    const float baseT = pick<NA>(accT, i - 1);
+    const float baseW = pick<NA>(accW, i - 1);
+    const float rT = (i == dn ? 1.f : 0.f) - inv_phi * aiT;
+    const float rW = yW - inv_phi * aiW;
+    const bool own = i <= dn;
+    const float sT = own ? rT * f : 0.f;
+    const float sW = own ? rW * f : 0.f;
+    if (own) {
+      const int col = (pi >> 3);
+      const int sub = (pi & 7) * 2;
+      const int offT = atom_off(sn, col) + sub;
+      const int offW = atom_off(64 + sn, col) + sub;
+      const __nv_bfloat16 hT = __float2bfloat16_rn(rT);
+      const __nv_bfloat16 hW = __float2bfloat16_rn(rW);
+      *reinterpret_cast<__nv_bfloat16*>(smem + kOffA2hi + offT) = hT;
+      *reinterpret_cast<__nv_bfloat16*>(smem + kOffA2lo + offT) =
+          __float2bfloat16_rn(rT - __bfloat162float(hT));
+      *reinterpret_cast<__nv_bfloat16*>(smem + kOffA2hi + offW) = hW;
+      *reinterpret_cast<__nv_bfloat16*>(smem + kOffA2lo + offW) =
+          __float2bfloat16_rn(rW - __bfloat162float(hW));
     }
-    ai = fmaf(s, GRi[pn ^ xi], base);
+    const int lim = i - 1;
+    if (lim <= 4) {
+      path_update2<4>(accT, accW, pw, sT, sW, GRi, xi);
+    } else if (lim <= 8) {
+      path_update2<8>(accT, accW, pw, sT, sW, GRi, xi);
+    } else if (lim <= 12) {
+      path_update2<12>(accT, accW, pw, sT, sW, GRi, xi);
+    } else {
+      path_update2<16>(accT, accW, pw, sT, sW, GRi, xi);
+    }
+    aiT = fmaf(sT, kn, baseT);
+    aiW = fmaf(sW, kn, baseW);
+    pi = pn;
+    pn = pnn;
+    Gi = Gnx;
+    bi = bnx;
+    qi = qnx;
   }
 }
 
@@ -284,6 +395,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     sh.abort = 0;
     sh.tma_issued = 0;
     sh.v_issued = 0;
+    sh.mma1_issued = 0;
   }
   if (warp == 0) tmem_alloc(&sh.tmem_slot, kTmemCols);
   tc_fence_before_sync();
@@ -317,19 +429,21 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     };
     // Warp 0, two items ahead of its staging: the item's accepted path in the
     // previous tree (lane l holds entry l) and that sequence's bounds and status.
-    int c_node = -1, c_plo = 0, c_pN = 0, c_st = TGDN_SEQ_OK;
+    // (Raw values only: nothing here waits for these loads; they are combined
+    // when the item is published, an iteration later.)
+    int c_node = -1, c_plo = 0, c_phi = 0, c_st = TGDN_SEQ_OK;
     auto load_commit_meta = [&](int it) {
       const int bi = it / H_v;
       c_plo = cm.cu[bi];
-      c_pN = cm.cu[bi + 1] - c_plo;
+      c_phi = cm.cu[bi + 1];
       c_st = cm.status[bi];
-      c_node = p < cm.path_len ? cm.path[(size_t)bi * cm.path_len + p] : -1;
+      c_node = cm.path[(size_t)bi * cm.path_len + (p < cm.path_len ? p : cm.path_len - 1)];
     };
     // Warp 0: the item's staged path (entries after the first invalid one are
     // ignored) -> c_L[cb], c_row[cb].
     auto publish_commit = [&](int cb) {
-      const bool valid =
-          c_st == TGDN_SEQ_OK && p < cm.path_len && c_node >= 0 && c_node < c_pN;
+      const bool valid = c_st == TGDN_SEQ_OK && p < cm.path_len && c_node >= 0 &&
+                         c_node < c_phi - c_plo;
       const int L = __ffs(__ballot_sync(0xffffffffu, !valid)) - 1;  // path_len <= 31
       if (p == 0) sh.c_L[cb] = L;
       if (p < L) sh.c_row[cb][p] = c_plo + c_node;
@@ -358,19 +472,20 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       cp_async_commit();
     };
     // Sequence bounds and status one item ahead of the node metadata, so that no
-    // load waits on another load of the same iteration.
-    int q_lo = 0, q_N = 0, q_st = 0;
+    // load waits on another load of the same iteration (raw bounds: the count is
+    // formed when they are used).
+    int q_lo = 0, q_hi = 0, q_st = 0;
     auto load_seq = [&](int item) {
       const int bi = item / H_v;
       q_lo = cu[bi];
-      q_N = cu[bi + 1] - q_lo;
+      q_hi = cu[bi + 1];
       q_st = status[bi];
     };
     Prefetch pf;
     auto load_meta = [&](int item) {  // node metadata; the bounds come from load_seq
       const int h = item % H_v;
       pf.lo = q_lo;
-      pf.N = q_N;
+      pf.N = q_hi - q_lo;
       pf.st = q_st;
       if (p < pf.N && p < kTcNodes) {
         pf.dep = depth[pf.lo + p];
@@ -395,9 +510,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       if (p < 32 && item + i_step < i_end) load_commit_meta(item + i_step);
     }
 
-    int prev_bi = -1;           // sequence of the previous item when its tree was valid
-    bool mma1_pending = false;  // thread 0: a first product not yet seen complete
-    uint32_t mma1_seen = 0;     // thread 0: first products seen complete
+    int prev_bi = -1;  // sequence of the previous item when its tree was valid
     for (int j = 0; item < i_end; ++j, item += i_step) {
       const int slot = j & 1;
       ItemMeta& M = sh.meta[slot];
@@ -432,7 +545,14 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         // written back in place; the committed state is what gets verified
         cp_async_wait_all();
         if (p < 32 && next < i_end) publish_commit(slot ^ 1);  // the next item's path
-        named_sync(kBarP, kGroup);
+        // thread 0: the previous first product has completed, so its operands (the
+        // [K; Q] and S0 areas) are free; this item's key and query rows go out
+        bool w_ok = true;
+        if (p == 0) {
+          if (j > 0) w_ok = mbar_wait_suspend(&sh.mma1_bar, (j - 1) & 1, abort);
+          if (w_ok) issue_kq(item, lo);
+        }
+        if (!named_sync_and(kBarP, kGroup, w_ok && !*abort)) break;
         const int L = sh.c_L[slot];
         if (L > 0) {
           const float4* UP = reinterpret_cast<const float4*>(smem + kOffUP);
@@ -447,16 +567,26 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             sreg[r].z *= decay;
             sreg[r].w *= decay;
           }
+          // one path node per step; its u row, k rows and G_s are read a step ahead
+          const int kq = srow0 >> 3;  // 16-byte chunk of this warp's 16 rows of k
+          float4 un = UP[sq];
+          uint4 kan = KP[kq], kbn = KP[kq + 1];
+          float gn = GP[sh.c_gi[slot][0]];
           for (int l = 0; l < L; ++l) {
-            const float cl = __expf(Gstar - GP[l * 4 + sh.c_gi[slot][l]]);
-            float4 u = UP[l * (kTcDV / 4) + sq];
+            float4 u = un;
+            const uint4 ka = kan, kb = kbn;
+            const float cl = __expf(Gstar - gn);
+            if (l + 1 < L) {
+              un = UP[(l + 1) * (kTcDV / 4) + sq];
+              kan = KP[(l + 1) * (kTcDK / 8) + kq];
+              kbn = KP[(l + 1) * (kTcDK / 8) + kq + 1];
+              gn = GP[(l + 1) * 4 + sh.c_gi[slot][l + 1]];
+            }
             u.x *= cl;
             u.y *= cl;
             u.z *= cl;
             u.w *= cl;
             // k_l at this warp's 16 rows: 32 bytes, the same for the whole warp
-            const uint4 ka = KP[l * (kTcDK / 8) + (srow0 >> 3)];
-            const uint4 kb = KP[l * (kTcDK / 8) + (srow0 >> 3) + 1];
             const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
 #pragma unroll
             for (int i = 0; i < 8; ++i) {  // bf16 pair -> rows srow0 + 2 i, + 2 i + 1
@@ -474,21 +604,17 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
               a1.w = fmaf(k1, u.w, a1.w);
             }
           }
+          // the committed rows, written back in place (a warp stores whole rows)
           float* dst = S + (size_t)item * kTcDK * kTcDV;
 #pragma unroll
           for (int r = 0; r < 16; ++r)
             reinterpret_cast<float4*>(dst + (size_t)(srow0 + r) * kTcDV)[sq] = sreg[r];
         }
       }
-      // Thread 0: the previous first product has completed, so its operands (the
-      // [K; Q] and S0 areas) are free; this item's key and query rows go out.
+      // Without a pending commit the same hand-over happens here.
       bool step_ok = true;
-      if (p == 0) {
-        if (mma1_pending) {
-          step_ok = mbar_wait_suspend(&sh.mma1_bar, mma1_seen & 1, abort);
-          ++mma1_seen;
-          mma1_pending = false;
-        }
+      if (!fused && p == 0) {
+        if (j > 0) step_ok = mbar_wait_suspend(&sh.mma1_bar, (j - 1) & 1, abort);
         if (step_ok) issue_kq(item, lo);
       }
       // (also: every thread has finished reading this item's staged commit)
@@ -510,6 +636,39 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             make_uint2(pack_bf16x2(xv.x - h0, xv.y - h1), pack_bf16x2(xv.z - h2, xv.w - h3));
       }
       fence_proxy_async_smem();
+      named_sync(kBarP, kGroup);  // the S0 operand is complete
+      // First product into TMEM half `slot`, issued by the group's last thread (no
+      // node of its own) while the others prefetch and build the paths; its
+      // completion is awaited in the next iteration.  Items found invalid below
+      // get the product too; the consumer ignores it and zero-fills.
+      if (p == kGroup - 1) {
+        if (mbar_wait_suspend(&sh.tma_bar, j & 1, abort)) {
+          tc_fence_after_sync();
+          const uint32_t tb = tmem + slot * 256;
+          const uint32_t sA = smem_addr(smem + kOffA);
+          const uint32_t sHi = smem_addr(smem + kOffS0hi);
+          const uint32_t sLo = smem_addr(smem + kOffS0lo);
+          constexpr uint32_t id_s0 = idesc_bf16_f32(128, 128, 0, 1);
+          constexpr uint32_t id_gram = idesc_bf16_f32(128, kTcNodes, 0, 0);
+#pragma unroll
+          for (int s = 0; s < kTcDK / 16; ++s) {
+            const uint64_t ad = smem_desc(sA + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024,
+                                          kSwizzle128B);
+            // MN-major S0: value-column atoms 16 KiB apart (leading byte offset),
+            // 8-row k groups 1 KiB apart (stride byte offset)
+            const uint64_t hd = smem_desc(sHi + s * 2048, 16384, 1024, kSwizzle128B);
+            const uint64_t ld = smem_desc(sLo + s * 2048, 16384, 1024, kSwizzle128B);
+            umma_bf16(tb, ad, hd, id_s0, s > 0);
+            umma_bf16(tb, ad, ld, id_s0, 1);
+            umma_bf16(tb + kGramCol, ad, ad, id_gram, s > 0);  // B = the key rows of A
+          }
+          umma_commit(&sh.mma1_bar);
+          umma_commit(&sh.s1_done[slot]);
+          sh.mma1_issued += 1;
+        } else {
+          mbar_arrive(&sh.s1_done[slot]);  // no product: the consumer zero-fills
+        }
+      }
       // prefetch the next item while this one is finished
       if (next < i_end) {  // the small loads first: they are not queued behind S0
         load_meta(next);
@@ -560,43 +719,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         M.G[p] = acc;
       }
       ok = named_sync_and(kBarP, kGroup, ok);
-      if (p == 0) M.good = ok;
       prev_bi = ok ? bi : -1;
-      // first product into TMEM half `slot` (one thread); its completion is
-      // awaited in the next iteration
       if (p == 0) {
-        const bool tma_ok = mbar_wait_suspend(&sh.tma_bar, j & 1, abort);
-        if (tma_ok && ok) {
-          tc_fence_after_sync();
-          const uint32_t tb = tmem + slot * 256;
-          const uint32_t sA = smem_addr(smem + kOffA);
-          const uint32_t sHi = smem_addr(smem + kOffS0hi);
-          const uint32_t sLo = smem_addr(smem + kOffS0lo);
-          constexpr uint32_t id_s0 = idesc_bf16_f32(128, 128, 0, 1);
-          constexpr uint32_t id_gram = idesc_bf16_f32(128, kTcNodes, 0, 0);
-#pragma unroll
-          for (int s = 0; s < kTcDK / 16; ++s) {
-            const uint64_t ad = smem_desc(sA + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024,
-                                          kSwizzle128B);
-            // MN-major S0: value-column atoms 16 KiB apart (leading byte offset),
-            // 8-row k groups 1 KiB apart (stride byte offset)
-            const uint64_t hd = smem_desc(sHi + s * 2048, 16384, 1024, kSwizzle128B);
-            const uint64_t ld = smem_desc(sLo + s * 2048, 16384, 1024, kSwizzle128B);
-            umma_bf16(tb, ad, hd, id_s0, s > 0);
-            umma_bf16(tb, ad, ld, id_s0, 1);
-            umma_bf16(tb + kGramCol, ad, ad, id_gram, s > 0);  // B = the key rows of A
-          }
-          umma_commit(&sh.mma1_bar);
-          umma_commit(&sh.s1_done[slot]);
-          mma1_pending = true;
-        } else {
-          mbar_arrive(&sh.s1_done[slot]);  // no product: the consumer zero-fills
-        }
+        M.good = ok;
         mbar_arrive(&sh.s1_done[slot]);  // the metadata above is written
       }
     }
-    // the last first product, before TMEM and the operands are released (bounded)
-    if (p == 0 && mma1_pending) (void)mbar_wait_suspend(&sh.mma1_bar, mma1_seen & 1, abort);
   } else {
     // =================================================== consumer warps 8-15
     const int c = tid - kGroup;
@@ -706,18 +834,30 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         }
       }
 
-      // ---- one row of T (sc < 64) or W (64 <= sc < 128) per query-lane thread
-      // (solve_path_row).  Rows are handed out in topological order so that a
-      // warp sees similar depths.
+      // ---- the rows of T and W on the query-lane warps (solve_path_pair for
+      // trees of depth <= 16, else solve_path_row).  Rows are handed out in
+      // topological order so that a warp sees similar depths.
       if (!key_lane) {
-        const int sc = (lq - 2) * 64 + chalf * 32 + (c & 31);  // solver index 0..127
-        const int spos = sc & 63;
-        const bool act = spos < N;
-        const int sn = act ? M.ord[spos] : 0;
-        const int dn = act ? M.dep[sn] : -1;
-        const int wmax = __reduce_max_sync(0xffffffffu, dn);
-        solve_path_row<kSolveD>(M, reinterpret_cast<const float*>(smem + kOffGR), smem, sn, dn,
-                                wmax, sc < 64);
+        const float* GR = reinterpret_cast<const float*>(smem + kOffGR);
+        if constexpr (kSolveD <= 16) {
+          // warps 10 and 11 (one per scheduler): a node's T and W rows per thread
+          if (chalf == 0) {
+            const int spos = (lq - 2) * 32 + (c & 31);
+            const bool act = spos < N;
+            const int sn = act ? M.ord[spos] : 0;
+            const int dn = act ? M.dep[sn] : -1;
+            const int wmax = __reduce_max_sync(0xffffffffu, dn);
+            solve_path_pair<kSolveD>(M, GR, smem, sn, dn, wmax);
+          }
+        } else {
+          const int sc = (lq - 2) * 64 + chalf * 32 + (c & 31);  // solver index 0..127
+          const int spos = sc & 63;
+          const bool act = spos < N;
+          const int sn = act ? M.ord[spos] : 0;
+          const int dn = act ? M.dep[sn] : -1;
+          const int wmax = __reduce_max_sync(0xffffffffu, dn);
+          solve_path_row<kSolveD>(M, GR, smem, sn, dn, wmax, sc < 64);
+        }
       }
       fence_proxy_async_smem();
       tc_fence_before_sync();
@@ -822,6 +962,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     if (sh.tma_issued > 0) (void)mbar_wait(&sh.tma_bar, (sh.tma_issued - 1) & 1);
     if (sh.v_issued > 0) (void)mbar_wait(&sh.v_bar, (sh.v_issued - 1) & 1);
   }
+  // the last first product, before TMEM and the operands are released (bounded)
+  if (tid == 0 && sh.mma1_issued > 0) (void)mbar_wait(&sh.mma1_bar, (sh.mma1_issued - 1) & 1);
   __syncthreads();
   if (warp == 0) {
     tc_fence_after_sync();

@@ -47,6 +47,7 @@ constexpr int kO8GK = 131072;     // K K^T along each node's path [128][kT8Path]
 constexpr int kO8GQ = 131072 + 16384;        // Q K^T along each node's path
 constexpr int kO8Meta = 131072 + 32768;
 
+
 struct T8Meta {
   uint64_t tma_bar, mma_bar;
   uint32_t tmem_slot;
@@ -129,45 +130,63 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
   float* GK = reinterpret_cast<float*>(smem + kO8GK);
   float* GQ = reinterpret_cast<float*>(smem + kO8GQ);
 
-  // One item ahead: the sequence's bounds, status and root depth in registers,
-  // and the item's state, V rows and tree metadata pulled into L2 while the
-  // current item is being finished (16-byte aligned ranges inside the arrays).
+  // The sequence bounds and status two items ahead and the root depth one item
+  // ahead in registers (raw values: nothing waits for them before they are
+  // used), and the next item's state, V rows and tree metadata pulled into L2
+  // while the current item is being worked on (16-byte aligned ranges).
   const int sq = tid & 31, r0 = tid >> 5;
-  int nx_lo = 0, nx_hi = 0, nx_st = 0, nx_d0 = 0;
+  int nx_lo = 0, nx_hi = 0, nx_st = 0, nx_d0 = 0;  // the next item
+  int nb_lo = 0, nb_hi = 0, nb_st = 0;             // the item after it
   float4 sr[8];
-#define T8_PREFETCH(it)                                                          \
-  if ((it) < n_items) {                                                          \
-    const int b2 = (it) / H_v;                                                   \
-    nx_lo = cu[b2];                                                              \
-    nx_hi = cu[b2 + 1];                                                          \
-    nx_st = status[b2];                                                          \
-    nx_d0 = nx_hi > nx_lo ? depth[nx_lo] : 0;                                    \
-    if (tid == 0) prefetch_l2(S0 + (size_t)(it) * kT8D * kT8D, kT8D * kT8D * 4); \
-    if (tid < nx_hi - nx_lo && tid <= kT8Nodes)                                  \
-      prefetch_l2(v + ((size_t)(nx_lo + tid) * H_v + (it) % H_v) * kT8D, kT8D * 2); \
-    if (tid >= 32 && tid < 35) {                                                 \
-      const int32_t* arr = tid == 32 ? depth : tid == 33 ? pos : order;          \
-      const uintptr_t a0 = reinterpret_cast<uintptr_t>(arr + nx_lo) & ~(uintptr_t)15; \
-      const uintptr_t a1 = reinterpret_cast<uintptr_t>(arr + nx_hi) & ~(uintptr_t)15; \
-      if (a1 > a0) prefetch_l2(reinterpret_cast<const void*>(a0), (uint32_t)(a1 - a0)); \
-    }                                                                            \
-  }
+  auto load_bounds = [&](int it) {
+    if (it < n_items) {
+      const int b2 = it / H_v;
+      nb_lo = cu[b2];
+      nb_hi = cu[b2 + 1];
+      nb_st = status[b2];
+    }
+  };
+  auto advance = [&](int it) {  // it: the next item; its bounds are in nb_*
+    nx_lo = nb_lo;
+    nx_hi = nb_hi;
+    nx_st = nb_st;
+    nx_d0 = 0;
+    if (it < n_items && nx_hi > nx_lo) {
+      nx_d0 = depth[nx_lo];
+      if (tid == 0) prefetch_l2(S0 + (size_t)it * kT8D * kT8D, kT8D * kT8D * 4);
+      if (tid < nx_hi - nx_lo && tid <= kT8Nodes)
+        prefetch_l2(v + ((size_t)(nx_lo + tid) * H_v + it % H_v) * kT8D, kT8D * 2);
+      if (tid >= 32 && tid < 35) {
+        const int32_t* arr = tid == 32 ? depth : tid == 33 ? pos : order;
+        const uintptr_t a0 = reinterpret_cast<uintptr_t>(arr + nx_lo) & ~(uintptr_t)15;
+        const uintptr_t a1 = reinterpret_cast<uintptr_t>(arr + nx_hi) & ~(uintptr_t)15;
+        if (a1 > a0) prefetch_l2(reinterpret_cast<const void*>(a0), (uint32_t)(a1 - a0));
+      }
+      if (tid == 35) {  // the ancestor masks (16-byte aligned range inside the array)
+        const uintptr_t a0 =
+            reinterpret_cast<uintptr_t>(anc + (size_t)nx_lo * words) & ~(uintptr_t)15;
+        const uintptr_t a1 =
+            reinterpret_cast<uintptr_t>(anc + (size_t)nx_hi * words) & ~(uintptr_t)15;
+        if (a1 > a0) prefetch_l2(reinterpret_cast<const void*>(a0), (uint32_t)(a1 - a0));
+      }
+    }
+  };
+#define T8_PREFETCH(it)              \
+  advance(it);                       \
+  load_bounds((it) + (int)gridDim.x);
+  load_bounds((int)blockIdx.x);
   T8_PREFETCH((int)blockIdx.x)
 
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const int bi = item / H_v, h = item % H_v, qh = h / grp;
+    const int h = item % H_v, qh = h / grp;
     const int lo = nx_lo, N = nx_hi - nx_lo;
     const bool st_ok = nx_st == TGDN_SEQ_OK;
     const int d0 = nx_d0;
-    if (N <= 0) {  // uniform over the CTA
-      T8_PREFETCH(item + (int)gridDim.x)
-      continue;
-    }
+    // the next item's bounds and L2 prefetches go out now and land during this item
+    T8_PREFETCH(item + (int)gridDim.x)
+    if (N <= 0) continue;  // uniform over the CTA
     const int fold = (st_ok && N == kT8Nodes + 1 && d0 == 0) ? 1 : 0;
-    if (st_ok && N == kT8Nodes + 1 && !fold) {  // root elsewhere: the SIMT kernel's
-      T8_PREFETCH(item + (int)gridDim.x)
-      continue;
-    }
+    if (st_ok && N == kT8Nodes + 1 && !fold) continue;  // root elsewhere: the SIMT kernel's
     const int Nf = N - fold;                             // nodes on the tensor cores
     const size_t obase0 = (size_t)lo * H_v + h;          // row of node 0
     const size_t obase = obase0 + (size_t)fold * H_v;    // row of the first tensor-core node
@@ -188,9 +207,19 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
         }
       M.tma_n += 1;
     }
+    // the item's state rows and this thread's V slice, ahead of their use
+    load_state_rows(sr, S0 + (size_t)item * kT8D * kT8D, r0, sq);
+    uint4 vreg[4];  // this thread's V row slice (32 columns), for R after the product
+    if (ok && my_row < Nf) {
+      const uint4* vp =
+          reinterpret_cast<const uint4*>(v + (obase + (size_t)my_row * H_v) * kT8D + cg * 32);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) vreg[i] = __ldg(vp + i);
+    }
     // ---- metadata, root paths and path-cumulative gates (one thread per node)
     // (with a folded root, node nd = tid + 1 is tensor-core node tid; depths and
     // topological positions drop by one: the root is position 0)
+    uint64_t mk3[3] = {0ull, 0ull, 0ull};  // this node's ancestor mask words
     if (ok && tid < Nf) {
       const int nd = tid + fold;
       const int dn = depth[lo + nd] - fold, pn = pos[lo + nd] - fold;
@@ -201,6 +230,12 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
       M.ord[tid] = v_ok ? od : 0;
       M.gg[tid] = g[(size_t)(lo + nd) * H_v + h];
       M.bb[tid] = bta[(size_t)(lo + nd) * H_v + h];
+      if (v_ok) {  // the mask is read before the barrier, used after it
+        const uint64_t* am = anc + (size_t)(lo + pn + fold) * words;
+#pragma unroll
+        for (int w = 0; w < 3; ++w)
+          if (w < words) mk3[w] = am[w];
+      }
       if (!v_ok) ok = false;
     }
     ok = __syncthreads_and(ok) != 0;
@@ -210,8 +245,10 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
       int i = 0;
       float acc = 0.f;
       bool pk = true;
-      for (int w = 0; w < words && w < 3 && pk; ++w) {
-        uint64_t mk = anc[(size_t)(lo + pos[lo + tid + fold]) * words + w];
+#pragma unroll
+      for (int w = 0; w < 3; ++w) {
+        if (w >= words || !pk) break;
+        uint64_t mk = mk3[w];
         while (mk && pk) {
           const int b = w * 64 + __ffsll(static_cast<long long>(mk)) - 1 - fold;
           mk &= mk - 1;
@@ -232,7 +269,6 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
     }
     // ---- S0 -> bf16 hi + lo operand (thread: rows (tid >> 5) + 16 r, float4 column tid & 31)
     {
-      load_state_rows(sr, S0 + (size_t)item * kT8D * kT8D, r0, sq);
       if (fold) {  // the root's own step: S_r = a_r S0 + k_r u_r^T, o_r = S_r^T q_r
         float* part = reinterpret_cast<float*>(smem + kO8GK);  // [16][128] partial sums
         float* kr = part + 16 * kT8D;
@@ -301,13 +337,6 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
       }
     }
     fence_proxy_async_smem();
-    uint4 vreg[4];  // this thread's V row slice (32 columns), for R after the product
-    if (ok && my_row < Nf) {
-      const uint4* vp =
-          reinterpret_cast<const uint4*>(v + (obase + (size_t)my_row * H_v) * kT8D + cg * 32);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) vreg[i] = __ldg(vp + i);
-    }
     ok = __syncthreads_and(ok) != 0;
     if (!ok) {  // bad sequence: zero rows, and let an issued copy land before reuse
       if (tid == 0 && tma_issued) (void)mbar_wait_suspend(&M.tma_bar, (M.tma_n - 1) & 1, abort);
@@ -319,7 +348,6 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
       }
       for (int n = tid; n < N; n += kT8Threads) Gws[obase0 + (size_t)n * H_v] = 0.f;
       if (__syncthreads_or(*abort)) break;
-      T8_PREFETCH(item + (int)gridDim.x)
       continue;
     }
 
@@ -331,22 +359,20 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
         tc_fence_after_sync();
         const uint32_t sK = smem_addr(smem + kO8AK), sQ = smem_addr(smem + kO8AQ);
         const uint32_t sHi = smem_addr(smem + kO8S0hi), sLo = smem_addr(smem + kO8S0lo);
-        constexpr uint32_t id_s0 = idesc_bf16_f32(128, 64, 0, 1);
+        constexpr uint32_t id_s0 = idesc_bf16_f32(128, 128, 0, 1);
         constexpr uint32_t id_g = idesc_bf16_f32(128, 128, 0, 0);
 #pragma unroll
         for (int s = 0; s < kT8D / 16; ++s) {
           const uint32_t ko = (s >> 2) * 16384 + (s & 3) * 32;
           const uint64_t ak = smem_desc(sK + ko, 16, 1024, kSwizzle128B);
           const uint64_t aq = smem_desc(sQ + ko, 16, 1024, kSwizzle128B);
-#pragma unroll
-          for (int at = 0; at < 2; ++at) {
-            const uint64_t hd = smem_desc(sHi + at * 16384 + s * 2048, 1024, 1024, kSwizzle128B);
-            const uint64_t ld = smem_desc(sLo + at * 16384 + s * 2048, 1024, 1024, kSwizzle128B);
-            umma_bf16(tmem + at * 64, ak, hd, id_s0, s > 0);
-            umma_bf16(tmem + at * 64, ak, ld, id_s0, 1);
-            umma_bf16(tmem + 128 + at * 64, aq, hd, id_s0, s > 0);
-            umma_bf16(tmem + 128 + at * 64, aq, ld, id_s0, 1);
-          }
+          // MN-major S0: value-column atoms 16 KiB apart, 8-row k groups 1 KiB apart
+          const uint64_t hd = smem_desc(sHi + s * 2048, 16384, 1024, kSwizzle128B);
+          const uint64_t ld = smem_desc(sLo + s * 2048, 16384, 1024, kSwizzle128B);
+          umma_bf16(tmem, ak, hd, id_s0, s > 0);
+          umma_bf16(tmem, ak, ld, id_s0, 1);
+          umma_bf16(tmem + 128, aq, hd, id_s0, s > 0);
+          umma_bf16(tmem + 128, aq, ld, id_s0, 1);
           umma_bf16(tmem + 256, ak, ak, id_g, s > 0);  // B = the key rows
           umma_bf16(tmem + 384, aq, ak, id_g, s > 0);
         }
@@ -495,7 +521,6 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
     tc_fence_before_sync();
     __syncthreads();  // TMEM and shared memory are reused by the next item
     tc_fence_after_sync();
-    T8_PREFETCH(item + (int)gridDim.x)  // lands while the next item's metadata is read
   }
 
   // ---- end.  After an expired wait every item still owned by this CTA is
