@@ -597,7 +597,8 @@ def run_recurrent_compare(args):
         t1 = _launch_times(torch, stream, f_single, 20, flush)
         t2 = _launch_times(torch, stream, f_rec, 20, flush)
         kern = ("verify_tc_kernel" if trees.n_max <= 64 else
-                "verify_tc128_kernel" if trees.n_max <= 129 else "verify_simt_kernel")
+                "verify_tc_kernel (<= 64-node sequences) + verify_tc128_kernel" if trees.n_max <= 129
+                else "verify_simt_kernel")
         out.append({"tree": kind, "nodes": int(trees.n_max), "depth_max": dcap, "B": B,
                     "single_pass_us": t1, "single_pass_kernel": kern, "recurrent_us": t2,
                     "ratio": t2 / t1})
@@ -736,7 +737,8 @@ def run_config_times(args):
                       acc["accept_node"])
         t_or = time.perf_counter() - t0
         kern = ("verify_tc_kernel" if t.n_max <= 64 else
-                "verify_tc128_kernel" if t.n_max <= 129 else "verify_simt_kernel")
+                "verify_tc_kernel (<= 64-node sequences) + verify_tc128_kernel" if t.n_max <= 129
+                else "verify_simt_kernel")
         out.append({"workload": name, "B": t.B, "nodes": t.T, "verify_kernel": kern,
                     "verify_us": tv, "verify_frac_hbm": vb / (tv * 1e-6) / 1e9 / hbm,
                     "commit_us": tcm, "commit_frac_hbm": cb / (tcm * 1e-6) / 1e9 / hbm,

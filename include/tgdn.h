@@ -151,9 +151,9 @@ size_t tgdn_verify_workspace_bytes(const tgdn_tree* tree, const tgdn_dims* dims)
  *   ws    tgdn_verify_workspace_bytes() bytes, 256-byte aligned, written
  * tgdn_tree_prep must have run on `tree` (same stream or ordered before).
  * A sequence with a bad status gets zero outputs and zero workspace rows.
- * bf16 io with d_k = d_v = 128 and depth_max <= 30 runs a tensor-core kernel
- * (two items per SM in flight when n_max <= 64, one when n_max <= 128); every
- * other valid case runs the fp32 SIMT kernel.
+ * bf16 io with d_k = d_v = 128 and depth_max <= 30 runs on tensor-core kernels
+ * (sequences of at most 64 nodes: two items per SM in flight; 65-129 nodes: one
+ * item at a time); every other valid case runs the fp32 SIMT kernel.
  * Returns TGDN_OK, TGDN_EINVAL, TGDN_ETOOBIG or TGDN_ECUDA. */
 int tgdn_verify(const tgdn_tree* tree, const tgdn_dims* dims, const void* q, const void* k,
                 const void* v, const float* g, const float* b, const float* S0, void* o,

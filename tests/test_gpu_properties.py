@@ -138,10 +138,13 @@ def _relabel(par, new_root):
                     np.int32)
 
 
-@pytest.mark.parametrize("case", ["random", "deep", "chain60", "star128", "ragged", "fold129"])
+@pytest.mark.parametrize("case", ["random", "deep", "chain60", "star128", "ragged", "fold129",
+                                  "mixed16", "mixed30"])
 def test_trees_of_65_to_128_nodes(case):
     """The 128-node tensor-core kernel: full, deep, chain and star trees, and a ragged batch
-    with empty and invalid sequences."""
+    with empty and invalid sequences.  In a launch above 64 nodes the sequences of at most
+    64 nodes go to the 64-node kernel (mixed16: its paired path solve, depth <= 16;
+    mixed30: its one-row solve, depth up to 30)."""
     rng = np.random.default_rng(41)
     if case == "random":
         parents = [synth.random_recursive_tree(rng, int(n), 16) for n in (65, 90, 128, 100)]
@@ -155,14 +158,25 @@ def test_trees_of_65_to_128_nodes(case):
         parents = [synth.random_recursive_tree(rng, 120, 12), np.zeros(0, np.int32),
                    np.array([-1, 0, 3, 2], np.int32), synth.chain_tree(5),
                    synth.random_recursive_tree(rng, 128, 20)]
+    elif case == "mixed16":
+        parents = [synth.chain_tree(17), synth.random_recursive_tree(rng, 100, 16),
+                   np.array([-1], np.int32), synth.random_recursive_tree(rng, 64, 16),
+                   synth.top_m_tree(rng, 8, 16), synth.random_recursive_tree(rng, 33, 5),
+                   synth.random_recursive_tree(rng, 65, 16), np.array([-1, 0, 3, 2], np.int32)]
+    elif case == "mixed30":
+        parents = [synth.chain_tree(25), synth.random_recursive_tree(rng, 128, 30),
+                   synth.random_recursive_tree(rng, 50, 30), synth.chain_tree(31)]
     else:   # 129 nodes: root first (folded into the state) and root in the middle (SIMT)
         t129 = synth.top_m_tree(rng, 8, 16)
         parents = [t129, _relabel(t129, 64), synth.random_recursive_tree(rng, 129, 14),
                    synth.chain_tree(17), np.array([-1, 0, 3, 2], np.int32)]
-    p = custom(parents, 2, 4, 128, "bf16", 12, n_max=129 if case == "fold129" else 128)
+    n_max = 129 if case in ("fold129", "mixed16") else 128
+    p = custom(parents, 2, 4, 128, "bf16", 12, n_max=n_max)
     got, ref = run_and_check(p, TOL_BF16)
     if case == "ragged":
         assert got["status"].tolist() == [0, 0, 4, 0, 0]
+    if case == "mixed16":
+        assert got["status"].tolist() == [0, 0, 0, 0, 0, 0, 0, 4]
 
 
 @pytest.mark.parametrize("io", ["bf16", "f32"])

@@ -128,13 +128,21 @@ int tgdn_verify(const tgdn_tree* tree, const tgdn_dims* dims, const void* q, con
       return TGDN_ECUDA;  // the driver could not describe q/k/v for TMA
     const tgdn::PendingCommit none{};
     return from_cuda(tgdn::launch_verify_tc(t, d, qmap, kmap, vmap, g, b, const_cast<float*>(S0),
-                                            o, U, G, none, s));
+                                            o, U, G, none, false, s));
   }
   if (tgdn::verify_tc128_supported(t, d, q, k, v, S0, o)) {
-    CUtensorMap qmap, kmap;
-    if (!encode_qk_map(&qmap, q, t.T, d.H_qk) || !encode_qk_map(&kmap, k, t.T, d.H_qk))
+    CUtensorMap qmap, kmap, vmap;
+    if (!encode_qk_map(&qmap, q, t.T, d.H_qk) || !encode_qk_map(&kmap, k, t.T, d.H_qk) ||
+        !encode_rows_map(&vmap, v, t.T, d.H_v, 1, 64))
       return TGDN_ECUDA;
-    rc = from_cuda(tgdn::launch_verify_tc128(t, d, qmap, kmap, q, k, v, g, b, S0, o, U, G, s));
+    // sequences of at most 64 nodes on the 64-node kernel (two items in flight per SM),
+    // the larger ones on the 128-node kernel; each kernel passes over the other's
+    const tgdn::PendingCommit none{};
+    rc = from_cuda(tgdn::launch_verify_tc(t, d, qmap, kmap, vmap, g, b, const_cast<float*>(S0),
+                                          o, U, G, none, true, s));
+    if (rc != TGDN_OK) return rc;
+    rc = from_cuda(
+        tgdn::launch_verify_tc128(t, d, qmap, kmap, q, k, v, g, b, S0, o, U, G, true, s));
     if (rc != TGDN_OK || t.n_max < tgdn::kTc128FoldNodes) return rc;
     // 129-node trees whose root is not node 0 (the rest of the batch is done)
     return from_cuda(tgdn::launch_verify_simt(t, d, q, k, v, g, b, S0, o, U, G, s,
@@ -189,7 +197,7 @@ int tgdn_verify_fused(const tgdn_tree* tree, const tgdn_dims* dims, const void* 
     float* G = reinterpret_cast<float*>(static_cast<char*>(ws) + L.g_off);
     const tgdn::PendingCommit cm{pt.cu_nodes, pt.status, prev_path, pt.depth_max + 1,
                                  prev_k,      pU,        pG};
-    return from_cuda(tgdn::launch_verify_tc(t, d, qmap, kmap, vmap, g, b, S, o, U, G, cm, s));
+    return from_cuda(tgdn::launch_verify_tc(t, d, qmap, kmap, vmap, g, b, S, o, U, G, cm, false, s));
   }
   // any other case: the commit as its own pass, then the verify
   if (pt.T > 0) {

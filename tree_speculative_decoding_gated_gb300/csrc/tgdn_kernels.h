@@ -48,9 +48,10 @@ struct PendingCommit {
   const float* G;         // previous path-cumulative log-gates [T'][H_v]
 };
 
-// Tensor-core verify: bf16 io, d_k = d_v = 128, n_max <= 64, depth_max <= 30.
+// Tensor-core verify: bf16 io, d_k = d_v = 128, n_max <= 64, depth_max <= 30; with
+// small_only the node bound is per sequence (larger sequences are passed over).
 bool verify_tc_supported(const tgdn_tree& t, const tgdn_dims& d, const void* q, const void* k,
-                         const void* v, const float* S0, const void* o);
+                         const void* v, const float* S0, const void* o, bool small_only = false);
 // Tensor-core verify for larger trees: bf16 io, d_k = d_v = 128, n_max <= 129,
 // depth_max <= 30; one item per SM at a time, sparse second step on CUDA cores.
 // A 129-node tree is taken when its root is node 0 (the root is folded into the
@@ -58,19 +59,21 @@ bool verify_tc_supported(const tgdn_tree& t, const tgdn_dims& d, const void* q, 
 constexpr int kTc128FoldNodes = 129;
 bool verify_tc128_supported(const tgdn_tree& t, const tgdn_dims& d, const void* q,
                             const void* k, const void* v, const float* S0, const void* o);
+// big_only: sequences of at most 64 nodes are passed over (the 64-node kernel's).
 cudaError_t launch_verify_tc128(const tgdn_tree& t, const tgdn_dims& d, const CUtensorMap& qmap,
                                 const CUtensorMap& kmap, const void* q, const void* k,
                                 const void* v, const float* g,
                                 const float* b, const float* S0, void* o, float* U, float* G,
-                                cudaStream_t s);
+                                bool big_only, cudaStream_t s);
 // Whether the tensor-core verify can also apply a pending commit of `prev`.
 bool pending_commit_tc_supported(const tgdn_tree& prev, const void* prev_k);
 // With cm.path set, S is first updated in place by the pending commit and the
-// committed state is verified; otherwise S is only read.
+// committed state is verified; otherwise S is only read.  small_only (no pending
+// commit): only the sequences of at most 64 nodes are verified, the rest untouched.
 cudaError_t launch_verify_tc(const tgdn_tree& t, const tgdn_dims& d, const CUtensorMap& qmap,
                              const CUtensorMap& kmap, const CUtensorMap& vmap, const float* g,
                              const float* b, float* S, void* o, float* U, float* G,
-                             const PendingCommit& cm, cudaStream_t s);
+                             const PendingCommit& cm, bool small_only, cudaStream_t s);
 
 // Per-branch recurrent verification (every root-to-leaf path replayed from S0).
 cudaError_t launch_verify_recurrent(const tgdn_tree& t, const tgdn_dims& d, const void* q,

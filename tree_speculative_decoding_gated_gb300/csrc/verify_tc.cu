@@ -88,6 +88,7 @@ static_assert(kOffOst + 64 * kOstRow <= kOffUP, "O staging stays in the [T; W] a
 struct alignas(16) ItemMeta {
   uint8_t path[kTcNodes][kPathBytes];  // [node][depth]: the node's ancestor at that depth
   int lo, N, bi, h, good;
+  int skip;  // a sequence above 64 nodes in a mixed launch: nothing to do here
   int dep[kTcNodes];
   int ord[kTcNodes];
   int pos[kTcNodes];
@@ -355,7 +356,8 @@ template <int kSolveD>
 __global__ void __launch_bounds__(kTcThreads, 1)
 verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                  const __grid_constant__ CUtensorMap vmap,
-                 int n_items, int H_qk, int H_v, int depth_max, const int32_t* __restrict__ cu,
+                 int n_items, int H_qk, int H_v, int depth_max, int words, int small_only,
+                 const int32_t* __restrict__ cu,
                  const int32_t* __restrict__ depth, const int32_t* __restrict__ order,
                  const int32_t* __restrict__ pos, const uint64_t* __restrict__ anc,
                  int32_t* __restrict__ status,
@@ -380,6 +382,15 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
   const int i_step = runs ? 1 : (int)gridDim.x;
   const int grp = H_v / H_qk;  // v-heads per query/key head
   const bool fused = cm.path != nullptr;
+  if (small_only) {  // a CTA whose items all belong to the 128-node kernel leaves at once
+    int mine = 0;
+    if (warp == 0)
+      for (int it = i_begin + (tid & 31) * i_step; it < i_end; it += 32 * i_step) {
+        const int n = cu[it / H_v + 1] - cu[it / H_v];
+        mine |= (n > 0 && n <= kTcNodes) ? 1 : 0;
+      }
+    if (!__syncthreads_or(mine)) return;
+  }
 
   if (tid == 0) {
     mbar_init(&sh.tma_bar, 1);
@@ -499,7 +510,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     load_seq(item);
     load_meta(item);
     if (item + i_step < i_end) load_seq(item + i_step);
-    load_s0(item);
+    if (!(small_only && pf.N > kTcNodes)) load_s0(item);
     if (fused) {
       if (p < 32) {
         load_commit_meta(item);
@@ -511,6 +522,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     }
 
     int prev_bi = -1;  // sequence of the previous item when its tree was valid
+    int npr = 0;       // items processed so far (passed-over items excluded): one [K;Q]
+                       // copy and one first product each, in order
     for (int j = 0; item < i_end; ++j, item += i_step) {
       const int slot = j & 1;
       ItemMeta& M = sh.meta[slot];
@@ -522,12 +535,16 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       const int lo = pf.lo, N = pf.N;
       const int next = item + i_step;
       bool ok = (pf.st == TGDN_SEQ_OK) && N > 0 && N <= kTcNodes;
+      // (small_only: sequences above 64 nodes belong to the 128-node kernel; their
+      // items pass through without state, solve or writes)
+      const bool skip = small_only && N > kTcNodes;
       uint64_t my_anc = 0;
       if (p == 0) {
         M.lo = lo;
         M.N = N;
         M.bi = bi;
         M.h = h;
+        M.skip = skip;
       }
       if (ok && p < N) {
         const bool v_ok = pf.dep >= 0 && pf.dep <= depth_max && pf.dep <= kTcDepth &&
@@ -538,7 +555,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         M.ord[p] = pf.ord;
         M.gg[p] = pf.gg;
         M.bb[p] = pf.bb;
-        if (v_ok) my_anc = anc[lo + pf.pos];  // one 64-bit word: n_max <= 64
+        if (v_ok) my_anc = anc[(size_t)(lo + pf.pos) * words];  // positions < 64: word 0
       }
       if (fused) {
         // the previous step's commit: S = e^{G*} S + sum_l e^{G*-G_l} k_l u_l^T,
@@ -549,7 +566,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         // [K; Q] and S0 areas) are free; this item's key and query rows go out
         bool w_ok = true;
         if (p == 0) {
-          if (j > 0) w_ok = mbar_wait_suspend(&sh.mma1_bar, (j - 1) & 1, abort);
+          if (npr > 0) w_ok = mbar_wait_suspend(&sh.mma1_bar, (npr - 1) & 1, abort);
           if (w_ok) issue_kq(item, lo);
         }
         if (!named_sync_and(kBarP, kGroup, w_ok && !*abort)) break;
@@ -613,8 +630,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       }
       // Without a pending commit the same hand-over happens here.
       bool step_ok = true;
-      if (!fused && p == 0) {
-        if (j > 0) step_ok = mbar_wait_suspend(&sh.mma1_bar, (j - 1) & 1, abort);
+      if (!fused && p == 0 && !skip) {
+        if (npr > 0) step_ok = mbar_wait_suspend(&sh.mma1_bar, (npr - 1) & 1, abort);
         if (step_ok) issue_kq(item, lo);
       }
       // (also: every thread has finished reading this item's staged commit)
@@ -623,6 +640,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       // S0 registers -> bf16 hi/lo operand
 #pragma unroll
       for (int r = 0; r < 16; ++r) {
+        if (skip) break;  // (uniform)
         const int kr = srow0 + r;
         const float4 xv = sreg[r];
         const float h0 = __bfloat162float(__float2bfloat16_rn(xv.x));
@@ -641,8 +659,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       // node of its own) while the others prefetch and build the paths; its
       // completion is awaited in the next iteration.  Items found invalid below
       // get the product too; the consumer ignores it and zero-fills.
-      if (p == kGroup - 1) {
-        if (mbar_wait_suspend(&sh.tma_bar, j & 1, abort)) {
+      if (p == kGroup - 1 && skip) {
+        mbar_arrive(&sh.s1_done[slot]);  // a passed-over item: no copy, no product
+      } else if (p == kGroup - 1) {
+        if (mbar_wait_suspend(&sh.tma_bar, npr & 1, abort)) {
           tc_fence_after_sync();
           const uint32_t tb = tmem + slot * 256;
           const uint32_t sA = smem_addr(smem + kOffA);
@@ -676,7 +696,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
           load_seq(next + i_step);
           if (fused && p < 32) load_commit_meta(next + i_step);
         }
-        load_s0(next);
+        if (!(small_only && pf.N > kTcNodes)) load_s0(next);
       }
       ok = named_sync_and(kBarP, kGroup, ok);
       // root paths from the ancestor masks (bits = topological positions,
@@ -724,6 +744,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         M.good = ok;
         mbar_arrive(&sh.s1_done[slot]);  // the metadata above is written
       }
+      if (!skip) ++npr;
     }
   } else {
     // =================================================== consumer warps 8-15
@@ -737,8 +758,13 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     const int lane_node = key_lane ? lane_row : lane_row - 64;
     // Thread 0, one item ahead: the V rows of an item go by TMA into the R lo
     // operand area (the same swizzled layout), where R is then formed in place.
-    int cv_lo = 0;  // first node row of the item whose V rows go out next
-    auto load_vseq = [&](int item) { cv_lo = cu[item / H_v]; };
+    int cv_lo = 0, cv_hi = 0;  // node rows of the item whose V rows go out next
+    auto load_vseq = [&](int item) {
+      cv_lo = cu[item / H_v];
+      cv_hi = cu[item / H_v + 1];
+    };
+    // a passed-over item (small_only, above 64 nodes) gets no V rows
+    auto v_wanted = [&]() { return !(small_only && cv_hi - cv_lo > kTcNodes); };
     auto issue_v = [&](int item) {
       mbar_arrive_expect_tx(&sh.v_bar, 2 * 64 * 128);
       tma_load_3d(smem + kOffRlo, &vmap, &sh.v_bar, 0, item % H_v, cv_lo);
@@ -748,10 +774,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     int item = i_begin;
     if (c == 0) {
       load_vseq(item);
-      issue_v(item);
+      if (v_wanted()) issue_v(item);
       if (item + i_step < i_end) load_vseq(item + i_step);
     }
     uint32_t mma2_count = 0;  // second products issued so far (same in every thread)
+    int nv = 0;               // V copies consumed so far (one per item not passed over)
     for (int j = 0; item < i_end; ++j, item += i_step) {
       const int slot = j & 1;
       bulk_wait_read();  // the previous item's output rows have left shared memory
@@ -762,22 +789,24 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       const uint32_t tb = tmem + slot * 256;
       const int next = item + i_step;
 
-      if (!M.good) {  // bad or empty sequence: zero rows
-        for (int e = c; e < N * (kTcDV / 4); e += kGroup) {
+      if (!M.good) {  // bad or empty sequence: zero rows (none for a passed-on item)
+        const int nz = M.skip ? 0 : N;
+        for (int e = c; e < nz * (kTcDV / 4); e += kGroup) {
           const int n = e >> 5, c4 = e & 31;
           const size_t row = ((size_t)(lo + n) * H_v + h) * kTcDV + c4 * 4;
           *reinterpret_cast<uint2*>(o + row) = make_uint2(0u, 0u);
           *reinterpret_cast<float4*>(Uws + row) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        for (int n = c; n < N; n += kGroup) Gws[(size_t)(lo + n) * H_v + h] = 0.f;
+        for (int n = c; n < nz; n += kGroup) Gws[(size_t)(lo + n) * H_v + h] = 0.f;
         bool v_ok = true;
         if (c == 0) {  // this item's V rows have landed: the area is free for the next
-          v_ok = mbar_wait_suspend(&sh.v_bar, j & 1, abort);
+          if (!M.skip) v_ok = mbar_wait_suspend(&sh.v_bar, nv & 1, abort);
           if (v_ok && next < i_end) {
-            issue_v(next);
+            if (v_wanted()) issue_v(next);
             if (next + i_step < i_end) load_vseq(next + i_step);
           }
         }
+        if (!M.skip) ++nv;
         if (!named_sync_and(kBarC, kGroup, v_ok)) break;
         if (c == 0) mbar_arrive(&sh.tmem_free[slot]);
         continue;
@@ -805,7 +834,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       // ---- R = diag(b)(V - e^G K S0) as a bf16 hi/lo operand (key lanes)
       bool v_ok = true;
       if (key_lane) {
-        v_ok = mbar_wait_suspend(&sh.v_bar, j & 1, abort);
+        v_ok = mbar_wait_suspend(&sh.v_bar, nv & 1, abort);
         const bool live = lane_node < N;
         const float eG = live ? __expf(M.G[lane_node]) : 0.f;
         const float bn = live ? M.bb[lane_node] : 0.f;
@@ -890,8 +919,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       if (!done2) break;
       tc_fence_after_sync();
       // the operand areas are free: the next item's V rows go out now
+      ++nv;
       if (c == 0 && next < i_end) {
-        issue_v(next);
+        if (v_wanted()) issue_v(next);
         if (next + i_step < i_end) load_vseq(next + i_step);
       }
 
@@ -976,11 +1006,11 @@ bool pending_commit_tc_supported(const tgdn_tree& prev, const void* prev_k) {
 }
 
 bool verify_tc_supported(const tgdn_tree& t, const tgdn_dims& d, const void* q, const void* k,
-                         const void* v, const float* S0, const void* o) {
+                         const void* v, const float* S0, const void* o, bool small_only) {
   auto al = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; };
-  return d.io == TGDN_BF16 && d.d_k == kTcDK && d.d_v == kTcDV && t.n_max <= kTcNodes &&
-         t.depth_max <= kTcDepth && al(q, 16) && al(k, 16) && al(v, 16) && al(S0, 16) &&
-         al(o, 16);
+  return d.io == TGDN_BF16 && d.d_k == kTcDK && d.d_v == kTcDV &&
+         (small_only || t.n_max <= kTcNodes) && t.depth_max <= kTcDepth && al(q, 16) &&
+         al(k, 16) && al(v, 16) && al(S0, 16) && al(o, 16);
 }
 
 static int sm_count() {
@@ -999,7 +1029,7 @@ static int sm_count() {
 cudaError_t launch_verify_tc(const tgdn_tree& t, const tgdn_dims& d, const CUtensorMap& qmap,
                              const CUtensorMap& kmap, const CUtensorMap& vmap, const float* g,
                              const float* b, float* S, void* o, float* U, float* G,
-                             const PendingCommit& cm, cudaStream_t s) {
+                             const PendingCommit& cm, bool small_only, cudaStream_t s) {
   // the path solve keeps depth_max + 1 partial sums in registers
   auto kern = t.depth_max <= 16 ? verify_tc_kernel<16> : verify_tc_kernel<kTcDepth>;
   cudaError_t e =
@@ -1011,8 +1041,8 @@ cudaError_t launch_verify_tc(const tgdn_tree& t, const tgdn_dims& d, const CUten
   const int sms = sm_count();
   const int grid = (int)(items < sms ? items : sms);
   kern<<<grid, kTcThreads, kTcSmemBytes, s>>>(
-      qmap, kmap, vmap, (int)items, d.H_qk, d.H_v, t.depth_max, t.cu_nodes, t.depth, t.order,
-      t.pos, t.anc, t.status, g, b, S,
+      qmap, kmap, vmap, (int)items, d.H_qk, d.H_v, t.depth_max, t.words, small_only ? 1 : 0,
+      t.cu_nodes, t.depth, t.order, t.pos, t.anc, t.status, g, b, S,
       static_cast<__nv_bfloat16*>(o), U, G, cm);
   return cudaGetLastError();
 }

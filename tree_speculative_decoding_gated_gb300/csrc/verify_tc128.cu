@@ -94,7 +94,7 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
                     const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
                     const float* __restrict__ g, const float* __restrict__ bta,
                     const float* __restrict__ S0, __nv_bfloat16* __restrict__ o,
-                    float* __restrict__ Uws, float* __restrict__ Gws) {
+                    float* __restrict__ Uws, float* __restrict__ Gws, int big_only) {
   extern __shared__ uint8_t t8_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(t8_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -185,6 +185,7 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
     // the next item's bounds and L2 prefetches go out now and land during this item
     T8_PREFETCH(item + (int)gridDim.x)
     if (N <= 0) continue;  // uniform over the CTA
+    if (big_only && N <= 64) continue;  // the 64-node kernel's sequence
     const int fold = (st_ok && N == kT8Nodes + 1 && d0 == 0) ? 1 : 0;
     if (st_ok && N == kT8Nodes + 1 && !fold) continue;  // root elsewhere: the SIMT kernel's
     const int Nf = N - fold;                             // nodes on the tensor cores
@@ -566,7 +567,7 @@ cudaError_t launch_verify_tc128(const tgdn_tree& t, const tgdn_dims& d, const CU
                                 const CUtensorMap& kmap, const void* q, const void* k,
                                 const void* v, const float* g,
                                 const float* b, const float* S0, void* o, float* U, float* G,
-                                cudaStream_t s) {
+                                bool big_only, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(verify_tc128_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kT8SmemBytes);
   if (e != cudaSuccess) return e;
@@ -579,7 +580,7 @@ cudaError_t launch_verify_tc128(const tgdn_tree& t, const tgdn_dims& d, const CU
       qmap, kmap, (int)items, d.H_qk, d.H_v, t.depth_max, t.words, t.cu_nodes, t.depth, t.order,
       t.pos, t.anc, t.status, static_cast<const __nv_bfloat16*>(q),
       static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), g, b, S0,
-      static_cast<__nv_bfloat16*>(o), U, G);
+      static_cast<__nv_bfloat16*>(o), U, G, big_only ? 1 : 0);
   return cudaGetLastError();
 }
 
