@@ -636,6 +636,15 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       }
       // (also: every thread has finished reading this item's staged commit)
       if (!named_sync_and(kBarP, kGroup, step_ok && !*abort)) break;
+      // the next item's small loads go out before the operand stores, so that they
+      // wait neither behind those stores nor for their source registers
+      if (next < i_end) {
+        load_meta(next);
+        if (next + i_step < i_end) {
+          load_seq(next + i_step);
+          if (fused && p < 32) load_commit_meta(next + i_step);
+        }
+      }
       if (fused && next < i_end) stage_commit(next, slot ^ 1);
       // S0 registers -> bf16 hi/lo operand
 #pragma unroll
@@ -689,15 +698,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
           mbar_arrive(&sh.s1_done[slot]);  // no product: the consumer zero-fills
         }
       }
-      // prefetch the next item while this one is finished
-      if (next < i_end) {  // the small loads first: they are not queued behind S0
-        load_meta(next);
-        if (next + i_step < i_end) {
-          load_seq(next + i_step);
-          if (fused && p < 32) load_commit_meta(next + i_step);
-        }
-        if (!(small_only && pf.N > kTcNodes)) load_s0(next);
-      }
+      // the next item's state while this one is finished
+      if (next < i_end && !(small_only && pf.N > kTcNodes)) load_s0(next);
       ok = named_sync_and(kBarP, kGroup, ok);
       // root paths from the ancestor masks (bits = topological positions,
       // ascending = root first) and path-cumulative log-gates; the same tree as
