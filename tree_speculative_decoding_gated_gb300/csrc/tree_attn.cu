@@ -205,9 +205,12 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
     __syncthreads();
     tc_fence_after_sync();
   };
-  // every thread: wait for the latest products (bounded; the CTA agrees on the outcome)
+  // wait for the latest products: thread 0 waits on the mbarrier (suspended in
+  // hardware, bounded), the others park at the CTA barrier, which also carries
+  // the outcome to every thread
   auto wait_mma = [&]() -> bool {
-    const bool ok = mbar_wait_or_abort(mma_bar, mma_phase & 1, abort);
+    bool ok = true;
+    if (tid == 0) ok = mbar_wait_suspend(mma_bar, mma_phase & 1, abort);
     ++mma_phase;
     return __syncthreads_and(ok) != 0;
   };
@@ -494,6 +497,10 @@ cudaError_t launch_tree_attn(const tgdn_tree& t, int H_q, int H_kv, int P_max, f
   if ((long)a.n_items * a.splits > 0x7fffffffL) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(tree_attn_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kAtSmemBytes);
+  if (e != cudaSuccess) return e;
+  // the whole unified L1 / shared memory as shared memory: two CTAs per SM
+  e = cudaFuncSetAttribute(tree_attn_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   tree_attn_kernel<<<(unsigned)(items * a.splits), kAtThreads, kAtSmemBytes, s>>>(
       qmap, ktmap, vtmap, kcmap, vcmap, a);
