@@ -151,3 +151,26 @@ def test_deep_previous_tree_runs_two_passes():
 def test_trees_above_64_nodes_run_two_passes():
     ps = [head_pair_subset(synth.make_problem("cfg3", step=s), [3]) for s in (0, 1)]
     check_decode(ps, ps[0].S0, n_max=65)
+
+
+def test_stack_layer_full_size_sampled():
+    """One layer of the 36-layer stack at full size (32 sequences of 64-node trees, depth
+    <= 12, all 32 value heads), three decode steps with the commit fused in: the launch
+    configuration the benchmark times.  The oracle replays a sample of sequences on two
+    query/key heads."""
+    ps = [synth.make_problem("cfg5", step=s) for s in (0, 1, 2)]
+    fo, fv, fS = gpu_decode(ps, ps[0].S0, fused=True)
+    seqs = [0, 7, 19, 31]
+    subs = [head_pair_subset(synth.select_sequences(p, seqs), [0, 11]) for p in ps]
+    ref_o, ref_S = oracle_decode(subs, subs[0].S0)
+    vh = subs[0].meta["v_heads"]
+    for s, sub in enumerate(subs):
+        rows = sub.meta["rows"]
+        eo = rel_fro_blocks(fo[s][rows][:, vh], ref_o[s], sub.trees.cu_nodes)
+        print(f"stack layer step {s}: sampled o={eo:.3e}")
+        assert eo <= TOL_BF16, (s, eo)
+        if s > 0:
+            es = rel_fro_blocks(fv[s][seqs][:, vh], ref_S[s - 1])
+            print(f"stack layer step {s}: sampled committed state={es:.3e}")
+            assert es <= TOL_BF16, (s, es)
+    assert rel_fro_blocks(fS[seqs][:, vh], ref_S[-1]) <= TOL_BF16
