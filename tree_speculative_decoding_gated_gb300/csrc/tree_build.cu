@@ -61,6 +61,7 @@ tree_build_kernel(int B, int budget, int K, int w, int depth_max,
   float* nscore = reinterpret_cast<float*>(pool + (size_t)budget * K);    // [budget]
   int* ndepth = reinterpret_cast<int*>(nscore + budget);                  // [budget]
   int* nid = ndepth + budget;  // [budget] candidate id (parent slot * K + rank); -1: root
+  float* lps = reinterpret_cast<float*>(nid + budget);  // [budget * K] the drafter's log-probs
   const int b = blockIdx.x;
   const int lane = threadIdx.x;
   if (b >= B) return;
@@ -73,6 +74,8 @@ tree_build_kernel(int B, int budget, int K, int w, int depth_max,
     ndepth[0] = 0;
     nid[0] = -1;
   }
+  // the whole child table once (coalesced), so no round waits on global memory
+  for (int e = lane; e < budget * K; e += 32) lps[e] = lp[e];
   __syncwarp();
 
   int count = 0;           // pool positions used (same in every lane)
@@ -85,7 +88,7 @@ tree_build_kernel(int B, int budget, int K, int w, int depth_max,
       const int node = s0 + e / K, r = e % K;
       uint64_t key = 0;
       if (ndepth[node] + 1 <= depth_max)
-        key = cand_key(__fadd_rn(nscore[node], lp[(size_t)node * K + r]),
+        key = cand_key(__fadd_rn(nscore[node], lps[node * K + r]),
                        static_cast<uint32_t>(node * K + r));
       pool[count + e] = key;
     }
@@ -160,7 +163,8 @@ tree_build_kernel(int B, int budget, int K, int w, int depth_max,
 }
 
 size_t tree_build_smem_bytes(int budget, int K) {
-  return (size_t)budget * K * sizeof(uint64_t) + (size_t)budget * (sizeof(float) + 2 * sizeof(int));
+  return (size_t)budget * K * (sizeof(uint64_t) + sizeof(float)) +
+         (size_t)budget * (sizeof(float) + 2 * sizeof(int));
 }
 
 cudaError_t launch_tree_build(int B, int budget, int K, int w, int depth_max,
