@@ -139,7 +139,7 @@ def _relabel(par, new_root):
 
 
 @pytest.mark.parametrize("case", ["random", "deep", "chain60", "star128", "ragged", "fold129",
-                                  "mixed16", "mixed30"])
+                                  "mixed16", "mixed30", "allsmall"])
 def test_trees_of_65_to_128_nodes(case):
     """The 128-node tensor-core kernel: full, deep, chain and star trees, and a ragged batch
     with empty and invalid sequences.  In a launch above 64 nodes the sequences of at most
@@ -166,6 +166,8 @@ def test_trees_of_65_to_128_nodes(case):
     elif case == "mixed30":
         parents = [synth.chain_tree(25), synth.random_recursive_tree(rng, 128, 30),
                    synth.random_recursive_tree(rng, 50, 30), synth.chain_tree(31)]
+    elif case == "allsmall":   # a launch above 64 nodes whose sequences are all small
+        parents = [synth.random_recursive_tree(rng, int(n), 12) for n in (64, 10, 40, 1)]
     else:   # 129 nodes: root first (folded into the state) and root in the middle (SIMT)
         t129 = synth.top_m_tree(rng, 8, 16)
         parents = [t129, _relabel(t129, 64), synth.random_recursive_tree(rng, 129, 14),

@@ -87,7 +87,7 @@ static_assert(kOffOst + 64 * kOstRow <= kOffUP, "O staging stays in the [T; W] a
 
 struct alignas(16) ItemMeta {
   uint8_t path[kTcNodes][kPathBytes];  // [node][depth]: the node's ancestor at that depth
-  int lo, N, bi, h, good;
+  int lo, N, h, good;
   int skip;  // a sequence above 64 nodes in a mixed launch: nothing to do here
   int dep[kTcNodes];
   int ord[kTcNodes];
@@ -542,7 +542,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       if (p == 0) {
         M.lo = lo;
         M.N = N;
-        M.bi = bi;
         M.h = h;
         M.skip = skip;
       }
