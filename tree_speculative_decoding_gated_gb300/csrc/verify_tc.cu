@@ -382,15 +382,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
   const int i_step = runs ? 1 : (int)gridDim.x;
   const int grp = H_v / H_qk;  // v-heads per query/key head
   const bool fused = cm.path != nullptr;
-  if (small_only) {  // a CTA whose items all belong to the 128-node kernel leaves at once
-    int mine = 0;
-    if (warp == 0)
-      for (int it = i_begin + (tid & 31) * i_step; it < i_end; it += 32 * i_step) {
-        const int n = cu[it / H_v + 1] - cu[it / H_v];
-        mine |= (n > 0 && n <= kTcNodes) ? 1 : 0;
-      }
-    if (!__syncthreads_or(mine)) return;
-  }
+  // Launched with programmatic stream serialization: everything up to
+  // griddepcontrol.wait below touches no global memory (the first item's state
+  // is only pulled into L2, which stays coherent), so it can overlap the tail of
+  // the previous kernel in the stream.
+  if (tid == 0) prefetch_l2(S + (size_t)i_begin * kTcDK * kTcDV, kTcDK * kTcDV * 4);
 
   if (tid == 0) {
     mbar_init(&sh.tma_bar, 1);
@@ -413,6 +409,20 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = sh.tmem_slot;
+  grid_dependency_wait();     // the previous kernel's writes are visible from here on
+  grid_launch_dependents();   // the next kernel may start its own prologue
+  if (small_only) {  // a CTA whose items all belong to the 128-node kernel leaves at once
+    int mine = 0;
+    if (warp == 0)
+      for (int it = i_begin + (tid & 31) * i_step; it < i_end; it += 32 * i_step) {
+        const int n = cu[it / H_v + 1] - cu[it / H_v];
+        mine |= (n > 0 && n <= kTcNodes) ? 1 : 0;
+      }
+    if (!__syncthreads_or(mine)) {
+      if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+      return;
+    }
+  }
 
   if (tid < kGroup) {
     // =================================================== producer warps 0-7
@@ -1041,10 +1051,22 @@ cudaError_t launch_verify_tc(const tgdn_tree& t, const tgdn_dims& d, const CUten
   if (items > 0x7fffffffL) return cudaErrorInvalidConfiguration;
   const int sms = sm_count();
   const int grid = (int)(items < sms ? items : sms);
-  kern<<<grid, kTcThreads, kTcSmemBytes, s>>>(
-      qmap, kmap, vmap, (int)items, d.H_qk, d.H_v, t.depth_max, t.words, small_only ? 1 : 0,
-      t.cu_nodes, t.depth, t.order, t.pos, t.anc, t.status, g, b, S,
-      static_cast<__nv_bfloat16*>(o), U, G, cm);
+  // programmatic stream serialization: the kernel's prologue may overlap the
+  // previous kernel's tail (it waits for that kernel before reading any input)
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)grid);
+  lc.blockDim = dim3(kTcThreads);
+  lc.dynamicSmemBytes = kTcSmemBytes;
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  e = cudaLaunchKernelEx(&lc, kern, qmap, kmap, vmap, (int)items, d.H_qk, d.H_v, t.depth_max,
+                         t.words, small_only ? 1 : 0, t.cu_nodes, t.depth, t.order, t.pos,
+                         t.anc, t.status, g, b, S, static_cast<__nv_bfloat16*>(o), U, G, cm);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
