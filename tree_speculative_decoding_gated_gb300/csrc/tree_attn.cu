@@ -15,9 +15,12 @@
 // row maximum m as a bf16 operand and O += P V accumulates in TMEM; m is moved
 // (and O, the running sum rescaled in place) only when a tile's maximum exceeds
 // it by more than kRescaleGap, so P stays below e^kRescaleGap and rescaling is
-// rare.  O is divided by the sum at the end.  Key and value tiles are
-// double-buffered: the copy of the next tile is in flight while the current
-// one is scored.
+// rare.  O is divided by the sum at the end.  Pipeline: the score product of
+// tile u + 1 runs while the threads form P for tile u; P goes to TMEM over its
+// own score columns (two score buffers) and is the A operand of O += P V straight
+// from TMEM.  Key and value tiles are double-buffered with separate barriers: a
+// key buffer is refilled once its score product is done (two tiles ahead), a
+// value buffer once its P V product is done.
 //
 // With a workspace the cached context of each (sequence, head, row tile) is
 // split over several CTAs (the tree's own keys go to the last one); each writes
@@ -25,7 +28,7 @@
 // them (O = sum_s e^{m_s - M} O_s / sum_s e^{m_s - M} l_s).  That keeps every SM
 // busy when there are fewer (sequence, head, row tile) items than SMs.
 //   S tile = Q K^T: tcgen05.mma, A = Q (TMA, 128-byte swizzle), B = K tile
-//   O     += P V:   A = P (written by the threads), B = V tile (MN-major)
+//   O     += P V:   A = P (bf16 pairs in TMEM), B = V tile (MN-major)
 // Every wait is bounded; on expiry the sequence is marked TGDN_SEQ_TIMEOUT.
 #include "tgdn_device.cuh"
 #include "tgdn_kernels.h"
@@ -39,16 +42,14 @@ constexpr int kAtKeys = 64;              // keys per tile
 constexpr int kAtD = 128;
 constexpr int kPartStride = kAtD + 4;    // workspace row: O (128), m, l, 2 pad (528 B, 16-B aligned)
 constexpr int kAtMaxNodes = 128;         // tree nodes per sequence on this kernel
-constexpr uint32_t kAtTmemCols = 256;    // S tile: cols 0-63; O: cols 64-191
+constexpr uint32_t kAtTmemCols = 256;    // S / P buffers: cols 0-63, 192-255; O: cols 64-191
 constexpr int kAtOffQ = 0;               // [2 d halves][128 rows][128 B]     32 KiB
 constexpr int kAtOffK = 32768;           // 2 x [2 d halves][64 keys][128 B]  2 x 16 KiB
 constexpr int kAtOffV = 65536;           // 2 x [2 d atoms][64 keys][128 B]   2 x 16 KiB
-// P [128 rows][64 keys] bf16 (16 KiB) is written over the key tile of its own step,
-// which the score product has finished reading.
 constexpr int kAtOffMask = 98304;        // [kAtMaxNodes][2] uint64          2 KiB
 constexpr int kAtOffStat = kAtOffMask + kAtMaxNodes * 16;  // [2][128] row max, [2][128] sum
 constexpr int kAtOffBar = kAtOffStat + 4 * kAtRows * 4;
-constexpr int kAtSmemBytes = kAtOffBar + 64 + 1024;
+constexpr int kAtSmemBytes = kAtOffBar + 128 + 1024;
 
 __device__ __forceinline__ int at_swz(int row, int chunk) {
   return (row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4);
@@ -68,7 +69,7 @@ struct AtArgs {
   __nv_bfloat16* o;
 };
 
-__global__ void __launch_bounds__(kAtThreads)
+__global__ void __launch_bounds__(kAtThreads, 2)  // two CTAs per SM: <= 128 registers
 tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
                  const __grid_constant__ CUtensorMap ktmap,
                  const __grid_constant__ CUtensorMap vtmap,
@@ -78,9 +79,11 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(at_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* amask = reinterpret_cast<uint64_t*>(smem + kAtOffMask);
-  uint64_t* tma_bar = reinterpret_cast<uint64_t*>(smem + kAtOffBar);  // [2], one per buffer
-  uint64_t* mma_bar = tma_bar + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_bar + 1);
+  uint64_t* kbar = reinterpret_cast<uint64_t*>(smem + kAtOffBar);  // [2] key tile (+ Q)
+  uint64_t* vbar = kbar + 2;                                          // [2] value tile
+  uint64_t* sbar = vbar + 2;   // score products, one completion per tile
+  uint64_t* pvbar = sbar + 1;  // P V products, one completion per tile
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pvbar + 1);
   int* s_abort = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int item = blockIdx.x / a.splits, sp = blockIdx.x % a.splits;
@@ -107,9 +110,12 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   const int P = max(0, min(a.prefix_len[b], a.P_max));
 
   if (tid == 0) {
-    mbar_init(&tma_bar[0], 1);
-    mbar_init(&tma_bar[1], 1);
-    mbar_init(mma_bar, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kbar[i], 1);
+      mbar_init(&vbar[i], 1);
+    }
+    mbar_init(sbar, 1);
+    mbar_init(pvbar, 1);
     fence_mbar_init();
     *s_abort = 0;
   }
@@ -137,7 +143,8 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tO = tmem + 64;
+  const uint32_t tO = tmem + 64;
+  auto tS_of = [&](int u) -> uint32_t { return tmem + ((u & 1) ? 192u : 0u); };
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
   volatile int* abort = s_abort;
 
@@ -149,75 +156,66 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   const int n_ctx = t_end - t_begin;
   const int nt = n_ctx + (sp == a.splits - 1 ? nt_tree : 0);  // steps of this CTA
   auto tile_of = [&](int u) { return u < n_ctx ? t_begin + u : nt_pre + (u - n_ctx); };
-  uint32_t mma_phase = 0;
   const uint64_t m_lo = row_live ? amask[2 * my_node] : 0;
   const uint64_t m_hi = row_live ? amask[2 * my_node + 1] : 0;
 
-  // Steps u = 0 .. nt - 1: key and value tile u, buffer u & 1.
-  const int steps = nt;
-  int tma_issued[2] = {0, 0};  // copies issued per buffer (thread 0)
-  // thread 0: the key and value tiles of step u into buffer u & 1
-  auto issue_tile = [&](int u) {
-    const int t = tile_of(u), buf = u & 1;
-    const bool with_v = true;
+  // Steps u = 0 .. nt - 1: key and value tile u in buffer u & 1, scores and P in
+  // TMEM buffer u & 1.  Thread 0 issues every copy and product.
+  int k_issued[2] = {0, 0}, v_issued[2] = {0, 0};  // copies issued per buffer (thread 0)
+  uint32_t n_s = 0;                                 // score products issued (thread 0)
+  auto tile_row = [&](int u, const CUtensorMap*& km, const CUtensorMap*& vm) {
+    const int t = tile_of(u);
     const bool pre = t < nt_pre;
-    const int row = pre ? b * a.P_max + t * kAtKeys : lo + (t - nt_pre) * kAtKeys;
-    const CUtensorMap* km = pre ? &kcmap : &ktmap;
-    const CUtensorMap* vm = pre ? &vcmap : &vtmap;
-    uint64_t* bar = &tma_bar[buf];
-    const uint32_t bytes = 2 * kAtKeys * 128 * (with_v ? 2 : 1) + (u == 0 ? 32768 : 0);
-    mbar_arrive_expect_tx(bar, bytes);
+    km = pre ? &kcmap : &ktmap;
+    vm = pre ? &vcmap : &vtmap;
+    return pre ? b * a.P_max + t * kAtKeys : lo + (t - nt_pre) * kAtKeys;
+  };
+  auto issue_k = [&](int u) {  // key tile u (with Q for u = 0) into key buffer u & 1
+    const CUtensorMap *km, *vm;
+    const int r = tile_row(u, km, vm);
+    uint64_t* bar = &kbar[u & 1];
+    mbar_arrive_expect_tx(bar, 2 * kAtKeys * 128 + (u == 0 ? 32768 : 0));
     if (u == 0) {
       tma_load_3d(smem + kAtOffQ, &qmap, bar, 0, hk * a.G, lo + node0);
       tma_load_3d(smem + kAtOffQ + 16384, &qmap, bar, 64, hk * a.G, lo + node0);
     }
-    uint8_t* kdst = smem + kAtOffK + buf * 16384;
-    tma_load_3d(kdst, km, bar, 0, hk, row);
-    tma_load_3d(kdst + 8192, km, bar, 64, hk, row);
-    if (with_v) {
-      uint8_t* vdst = smem + kAtOffV + buf * 16384;
-      tma_load_3d(vdst, vm, bar, 0, hk, row);
-      tma_load_3d(vdst + 8192, vm, bar, 64, hk, row);
-    }
-    tma_issued[buf] += 1;
+    uint8_t* kdst = smem + kAtOffK + (u & 1) * 16384;
+    tma_load_3d(kdst, km, bar, 0, hk, r);
+    tma_load_3d(kdst + 8192, km, bar, 64, hk, r);
+    k_issued[u & 1] += 1;
   };
-  // thread 0, once every thread is done with the previous step: start the copy of
-  // step u + 1 (its buffer's last readers have completed), then S = Q K^T of step u.
-  // On an expired wait it raises *abort and commits nothing (wait_mma then gives up).
-  auto load_and_score = [&](int u) {
-    if (tid != 0) return;
-    if (u + 1 < steps) issue_tile(u + 1);
-    const int buf = u & 1;
-    if (!mbar_wait_suspend(&tma_bar[buf], (u >> 1) & 1, abort)) return;
+  auto issue_v = [&](int u) {  // value tile u into value buffer u & 1
+    const CUtensorMap *km, *vm;
+    const int r = tile_row(u, km, vm);
+    uint64_t* bar = &vbar[u & 1];
+    mbar_arrive_expect_tx(bar, 2 * kAtKeys * 128);
+    uint8_t* vdst = smem + kAtOffV + (u & 1) * 16384;
+    tma_load_3d(vdst, vm, bar, 0, hk, r);
+    tma_load_3d(vdst + 8192, vm, bar, 64, hk, r);
+    v_issued[u & 1] += 1;
+  };
+  // thread 0: S = Q K^T of tile u into score buffer u & 1 (its key tile has landed)
+  auto score = [&](int u) -> bool {
+    if (!mbar_wait_suspend(&kbar[u & 1], (u >> 1) & 1, abort)) return false;
     tc_fence_after_sync();
-    const uint32_t sQ = smem_addr(smem + kAtOffQ), sK = smem_addr(smem + kAtOffK + buf * 16384);
+    const uint32_t sQ = smem_addr(smem + kAtOffQ);
+    const uint32_t sK = smem_addr(smem + kAtOffK + (u & 1) * 16384);
     constexpr uint32_t id_s = idesc_bf16_f32(128, kAtKeys, 0, 0);
 #pragma unroll
     for (int s = 0; s < kAtD / 16; ++s) {
       const uint64_t ad = smem_desc(sQ + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024, kSwizzle128B);
       const uint64_t bd = smem_desc(sK + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024, kSwizzle128B);
-      umma_bf16(tS, ad, bd, id_s, s > 0);
+      umma_bf16(tS_of(u), ad, bd, id_s, s > 0);
     }
-    umma_commit(mma_bar);
+    umma_commit(sbar);
+    ++n_s;
+    return true;
   };
-  auto tile_sync = [&]() {
-    tc_fence_before_sync();
-    __syncthreads();
-    tc_fence_after_sync();
-  };
-  // wait for the latest products: thread 0 waits on the mbarrier (suspended in
-  // hardware, bounded), the others park at the CTA barrier, which also carries
-  // the outcome to every thread
-  auto wait_mma = [&]() -> bool {
-    bool ok = true;
-    if (tid == 0) ok = mbar_wait_suspend(mma_bar, mma_phase & 1, abort);
-    ++mma_phase;
-    return __syncthreads_and(ok) != 0;
-  };
-  // this thread's 32 logits of tile t (keys kh * 32 ..), scaled, masked to -inf
+  // this thread's 32 logits of tile u (keys kh * 32 ..), scaled, masked to -inf
   constexpr int kHalf = kAtKeys / 2;
-  auto read_logits = [&](int t, float (&x)[kHalf]) {
-    tmem_ld32(tS + lane_base + kh * kHalf, x);
+  auto read_logits = [&](int u, float (&x)[kHalf]) {
+    const int t = tile_of(u);
+    tmem_ld32(tS_of(u) + lane_base + kh * kHalf, x);
     tmem_ld_wait();
 #pragma unroll
     for (int c = 0; c < kHalf; ++c) x[c] *= a.scale;
@@ -236,23 +234,36 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   };
 
   bool ok = true;
-  if (tid == 0 && nt > 0) issue_tile(0);
+  if (tid == 0 && nt > 0) {
+    issue_k(0);
+    issue_v(0);
+    if (nt > 1) issue_k(1);
+    ok = score(0);
+  }
   float* st = reinterpret_cast<float*>(smem + kAtOffStat);
   float m = -INFINITY;  // running row maximum (same in both threads of a row)
   float lsum = 0.f;     // this thread's half of the row's sum of exp(logit - m)
-  for (int u = 0; u < nt && ok; ++u) {
-    tile_sync();
-    load_and_score(u);
-    ok = wait_mma();
+  uint32_t n_pv = 0;    // P V products issued (thread 0)
+  for (int u = 0; u < nt; ++u) {
+    // thread 0: S(u) and P V(u - 1) done (their buffers are free); value tile u + 1
+    // and key tile u + 2 go out; S(u + 1) starts and runs while P of tile u is formed
+    if (tid == 0 && ok) {
+      ok = mbar_wait_suspend(sbar, u & 1, abort);
+      if (ok && u > 0) ok = mbar_wait_suspend(pvbar, (u - 1) & 1, abort);
+      if (ok && u + 1 < nt) issue_v(u + 1);
+      if (ok && u + 2 < nt) issue_k(u + 2);
+      if (ok && u + 1 < nt) ok = score(u + 1);
+    }
+    ok = __syncthreads_and(ok) != 0;
     if (!ok) break;
     tc_fence_after_sync();
     float x[kHalf];
-    read_logits(tile_of(u), x);
+    read_logits(u, x);
     float lm = -INFINITY;
 #pragma unroll
     for (int c = 0; c < kHalf; ++c) lm = fmaxf(lm, x[c]);
     st[kh * kAtRows + row] = lm;
-    __syncthreads();
+    __syncthreads();  // (also: both halves of every row have read their scores)
     const float mt = fmaxf(st[row], st[kAtRows + row]);
     const bool need = mt > m + kRescaleGap;  // also the first finite maximum of the row
     const float alpha = need ? (m == -INFINITY ? 0.f : __expf(m - mt)) : 1.f;
@@ -270,43 +281,43 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
         for (int c = 0; c < 32; ++c) r[c] *= alpha;
         tmem_st32(tO + lane_base + q * 32, r);
       }
-      tmem_st_wait();
     }
+    // P = exp(logit - m) as bf16 pairs over this thread's 32 score columns' first
+    // 16 (key 2 c and 2 c + 1 in column c of the half)
+    uint32_t pw[kHalf / 2];
 #pragma unroll
-    for (int c8 = 0; c8 < kHalf / 8; ++c8) {
-      uint32_t w[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float p0 = m == -INFINITY ? 0.f : __expf(x[c8 * 8 + 2 * i] - m);
-        const float p1 = m == -INFINITY ? 0.f : __expf(x[c8 * 8 + 2 * i + 1] - m);
-        lsum += p0 + p1;
-        const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
-        w[i] = *reinterpret_cast<const uint32_t*>(&pp);
-      }
-      *reinterpret_cast<uint4*>(smem + kAtOffK + (u & 1) * 16384 + at_swz(row, kh * 4 + c8)) =
-          make_uint4(w[0], w[1], w[2], w[3]);
+    for (int i = 0; i < kHalf / 2; ++i) {
+      const float p0 = m == -INFINITY ? 0.f : __expf(x[2 * i] - m);
+      const float p1 = m == -INFINITY ? 0.f : __expf(x[2 * i + 1] - m);
+      lsum += p0 + p1;
+      const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
+      pw[i] = *reinterpret_cast<const uint32_t*>(&pp);
     }
-    fence_proxy_async_smem();
+    tmem_st16(tS_of(u) + lane_base + kh * (kHalf / 2), pw);
+    tmem_st_wait();
     tc_fence_before_sync();
-    __syncthreads();
-    if (tid == 0) {
+    ok = __syncthreads_and(ok && !*abort) != 0;
+    if (!ok) break;
+    if (tid == 0) {  // O += P V: A = P from TMEM (16 keys = 8 columns per step)
       tc_fence_after_sync();
-      const uint32_t sP = smem_addr(smem + kAtOffK + (u & 1) * 16384);
-      const uint32_t sV = smem_addr(smem + kAtOffV + (u & 1) * 16384);
-      constexpr uint32_t id_o = idesc_bf16_f32(128, 64, 0, 1);
+      ok = mbar_wait_suspend(&vbar[u & 1], (u >> 1) & 1, abort);
+      if (ok) {
+        const uint32_t sV = smem_addr(smem + kAtOffV + (u & 1) * 16384);
+        constexpr uint32_t id_o = idesc_bf16_f32(128, 128, 0, 1);
 #pragma unroll
-      for (int s = 0; s < kAtKeys / 16; ++s) {
-        const uint64_t ad = smem_desc(sP + s * 32, 16, 1024, kSwizzle128B);
-#pragma unroll
-        for (int at = 0; at < 2; ++at) {
-          const uint64_t bd = smem_desc(sV + at * 8192 + s * 2048, 1024, 1024, kSwizzle128B);
-          umma_bf16(tO + at * 64, ad, bd, id_o, (u > 0 || s > 0) ? 1u : 0u);
+        for (int s = 0; s < kAtKeys / 16; ++s) {
+          // MN-major V: the two 64-column atoms 8 KiB apart, 8-key groups 1 KiB apart
+          const uint64_t bd = smem_desc(sV + s * 2048, 8192, 1024, kSwizzle128B);
+          umma_bf16_tmem_a(tO, tS_of(u) + s * 8, bd, id_o, (u > 0 || s > 0) ? 1u : 0u);
         }
+        umma_commit(pvbar);
+        ++n_pv;
       }
-      umma_commit(mma_bar);
     }
-    ok = wait_mma();
   }
+  // the last P V product
+  if (tid == 0 && ok && n_pv > 0) ok = mbar_wait_suspend(pvbar, (n_pv - 1) & 1, abort);
+  ok = __syncthreads_and(ok) != 0;
   // the row's sum from its two halves (both kept against the same maximum)
   st[(2 + kh) * kAtRows + row] = lsum;
   __syncthreads();
@@ -358,9 +369,12 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   } else if (tid == 0) {
     // an expired wait: report it, and let the latest copy and products land (bounded)
     atomicCAS(&a.status[b], TGDN_SEQ_OK, TGDN_SEQ_TIMEOUT);
-    for (int bf = 0; bf < 2; ++bf)
-      if (tma_issued[bf] > 0) (void)mbar_wait(&tma_bar[bf], (tma_issued[bf] - 1) & 1);
-    if (mma_phase > 0) (void)mbar_wait(mma_bar, (mma_phase - 1) & 1);
+    for (int bf = 0; bf < 2; ++bf) {
+      if (k_issued[bf] > 0) (void)mbar_wait(&kbar[bf], (k_issued[bf] - 1) & 1);
+      if (v_issued[bf] > 0) (void)mbar_wait(&vbar[bf], (v_issued[bf] - 1) & 1);
+    }
+    if (n_s > 0) (void)mbar_wait(sbar, (n_s - 1) & 1);
+    if (n_pv > 0) (void)mbar_wait(pvbar, (n_pv - 1) & 1);
   }
   tc_fence_before_sync();
   __syncthreads();
