@@ -12,29 +12,37 @@
 // path of n: it solves a (depth+1)-sized unit triangular system.  So
 // U = T R and O = diag(e^G) Q S0 + W R, both tensor-core products.
 //
-// Persistent, warp-specialised kernel: one CTA per SM, 16 warps, looping over a
-// contiguous run of work items (sequence, v-head) that cover all 128 value
-// columns; trees have at most 64 nodes and depth at most 30.  Two items are in
-// flight per SM:
+// Persistent, warp-specialised kernel: one CTA per SM, 16 warps, looping over
+// work items (sequence, v-head) that cover all 128 value columns (a contiguous
+// run per CTA with a pending commit, else dealt round robin); trees have at most
+// 64 nodes and depth at most 30.  Two items are in flight per SM:
 //   producer warps 0-7, item j+1:
-//     tree metadata (prefetched) -> root paths (reused for the next head of the
-//     same sequence) and path-cumulative gates;
+//     tree metadata (prefetched as raw values) -> root paths (reused for the
+//     next head of the same sequence) and path-cumulative gates;
 //     S0 (prefetched into registers; warp w holds rows 16 w .. 16 w + 15) ->
 //     bf16 hi + lo operands (~16-bit products);
 //     TMA of the item's key and query rows -> A = [K; Q] (128-byte swizzle);
-//     tcgen05.mma into TMEM half (j+1)&1:
-//        D[:, 0:128] = A (S0_hi + S0_lo),  D[:, 128:192] = A K^T;
-//     the product's completion is awaited one item later, just before its
-//     operands are overwritten; prefetch of the next item's metadata and S0.
+//     the group's last thread issues tcgen05.mma into TMEM half (j+1)&1:
+//        D[:, 0:128] = A (S0_hi + S0_lo),  D[:, 128:192] = A K^T
+//     while the others prefetch the next item and build the paths; the
+//     product's completion is awaited one item later, just before its operands
+//     are overwritten.
 //   consumer warps 8-15, item j:
-//     Gram rows -> shared memory; R = diag(b)(V - e^G K S0) -> bf16 hi/lo operand;
-//     one thread per row of T (key lanes) or W (query lanes): substitution
-//     along the node's root path with the partial sums in registers, written
-//     straight into the [T; W] operand;
+//     Gram rows -> shared memory; V rows arrive by TMA in the R lo operand area
+//     and the key-lane warps form R = diag(b)(V - e^G K S0) there in place
+//     (bf16 hi/lo operand) while the query-lane warps substitute along the root
+//     paths with the partial sums in registers (depth <= 16: a node's T and W
+//     rows in one thread; deeper: one row per thread), writing straight into
+//     the [T; W] operand;
 //     tcgen05.mma: D[:, 128:256] = [T; W] R;
-//     key lanes store U (workspace), query lanes O = e^G Q S0 + W R (bf16).
+//     U (workspace) and O = e^G Q S0 + W R (bf16) leave through shared-memory
+//     staging and bulk copies.
 // The halves hand over through mbarriers: "stage 1 done" (the first product's
-// completion plus the producer's metadata) and "TMEM half free".
+// completion plus the producer's metadata) and "TMEM half free".  The kernel
+// is launched with programmatic stream serialization: its prologue may overlap
+// the previous kernel's tail and no input is read before griddepcontrol.wait.
+// In a launch above 64 nodes it takes only the sequences of at most 64 nodes
+// (small_only) and passes over the others without touching them.
 //
 // Deferred commit folded into the next verify (Methodik 3, last bullet: the
 // state is committed once the accepted branch is known, in the following
