@@ -7,18 +7,24 @@
 // ancestor-or-self bitmasks from tree prep.
 //
 // One CTA per (sequence, key/value head, tile of 128 query rows); a query row
-// is (node, query head of the group), row = node * G + g.  256 threads, two per
-// row (= TMEM lane), each taking half of every key tile and half of the output
-// columns; the halves of a row's maximum and normaliser are merged once.  Keys come in tiles of 64: first the cached context
-// (prefix_len[b] positions), then the tree's own nodes.  One pass over the key
-// tiles with an online softmax: P = exp(logit - m) is formed against a running
-// row maximum m as a bf16 operand and O += P V accumulates in TMEM; m is moved
-// (and O, the running sum rescaled in place) only when a tile's maximum exceeds
-// it by more than kRescaleGap, so P stays below e^kRescaleGap and rescaling is
-// rare.  O is divided by the sum at the end.  Pipeline: the score product of
-// tile u + 1 runs while the threads form P for tile u; P goes to TMEM over its
-// own score columns (two score buffers) and is the A operand of O += P V straight
-// from TMEM.  Key and value tiles are double-buffered with separate barriers: a
+// is (node, query head of the group), row = node * G + g.  256 softmax threads,
+// two per row (= TMEM lane), each taking half of every key tile and half of the
+// output columns; the halves of a row's maximum are exchanged per tile between
+// the two warps that hold the row, and its normaliser merged once at the end.
+// A ninth warp owns no rows: its lane 0 issues every copy and product, so the
+// softmax warps never wait for an issuing thread among them.
+//
+// Keys come in tiles of 64: first the cached context (prefix_len[b] positions),
+// then the tree's own nodes.  One pass over the key tiles with an online
+// softmax: P = exp(logit - m) is formed against a running row maximum m as a
+// bf16 operand and O += P V accumulates in TMEM; m is moved (and O, the running
+// sum rescaled in place) only when a tile's maximum exceeds it by more than
+// kRescaleGap, so P stays below e^kRescaleGap and rescaling is rare.  O is
+// divided by the sum at the end.  Pipeline: the score product of tile u + 1
+// runs while the softmax warps form P for tile u; P goes to TMEM over its own
+// score columns (two score buffers) and is the A operand of O += P V straight
+// from TMEM, issued once every softmax warp has arrived on the tile's "P ready"
+// barrier.  Key and value tiles are double-buffered with separate barriers: a
 // key buffer is refilled once its score product is done (two tiles ahead), a
 // value buffer once its P V product is done.
 //
@@ -35,7 +41,9 @@
 
 namespace tgdn {
 
-constexpr int kAtThreads = 256;
+constexpr int kAtThreads = 256;          // softmax threads: two per query row
+constexpr int kAtIssueWarp = kAtThreads / 32;  // the warp that issues every copy and product
+constexpr int kAtBlock = kAtThreads + 32;
 constexpr int kAtRows = 128;             // query rows per CTA
 constexpr float kRescaleGap = 8.f;       // lazy rescaling threshold (natural log units)
 constexpr int kAtKeys = 64;              // keys per tile
@@ -47,8 +55,8 @@ constexpr int kAtOffQ = 0;               // [2 d halves][128 rows][128 B]     32
 constexpr int kAtOffK = 32768;           // 2 x [2 d halves][64 keys][128 B]  2 x 16 KiB
 constexpr int kAtOffV = 65536;           // 2 x [2 d atoms][64 keys][128 B]   2 x 16 KiB
 constexpr int kAtOffMask = 98304;        // [kAtMaxNodes][2] uint64          2 KiB
-constexpr int kAtOffStat = kAtOffMask + kAtMaxNodes * 16;  // [2][128] row max, [2][128] sum
-constexpr int kAtOffBar = kAtOffStat + 4 * kAtRows * 4;
+constexpr int kAtOffStat = kAtOffMask + kAtMaxNodes * 16;  // [2 tiles][2][128] row max, [2][128] sum
+constexpr int kAtOffBar = kAtOffStat + 6 * kAtRows * 4;
 constexpr int kAtSmemBytes = kAtOffBar + 128 + 1024;
 
 __device__ __forceinline__ int at_swz(int row, int chunk) {
@@ -69,7 +77,7 @@ struct AtArgs {
   __nv_bfloat16* o;
 };
 
-__global__ void __launch_bounds__(kAtThreads, 2)  // two CTAs per SM: <= 128 registers
+__global__ void __launch_bounds__(kAtBlock, 2)  // two CTAs per SM: <= 112 registers
 tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
                  const __grid_constant__ CUtensorMap ktmap,
                  const __grid_constant__ CUtensorMap vtmap,
@@ -80,10 +88,11 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
       (reinterpret_cast<uintptr_t>(at_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* amask = reinterpret_cast<uint64_t*>(smem + kAtOffMask);
   uint64_t* kbar = reinterpret_cast<uint64_t*>(smem + kAtOffBar);  // [2] key tile (+ Q)
-  uint64_t* vbar = kbar + 2;                                          // [2] value tile
-  uint64_t* sbar = vbar + 2;   // score products, one completion per tile
-  uint64_t* pvbar = sbar + 1;  // P V products, one completion per tile
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pvbar + 1);
+  uint64_t* vbar = kbar + 2;     // [2] value tile
+  uint64_t* sbar = vbar + 2;     // [2] score product of tile u (buffer u & 1)
+  uint64_t* pvbar = sbar + 2;    // [2] P V product of tile u
+  uint64_t* pready = pvbar + 2;  // [2] P of tile u in TMEM: one arrival per softmax warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pready + 2);
   int* s_abort = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int item = blockIdx.x / a.splits, sp = blockIdx.x % a.splits;
@@ -91,7 +100,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   const int mt = item % a.mtiles;
   const int hk = (item / a.mtiles) % a.H_kv;
   const int b = item / (a.mtiles * a.H_kv);
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int lo = a.cu[b], N = a.cu[b + 1] - lo;
   const int npt = kAtRows / a.G;             // nodes per tile of query rows
   const int node0 = mt * npt;
@@ -102,7 +111,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   __nv_bfloat16* orow =
       a.o + ((size_t)(lo + my_node) * a.H_q + hk * a.G + my_g) * kAtD;
   if (a.status[b] != TGDN_SEQ_OK || N > kAtMaxNodes || N > a.n_max) {
-    if (row_live)
+    if (row_live && tid < kAtThreads)
       for (int c = kh * 8; c < kh * 8 + 8; ++c)
         reinterpret_cast<uint4*>(orow)[c] = make_uint4(0, 0, 0, 0);
     return;
@@ -113,9 +122,10 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
     for (int i = 0; i < 2; ++i) {
       mbar_init(&kbar[i], 1);
       mbar_init(&vbar[i], 1);
+      mbar_init(&sbar[i], 1);
+      mbar_init(&pvbar[i], 1);
+      mbar_init(&pready[i], kAtThreads / 32);
     }
-    mbar_init(sbar, 1);
-    mbar_init(pvbar, 1);
     fence_mbar_init();
     *s_abort = 0;
   }
@@ -160,9 +170,11 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   const uint64_t m_hi = row_live ? amask[2 * my_node + 1] : 0;
 
   // Steps u = 0 .. nt - 1: key and value tile u in buffer u & 1, scores and P in
-  // TMEM buffer u & 1.  Thread 0 issues every copy and product.
-  int k_issued[2] = {0, 0}, v_issued[2] = {0, 0};  // copies issued per buffer (thread 0)
-  uint32_t n_s = 0;                                 // score products issued (thread 0)
+  // TMEM buffer u & 1.  Lane 0 of the issuing warp issues every copy and product;
+  // each barrier of a pair serves every other tile, so no waiter can be a whole
+  // phase behind.
+  int k_issued[2] = {0, 0}, v_issued[2] = {0, 0};   // copies issued per buffer
+  int s_issued[2] = {0, 0}, pv_issued[2] = {0, 0};  // products issued per barrier
   auto tile_row = [&](int u, const CUtensorMap*& km, const CUtensorMap*& vm) {
     const int t = tile_of(u);
     const bool pre = t < nt_pre;
@@ -194,7 +206,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
     tma_load_3d(vdst + 8192, vm, bar, 64, hk, r);
     v_issued[u & 1] += 1;
   };
-  // thread 0: S = Q K^T of tile u into score buffer u & 1 (its key tile has landed)
+  // S = Q K^T of tile u into score buffer u & 1 (once its key tile has landed)
   auto score = [&](int u) -> bool {
     if (!mbar_wait_suspend(&kbar[u & 1], (u >> 1) & 1, abort)) return false;
     tc_fence_after_sync();
@@ -207,8 +219,8 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
       const uint64_t bd = smem_desc(sK + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024, kSwizzle128B);
       umma_bf16(tS_of(u), ad, bd, id_s, s > 0);
     }
-    umma_commit(sbar);
-    ++n_s;
+    umma_commit(&sbar[u & 1]);
+    s_issued[u & 1] += 1;
     return true;
   };
   // this thread's 32 logits of tile u (keys kh * 32 ..), scaled, masked to -inf
@@ -234,97 +246,138 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   };
 
   bool ok = true;
-  if (tid == 0 && nt > 0) {
-    issue_k(0);
-    issue_v(0);
-    if (nt > 1) issue_k(1);
-    ok = score(0);
-  }
   float* st = reinterpret_cast<float*>(smem + kAtOffStat);
   float m = -INFINITY;  // running row maximum (same in both threads of a row)
   float lsum = 0.f;     // this thread's half of the row's sum of exp(logit - m)
-  uint32_t n_pv = 0;    // P V products issued (thread 0)
-  for (int u = 0; u < nt; ++u) {
-    // thread 0: S(u) and P V(u - 1) done (their buffers are free); value tile u + 1
-    // and key tile u + 2 go out; S(u + 1) starts and runs while P of tile u is formed
-    if (tid == 0 && ok) {
-      ok = mbar_wait_suspend(sbar, u & 1, abort);
-      if (ok && u > 0) ok = mbar_wait_suspend(pvbar, (u - 1) & 1, abort);
-      if (ok && u + 1 < nt) issue_v(u + 1);
-      if (ok && u + 2 < nt) issue_k(u + 2);
-      if (ok && u + 1 < nt) ok = score(u + 1);
-    }
-    ok = __syncthreads_and(ok) != 0;
-    if (!ok) break;
-    tc_fence_after_sync();
-    float x[kHalf];
-    read_logits(u, x);
-    float lm = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < kHalf; ++c) lm = fmaxf(lm, x[c]);
-    st[kh * kAtRows + row] = lm;
-    __syncthreads();  // (also: both halves of every row have read their scores)
-    const float mt = fmaxf(st[row], st[kAtRows + row]);
-    const bool need = mt > m + kRescaleGap;  // also the first finite maximum of the row
-    const float alpha = need ? (m == -INFINITY ? 0.f : __expf(m - mt)) : 1.f;
-    if (need) {
-      m = mt;
-      lsum *= alpha;
-    }
-    if (u > 0 && __any_sync(0xffffffffu, need)) {  // O *= alpha (warp-collective)
-#pragma unroll
-      for (int q = 2 * kh; q < 2 * kh + 2; ++q) {
-        float r[32];
-        tmem_ld32(tO + lane_base + q * 32, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < 32; ++c) r[c] *= alpha;
-        tmem_st32(tO + lane_base + q * 32, r);
-      }
-    }
-    // P = exp(logit - m) as bf16 pairs over this thread's 32 score columns' first
-    // 16 (key 2 c and 2 c + 1 in column c of the half)
-    uint32_t pw[kHalf / 2];
-#pragma unroll
-    for (int i = 0; i < kHalf / 2; ++i) {
-      const float p0 = m == -INFINITY ? 0.f : __expf(x[2 * i] - m);
-      const float p1 = m == -INFINITY ? 0.f : __expf(x[2 * i + 1] - m);
-      lsum += p0 + p1;
-      const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
-      pw[i] = *reinterpret_cast<const uint32_t*>(&pp);
-    }
-    tmem_st16(tS_of(u) + lane_base + kh * (kHalf / 2), pw);
-    tmem_st_wait();
-    tc_fence_before_sync();
-    ok = __syncthreads_and(ok && !*abort) != 0;
-    if (!ok) break;
-    if (tid == 0) {  // O += P V: A = P from TMEM (16 keys = 8 columns per step)
-      tc_fence_after_sync();
-      ok = mbar_wait_suspend(&vbar[u & 1], (u >> 1) & 1, abort);
-      if (ok) {
-        const uint32_t sV = smem_addr(smem + kAtOffV + (u & 1) * 16384);
-        constexpr uint32_t id_o = idesc_bf16_f32(128, 128, 0, 1);
-#pragma unroll
-        for (int s = 0; s < kAtKeys / 16; ++s) {
-          // MN-major V: the two 64-column atoms 8 KiB apart, 8-key groups 1 KiB apart
-          const uint64_t bd = smem_desc(sV + s * 2048, 8192, 1024, kSwizzle128B);
-          umma_bf16_tmem_a(tO, tS_of(u) + s * 8, bd, id_o, (u > 0 || s > 0) ? 1u : 0u);
+  if (warp == kAtIssueWarp) {
+    // ---- the issuing warp: S(u + 1) is issued while the softmax warps form P of
+    // tile u, then O += P V of tile u once every softmax warp has stored its P
+    if (lane == 0 && nt > 0) {
+      issue_k(0);
+      issue_v(0);
+      if (nt > 1) issue_k(1);
+      ok = score(0);
+      for (int u = 0; ok && u < nt; ++u) {
+        const uint32_t ph = (u >> 1) & 1;
+        if (u + 1 < nt) {
+          // P V of tile u - 1 is done: score buffer (u + 1) & 1 and value buffer
+          // (u + 1) & 1 are free
+          if (u > 0) ok = mbar_wait_suspend(&pvbar[(u - 1) & 1], ((u - 1) >> 1) & 1, abort);
+          if (ok) issue_v(u + 1);
+          if (ok) ok = score(u + 1);
         }
-        umma_commit(pvbar);
-        ++n_pv;
+        if (ok && u + 2 < nt) {  // S(u) is done: key buffer u & 1 is free
+          ok = mbar_wait_suspend(&sbar[u & 1], ph, abort);
+          if (ok) issue_k(u + 2);
+        }
+        if (ok) ok = mbar_wait_suspend(&pready[u & 1], ph, abort);
+        if (ok) ok = mbar_wait_suspend(&vbar[u & 1], ph, abort);
+        if (ok) {  // O += P V: A = P from TMEM (16 keys = 8 columns per step)
+          tc_fence_after_sync();
+          const uint32_t sV = smem_addr(smem + kAtOffV + (u & 1) * 16384);
+          constexpr uint32_t id_o = idesc_bf16_f32(128, 128, 0, 1);
+#pragma unroll
+          for (int s = 0; s < kAtKeys / 16; ++s) {
+            // MN-major V: the two 64-column atoms 8 KiB apart, 8-key groups 1 KiB apart
+            const uint64_t bd = smem_desc(sV + s * 2048, 8192, 1024, kSwizzle128B);
+            umma_bf16_tmem_a(tO, tS_of(u) + s * 8, bd, id_o, (u > 0 || s > 0) ? 1u : 0u);
+          }
+          umma_commit(&pvbar[u & 1]);
+          pv_issued[u & 1] += 1;
+        }
       }
+      // the last P V product: O is final
+      if (ok) ok = mbar_wait_suspend(&pvbar[(nt - 1) & 1], ((nt - 1) >> 1) & 1, abort);
+    }
+    __syncwarp();
+  } else {
+    // ---- softmax warps.  The two threads of a row sit in warps w and w + 4 (the
+    // same TMEM lane quarter); they exchange their halves' maxima through shared
+    // memory behind a barrier of that warp pair, which also carries the decision
+    // to stop (so both warps of a pair leave the loop at the same step).
+    const int pair_bar = 1 + (warp & 3);
+    for (int u = 0; u < nt; ++u) {
+      const uint32_t ph = (u >> 1) & 1;
+      ok = __all_sync(0xffffffffu, ok && mbar_wait_suspend(&sbar[u & 1], ph, abort)) != 0;
+      float x[kHalf];
+      float lm = -INFINITY;
+      if (ok) {
+        tc_fence_after_sync();
+        read_logits(u, x);
+#pragma unroll
+        for (int c = 0; c < kHalf; ++c) lm = fmaxf(lm, x[c]);
+      }
+      float* stu = st + (u & 1) * 2 * kAtRows;
+      stu[kh * kAtRows + row] = lm;
+      // (also: both halves of the row have read their scores before P overwrites them)
+      if (!named_sync_and(pair_bar, 64, ok && !*abort)) {
+        ok = false;
+        break;
+      }
+      const float mt = fmaxf(stu[row], stu[kAtRows + row]);
+      const bool need = mt > m + kRescaleGap;  // also the first finite maximum of the row
+      const float alpha = need ? (m == -INFINITY ? 0.f : __expf(m - mt)) : 1.f;
+      if (need) {
+        m = mt;
+        lsum *= alpha;
+      }
+      if (u > 0 && __any_sync(0xffffffffu, need)) {  // O *= alpha (warp-collective)
+        // O is stable once the previous tile's P V product is done
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait_suspend(&pvbar[(u - 1) & 1], ((u - 1) >> 1) & 1, abort)) != 0;
+        if (ok) {
+          tc_fence_after_sync();
+#pragma unroll 1
+          for (int q = 4 * kh; q < 4 * kh + 4; ++q) {  // 16 columns at a time
+            float r[16];
+            tmem_ld16(tO + lane_base + q * 16, r);
+            tmem_ld_wait();
+            uint32_t w[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) w[c] = __float_as_uint(r[c] * alpha);
+            tmem_st16(tO + lane_base + q * 16, w);
+          }
+        }
+      }
+      if (!ok) continue;  // the next pair barrier stops both warps
+      // P = exp(logit - m) as bf16 pairs over this thread's 32 score columns' first
+      // 16 (key 2 c and 2 c + 1 in column c of the half)
+      uint32_t pw[kHalf / 2];
+#pragma unroll
+      for (int i = 0; i < kHalf / 2; ++i) {
+        const float p0 = m == -INFINITY ? 0.f : __expf(x[2 * i] - m);
+        const float p1 = m == -INFINITY ? 0.f : __expf(x[2 * i + 1] - m);
+        lsum += p0 + p1;
+        const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
+        pw[i] = *reinterpret_cast<const uint32_t*>(&pp);
+      }
+      tmem_st16(tS_of(u) + lane_base + kh * (kHalf / 2), pw);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pready[u & 1]);
     }
   }
-  // the last P V product
-  if (tid == 0 && ok && n_pv > 0) ok = mbar_wait_suspend(pvbar, (n_pv - 1) & 1, abort);
   ok = __syncthreads_and(ok) != 0;
   // the row's sum from its two halves (both kept against the same maximum)
-  st[(2 + kh) * kAtRows + row] = lsum;
+  float* ssum = st + 4 * kAtRows;
+  if (tid < kAtThreads) ssum[kh * kAtRows + row] = lsum;
   __syncthreads();
-  const float l = st[2 * kAtRows + row] + st[3 * kAtRows + row];
+  const float l = tid < kAtThreads ? ssum[row] + ssum[kAtRows + row] : 0.f;
   const float inv_l = l > 0.f ? 1.f / l : 0.f;
   // ---- epilogue: O rows to global (bf16), or this split's part to the workspace
-  if (ok && a.splits > 1) {
+  if (tid >= kAtThreads) {
+    if (!ok && lane == 0) {
+      // an expired wait: report it, and let the latest copies and products land (bounded)
+      atomicCAS(&a.status[b], TGDN_SEQ_OK, TGDN_SEQ_TIMEOUT);
+      for (int bf = 0; bf < 2; ++bf) {
+        if (k_issued[bf] > 0) (void)mbar_wait(&kbar[bf], (k_issued[bf] - 1) & 1);
+        if (v_issued[bf] > 0) (void)mbar_wait(&vbar[bf], (v_issued[bf] - 1) & 1);
+        if (s_issued[bf] > 0) (void)mbar_wait(&sbar[bf], (s_issued[bf] - 1) & 1);
+        if (pv_issued[bf] > 0) (void)mbar_wait(&pvbar[bf], (pv_issued[bf] - 1) & 1);
+      }
+    }
+  } else if (ok && a.splits > 1) {
     tc_fence_after_sync();
     float* prow = a.part + (((size_t)sp * a.n_items + item) * kAtRows + row) * kPartStride;
 #pragma unroll
@@ -366,15 +419,6 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
         }
       }
     }
-  } else if (tid == 0) {
-    // an expired wait: report it, and let the latest copy and products land (bounded)
-    atomicCAS(&a.status[b], TGDN_SEQ_OK, TGDN_SEQ_TIMEOUT);
-    for (int bf = 0; bf < 2; ++bf) {
-      if (k_issued[bf] > 0) (void)mbar_wait(&kbar[bf], (k_issued[bf] - 1) & 1);
-      if (v_issued[bf] > 0) (void)mbar_wait(&vbar[bf], (v_issued[bf] - 1) & 1);
-    }
-    if (n_s > 0) (void)mbar_wait(sbar, (n_s - 1) & 1);
-    if (n_pv > 0) (void)mbar_wait(pvbar, (n_pv - 1) & 1);
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -516,7 +560,7 @@ cudaError_t launch_tree_attn(const tgdn_tree& t, int H_q, int H_kv, int P_max, f
   e = cudaFuncSetAttribute(tree_attn_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                            (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  tree_attn_kernel<<<(unsigned)(items * a.splits), kAtThreads, kAtSmemBytes, s>>>(
+  tree_attn_kernel<<<(unsigned)(items * a.splits), kAtBlock, kAtSmemBytes, s>>>(
       qmap, ktmap, vtmap, kcmap, vcmap, a);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.splits == 1) return e;
