@@ -218,9 +218,9 @@ int tgdn_tree_build(int32_t B, int32_t budget, int32_t K, int32_t w, int32_t dep
  *           and the parts merged, which keeps every SM busy on small batches
  * tgdn_tree_prep must have run on `tree`; sequences with a bad status get zero
  * outputs.  Tensor-core kernel: d = 128, H_q / H_kv in {1, 2, 4, 8, 16},
- * n_max <= 128; other shapes return TGDN_EUNSUPPORTED.  All pointers 16-byte
- * aligned.  Returns TGDN_OK, TGDN_EINVAL, TGDN_ETOOBIG, TGDN_EUNSUPPORTED or
- * TGDN_ECUDA. */
+ * n_max <= 128; other shapes return TGDN_EUNSUPPORTED.  scale must be positive
+ * and finite (TGDN_EINVAL otherwise).  All pointers 16-byte aligned.  Returns
+ * TGDN_OK, TGDN_EINVAL, TGDN_ETOOBIG, TGDN_EUNSUPPORTED or TGDN_ECUDA. */
 int tgdn_tree_attention(const tgdn_tree* tree, int32_t H_q, int32_t H_kv, int32_t d,
                         const void* q, const void* k_tree, const void* v_tree,
                         const void* k_cache, const void* v_cache, const int32_t* prefix_len,

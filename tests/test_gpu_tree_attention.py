@@ -145,6 +145,14 @@ def test_unsupported_shapes_are_refused():
         run_gpu(c)
 
 
+@pytest.mark.parametrize("scale", [0.0, -0.1, float("nan"), float("inf")])
+def test_scale_must_be_positive_and_finite(scale):
+    c = make_case([np.array([-1, 0], np.int32)], 4, 4, 8, [8], seed=8)
+    c["scale"] = scale
+    with pytest.raises(tgdn.TgdnError):
+        run_gpu(c)
+
+
 def test_many_context_splits_with_an_empty_context():
     """Four splits of a 4096-position context next to a sequence with no context (its
     context splits are empty and only the last one, with the tree's keys, counts)."""

@@ -255,6 +255,7 @@ int tgdn_tree_attention(const tgdn_tree* tree, int32_t H_q, int32_t H_kv, int32_
   if (rc != TGDN_OK) return rc;
   const tgdn_tree& t = *tree;
   if (H_q < 1 || H_kv < 1 || H_q % H_kv != 0 || d < 1 || P_max < 0) return TGDN_EINVAL;
+  if (!(scale > 0.f && scale <= 3.0e38f)) return TGDN_EINVAL;  // positive and finite
   if (!tgdn::tree_attn_supported(t, H_q, H_kv, d)) return TGDN_EUNSUPPORTED;
   if (t.B > 0 && (!prefix_len || (P_max > 0 && (!k_cache || !v_cache)))) return TGDN_EINVAL;
   if (t.T > 0 && (!q || !k_tree || !v_tree || !o)) return TGDN_EINVAL;

@@ -223,19 +223,21 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
     s_issued[u & 1] += 1;
     return true;
   };
-  // this thread's 32 logits of tile u (keys kh * 32 ..), scaled, masked to -inf
+  // this thread's 32 raw scores q.k of tile u (keys kh * 32 ..), masked to -inf
+  // (the softmax scale enters with the exponent; only a partial context tile, a
+  // row past the tree or a tree tile needs the mask)
   constexpr int kHalf = kAtKeys / 2;
   auto read_logits = [&](int u, float (&x)[kHalf]) {
     const int t = tile_of(u);
     tmem_ld32(tS_of(u) + lane_base + kh * kHalf, x);
     tmem_ld_wait();
-#pragma unroll
-    for (int c = 0; c < kHalf; ++c) x[c] *= a.scale;
     if (t < nt_pre) {
       const int lim = P - t * kAtKeys - kh * kHalf;  // keys below lim are cached context
+      if (lim < kHalf || !row_live) {
 #pragma unroll
-      for (int c = 0; c < kHalf; ++c)
-        if (c >= lim || !row_live) x[c] = -INFINITY;
+        for (int c = 0; c < kHalf; ++c)
+          if (c >= lim || !row_live) x[c] = -INFINITY;
+      }
     } else {
       const int s0 = (t - nt_pre) * kAtKeys + kh * kHalf;
       const uint64_t mk = (s0 < 64 ? m_lo : m_hi) >> (s0 & 63);
@@ -247,7 +249,11 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
 
   bool ok = true;
   float* st = reinterpret_cast<float*>(smem + kAtOffStat);
-  float m = -INFINITY;  // running row maximum (same in both threads of a row)
+  float m = -INFINITY;  // running maximum of the row's raw scores (same in both threads)
+  // exp(scale (x - m)) = 2^(x c - m c) with c = scale log2(e); the rescaling
+  // threshold kRescaleGap (natural-log units) in raw-score units
+  const float c2 = a.scale * 1.4426950408889634f;
+  const float gap_raw = kRescaleGap / a.scale;
   float lsum = 0.f;     // this thread's half of the row's sum of exp(logit - m)
   if (warp == kAtIssueWarp) {
     // ---- the issuing warp: S(u + 1) is issued while the softmax warps form P of
@@ -315,8 +321,8 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
         break;
       }
       const float mt = fmaxf(stu[row], stu[kAtRows + row]);
-      const bool need = mt > m + kRescaleGap;  // also the first finite maximum of the row
-      const float alpha = need ? (m == -INFINITY ? 0.f : __expf(m - mt)) : 1.f;
+      const bool need = mt > m + gap_raw;  // also the first finite maximum of the row
+      const float alpha = need ? (m == -INFINITY ? 0.f : fast_exp2((m - mt) * c2)) : 1.f;
       if (need) {
         m = mt;
         lsum *= alpha;
@@ -342,11 +348,13 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
       if (!ok) continue;  // the next pair barrier stops both warps
       // P = exp(logit - m) as bf16 pairs over this thread's 32 score columns' first
       // 16 (key 2 c and 2 c + 1 in column c of the half)
+      // (m = -inf only while every score so far is masked: then 2^(-inf) = 0)
+      const float mc = m == -INFINITY ? 0.f : m * c2;
       uint32_t pw[kHalf / 2];
 #pragma unroll
       for (int i = 0; i < kHalf / 2; ++i) {
-        const float p0 = m == -INFINITY ? 0.f : __expf(x[2 * i] - m);
-        const float p1 = m == -INFINITY ? 0.f : __expf(x[2 * i + 1] - m);
+        const float p0 = fast_exp2(fmaf(x[2 * i], c2, -mc));
+        const float p1 = fast_exp2(fmaf(x[2 * i + 1], c2, -mc));
         lsum += p0 + p1;
         const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
         pw[i] = *reinterpret_cast<const uint32_t*>(&pp);
@@ -395,7 +403,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
             make_float4(r[c4 * 4], r[c4 * 4 + 1], r[c4 * 4 + 2], r[c4 * 4 + 3]);
     }
     if (kh == 0) {
-      prow[kAtD] = m;
+      prow[kAtD] = m * a.scale;  // the row maximum of the scaled logits
       prow[kAtD + 1] = l;
     }
   } else if (ok) {
