@@ -240,34 +240,6 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
       if (!v_ok) ok = false;
     }
     ok = __syncthreads_and(ok) != 0;
-    if (ok && tid < Nf) {
-      // bits of the ancestor mask are topological positions; ascending = root first
-      const int dn = M.dep[tid];
-      int i = 0;
-      float acc = 0.f;
-      bool pk = true;
-#pragma unroll
-      for (int w = 0; w < 3; ++w) {
-        if (w >= words || !pk) break;
-        uint64_t mk = mk3[w];
-        while (mk && pk) {
-          const int b = w * 64 + __ffsll(static_cast<long long>(mk)) - 1 - fold;
-          mk &= mk - 1;
-          if (b < 0) continue;  // the folded root
-          if (b >= Nf || i > dn) {
-            pk = false;
-            break;
-          }
-          const int s = M.ord[b];
-          pk = M.dep[s] == i;
-          M.anc_at[i][tid] = static_cast<uint8_t>(s);
-          acc += M.gg[s];
-          ++i;
-        }
-      }
-      if (!pk || i != dn + 1 || M.anc_at[dn][tid] != tid) ok = false;
-      M.G[tid] = acc;
-    }
     // ---- S0 -> bf16 hi + lo operand (thread: rows (tid >> 5) + 16 r, float4 column tid & 31)
     {
       if (fold) {  // the root's own step: S_r = a_r S0 + k_r u_r^T, o_r = S_r^T q_r
@@ -338,23 +310,12 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
       }
     }
     fence_proxy_async_smem();
-    ok = __syncthreads_and(ok) != 0;
-    if (!ok) {  // bad sequence: zero rows, and let an issued copy land before reuse
-      if (tid == 0 && tma_issued) (void)mbar_wait_suspend(&M.tma_bar, (M.tma_n - 1) & 1, abort);
-      for (int e = tid; e < N * (kT8D / 4); e += kT8Threads) {
-        const int n = e >> 5, c4 = e & 31;
-        const size_t row = (obase0 + (size_t)n * H_v) * kT8D + c4 * 4;
-        *reinterpret_cast<uint2*>(o + row) = make_uint2(0u, 0u);
-        *reinterpret_cast<float4*>(Uws + row) = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      for (int n = tid; n < N; n += kT8Threads) Gws[obase0 + (size_t)n * H_v] = 0.f;
-      if (__syncthreads_or(*abort)) break;
-      continue;
-    }
-
-    // ---- the tensor-core product (one thread issues, everyone waits)
+    __syncthreads();  // the S0 operand is complete
+    // ---- the tensor-core product, issued by the last thread (it has no node)
+    // while the node threads build their root paths
     bool step_ok = true;
-    if (tid == 0) {
+    const bool product = ok;  // (uniform) metadata valid: copy issued, product goes out
+    if (tid == kT8Threads - 1 && product) {
       step_ok = mbar_wait_suspend(&M.tma_bar, (M.tma_n - 1) & 1, abort);
       if (step_ok) {
         tc_fence_after_sync();
@@ -379,9 +340,54 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
         }
         umma_commit(&M.mma_bar);
         M.mma_n += 1;
-        step_ok = mbar_wait_suspend(&M.mma_bar, (M.mma_n - 1) & 1, abort);
       }
     }
+    if (ok && tid < Nf) {
+      // bits of the ancestor mask are topological positions; ascending = root first
+      const int dn = M.dep[tid];
+      int i = 0;
+      float acc = 0.f;
+      bool pk = true;
+#pragma unroll
+      for (int w = 0; w < 3; ++w) {
+        if (w >= words || !pk) break;
+        uint64_t mk = mk3[w];
+        while (mk && pk) {
+          const int b = w * 64 + __ffsll(static_cast<long long>(mk)) - 1 - fold;
+          mk &= mk - 1;
+          if (b < 0) continue;  // the folded root
+          if (b >= Nf || i > dn) {
+            pk = false;
+            break;
+          }
+          const int s = M.ord[b];
+          pk = M.dep[s] == i;
+          M.anc_at[i][tid] = static_cast<uint8_t>(s);
+          acc += M.gg[s];
+          ++i;
+        }
+      }
+      if (!pk || i != dn + 1 || M.anc_at[dn][tid] != tid) ok = false;
+      M.G[tid] = acc;
+    }
+    ok = __syncthreads_and(ok) != 0;
+    if (!ok) {  // bad sequence: zero rows, and let an issued copy and product land before reuse
+      if (tid == kT8Threads - 1 && product && step_ok)
+        (void)mbar_wait_suspend(&M.mma_bar, (M.mma_n - 1) & 1, abort);
+      if (tid == 0 && tma_issued) (void)mbar_wait_suspend(&M.tma_bar, (M.tma_n - 1) & 1, abort);
+      for (int e = tid; e < N * (kT8D / 4); e += kT8Threads) {
+        const int n = e >> 5, c4 = e & 31;
+        const size_t row = (obase0 + (size_t)n * H_v) * kT8D + c4 * 4;
+        *reinterpret_cast<uint2*>(o + row) = make_uint2(0u, 0u);
+        *reinterpret_cast<float4*>(Uws + row) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      for (int n = tid; n < N; n += kT8Threads) Gws[obase0 + (size_t)n * H_v] = 0.f;
+      if (__syncthreads_or(*abort)) break;
+      continue;
+    }
+
+    if (tid == kT8Threads - 1 && step_ok)
+      step_ok = mbar_wait_suspend(&M.mma_bar, (M.mma_n - 1) & 1, abort);
     if (!__syncthreads_and(step_ok)) break;
     tc_fence_after_sync();
 
