@@ -151,7 +151,9 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
     nx_hi = nb_hi;
     nx_st = nb_st;
     nx_d0 = 0;
-    if (it < n_items && nx_hi > nx_lo) {
+    // (an item this launch passes over, a sequence of at most 64 nodes when the
+    // 64-node kernel takes those, is not pulled into L2)
+    if (it < n_items && nx_hi > nx_lo && !(big_only && nx_hi - nx_lo <= 64)) {
       nx_d0 = depth[nx_lo];
       if (tid == 0) prefetch_l2(S0 + (size_t)it * kT8D * kT8D, kT8D * kT8D * 4);
       if (tid < nx_hi - nx_lo && tid <= kT8Nodes)
