@@ -310,8 +310,15 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
       if (ok) {
         tc_fence_after_sync();
         read_logits(u, x);
+        // pairwise: five dependent levels instead of 31
+        float t[kHalf / 2];
 #pragma unroll
-        for (int c = 0; c < kHalf; ++c) lm = fmaxf(lm, x[c]);
+        for (int c = 0; c < kHalf / 2; ++c) t[c] = fmaxf(x[2 * c], x[2 * c + 1]);
+#pragma unroll
+        for (int w = kHalf / 4; w >= 1; w /= 2)
+#pragma unroll
+          for (int c = 0; c < w; ++c) t[c] = fmaxf(t[c], t[c + w]);
+        lm = t[0];
       }
       float* stu = st + (u & 1) * 2 * kAtRows;
       stu[kh * kAtRows + row] = lm;
@@ -351,14 +358,16 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
       // (m = -inf only while every score so far is masked: then 2^(-inf) = 0)
       const float mc = m == -INFINITY ? 0.f : m * c2;
       uint32_t pw[kHalf / 2];
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};  // four independent partial sums
 #pragma unroll
       for (int i = 0; i < kHalf / 2; ++i) {
         const float p0 = fast_exp2(fmaf(x[2 * i], c2, -mc));
         const float p1 = fast_exp2(fmaf(x[2 * i + 1], c2, -mc));
-        lsum += p0 + p1;
+        ps[i & 3] += p0 + p1;
         const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
         pw[i] = *reinterpret_cast<const uint32_t*>(&pp);
       }
+      lsum += (ps[0] + ps[1]) + (ps[2] + ps[3]);
       tmem_st16(tS_of(u) + lane_base + kh * (kHalf / 2), pw);
       tmem_st_wait();
       tc_fence_before_sync();
