@@ -271,10 +271,10 @@ int tgdn_tree_attention(const tgdn_tree* tree, int32_t H_q, int32_t H_kv, int32_
   const void* vc = P_max > 0 ? v_cache : v_tree;
   const long crows = P_max > 0 ? (long)t.B * P_max : t.T;
   if (!encode_rows_map(&qm, q, t.T, H_q, G, 128 / G) ||
-      !encode_rows_map(&ktm, k_tree, t.T, H_kv, 1, 64) ||
-      !encode_rows_map(&vtm, v_tree, t.T, H_kv, 1, 64) ||
-      !encode_rows_map(&kcm, kc, crows, H_kv, 1, 64) ||
-      !encode_rows_map(&vcm, vc, crows, H_kv, 1, 64))
+      !encode_rows_map(&ktm, k_tree, t.T, H_kv, 1, 128) ||
+      !encode_rows_map(&vtm, v_tree, t.T, H_kv, 1, 128) ||
+      !encode_rows_map(&kcm, kc, crows, H_kv, 1, 128) ||
+      !encode_rows_map(&vcm, vc, crows, H_kv, 1, 128))
     return TGDN_ECUDA;
   return from_cuda(tgdn::launch_tree_attn(t, H_q, H_kv, P_max, scale, qm, ktm, vtm, kcm, vcm,
                                           prefix_len, o, ws, ws ? ws_bytes : 0,

@@ -12,9 +12,10 @@
 // output columns; the halves of a row's maximum are exchanged per tile between
 // the two warps that hold the row, and its normaliser merged once at the end.
 // A ninth warp owns no rows: its lane 0 issues every copy and product, so the
-// softmax warps never wait for an issuing thread among them.
+// softmax warps never wait for an issuing thread among them.  One CTA per SM
+// (the 512 TMEM columns: two 128-column score buffers and the 128-column O).
 //
-// Keys come in tiles of 64: first the cached context (prefix_len[b] positions),
+// Keys come in tiles of 128: first the cached context (prefix_len[b] positions),
 // then the tree's own nodes.  One pass over the key tiles with an online
 // softmax: P = exp(logit - m) is formed against a running row maximum m as a
 // bf16 operand and O += P V accumulates in TMEM; m is moved (and O, the running
@@ -26,7 +27,9 @@
 // from TMEM, issued once every softmax warp has arrived on the tile's "P ready"
 // barrier.  Key and value tiles are double-buffered with separate barriers: a
 // key buffer is refilled once its score product is done (two tiles ahead), a
-// value buffer once its P V product is done.
+// value buffer once its P V product is done.  The tile is 128 keys wide because
+// the SM issues tcgen05.mma instructions at a bounded rate: a 128-key score
+// product is 8 instructions of N = 128, where two 64-key tiles took 16 of N = 64.
 //
 // With a workspace the cached context of each (sequence, head, row tile) is
 // split over several CTAs (the tree's own keys go to the last one); each writes
@@ -46,15 +49,16 @@ constexpr int kAtIssueWarp = kAtThreads / 32;  // the warp that issues every cop
 constexpr int kAtBlock = kAtThreads + 32;
 constexpr int kAtRows = 128;             // query rows per CTA
 constexpr float kRescaleGap = 8.f;       // lazy rescaling threshold (natural log units)
-constexpr int kAtKeys = 64;              // keys per tile
+constexpr int kAtKeys = 128;             // keys per tile
 constexpr int kAtD = 128;
 constexpr int kPartStride = kAtD + 4;    // workspace row: O (128), m, l, 2 pad (528 B, 16-B aligned)
 constexpr int kAtMaxNodes = 128;         // tree nodes per sequence on this kernel
-constexpr uint32_t kAtTmemCols = 256;    // S / P buffers: cols 0-63, 192-255; O: cols 64-191
-constexpr int kAtOffQ = 0;               // [2 d halves][128 rows][128 B]     32 KiB
-constexpr int kAtOffK = 32768;           // 2 x [2 d halves][64 keys][128 B]  2 x 16 KiB
-constexpr int kAtOffV = 65536;           // 2 x [2 d atoms][64 keys][128 B]   2 x 16 KiB
-constexpr int kAtOffMask = 98304;        // [kAtMaxNodes][2] uint64          2 KiB
+constexpr uint32_t kAtTmemCols = 512;    // S / P buffers: cols 0-127, 256-383; O: cols 128-255
+constexpr int kAtTileBytes = kAtKeys * 128;  // one d half (or atom) of a key or value tile
+constexpr int kAtOffQ = 0;               // [2 d halves][128 rows][128 B]      32 KiB
+constexpr int kAtOffK = 32768;           // 2 x [2 d halves][128 keys][128 B]  2 x 32 KiB
+constexpr int kAtOffV = 98304;           // 2 x [2 d atoms][128 keys][128 B]   2 x 32 KiB
+constexpr int kAtOffMask = 163840;       // [kAtMaxNodes][2] uint64           2 KiB
 constexpr int kAtOffStat = kAtOffMask + kAtMaxNodes * 16;  // [2 tiles][2][128] row max, [2][128] sum
 constexpr int kAtOffBar = kAtOffStat + 6 * kAtRows * 4;
 constexpr int kAtSmemBytes = kAtOffBar + 128 + 1024;
@@ -77,7 +81,7 @@ struct AtArgs {
   __nv_bfloat16* o;
 };
 
-__global__ void __launch_bounds__(kAtBlock, 2)  // two CTAs per SM: <= 112 registers
+__global__ void __launch_bounds__(kAtBlock, 1)
 tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
                  const __grid_constant__ CUtensorMap ktmap,
                  const __grid_constant__ CUtensorMap vtmap,
@@ -153,8 +157,8 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tO = tmem + 64;
-  auto tS_of = [&](int u) -> uint32_t { return tmem + ((u & 1) ? 192u : 0u); };
+  const uint32_t tO = tmem + 128;
+  auto tS_of = [&](int u) -> uint32_t { return tmem + ((u & 1) ? 256u : 0u); };
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
   volatile int* abort = s_abort;
 
@@ -191,9 +195,9 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
       tma_load_3d(smem + kAtOffQ, &qmap, bar, 0, hk * a.G, lo + node0);
       tma_load_3d(smem + kAtOffQ + 16384, &qmap, bar, 64, hk * a.G, lo + node0);
     }
-    uint8_t* kdst = smem + kAtOffK + (u & 1) * 16384;
+    uint8_t* kdst = smem + kAtOffK + (u & 1) * (2 * kAtTileBytes);
     tma_load_3d(kdst, km, bar, 0, hk, r);
-    tma_load_3d(kdst + 8192, km, bar, 64, hk, r);
+    tma_load_3d(kdst + kAtTileBytes, km, bar, 64, hk, r);
     k_issued[u & 1] += 1;
   };
   auto issue_v = [&](int u) {  // value tile u into value buffer u & 1
@@ -201,9 +205,9 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
     const int r = tile_row(u, km, vm);
     uint64_t* bar = &vbar[u & 1];
     mbar_arrive_expect_tx(bar, 2 * kAtKeys * 128);
-    uint8_t* vdst = smem + kAtOffV + (u & 1) * 16384;
+    uint8_t* vdst = smem + kAtOffV + (u & 1) * (2 * kAtTileBytes);
     tma_load_3d(vdst, vm, bar, 0, hk, r);
-    tma_load_3d(vdst + 8192, vm, bar, 64, hk, r);
+    tma_load_3d(vdst + kAtTileBytes, vm, bar, 64, hk, r);
     v_issued[u & 1] += 1;
   };
   // S = Q K^T of tile u into score buffer u & 1 (once its key tile has landed)
@@ -211,26 +215,33 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
     if (!mbar_wait_suspend(&kbar[u & 1], (u >> 1) & 1, abort)) return false;
     tc_fence_after_sync();
     const uint32_t sQ = smem_addr(smem + kAtOffQ);
-    const uint32_t sK = smem_addr(smem + kAtOffK + (u & 1) * 16384);
+    const uint32_t sK = smem_addr(smem + kAtOffK + (u & 1) * (2 * kAtTileBytes));
     constexpr uint32_t id_s = idesc_bf16_f32(128, kAtKeys, 0, 0);
 #pragma unroll
     for (int s = 0; s < kAtD / 16; ++s) {
       const uint64_t ad = smem_desc(sQ + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024, kSwizzle128B);
-      const uint64_t bd = smem_desc(sK + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024, kSwizzle128B);
+      const uint64_t bd =
+          smem_desc(sK + (s >> 2) * kAtTileBytes + (s & 3) * 32, 16, 1024, kSwizzle128B);
       umma_bf16(tS_of(u), ad, bd, id_s, s > 0);
     }
     umma_commit(&sbar[u & 1]);
     s_issued[u & 1] += 1;
     return true;
   };
-  // this thread's 32 raw scores q.k of tile u (keys kh * 32 ..), masked to -inf
+  // this thread's 64 raw scores q.k of tile u (keys kh * 64 ..), masked to -inf
   // (the softmax scale enters with the exponent; only a partial context tile, a
   // row past the tree or a tree tile needs the mask)
   constexpr int kHalf = kAtKeys / 2;
   auto read_logits = [&](int u, float (&x)[kHalf]) {
     const int t = tile_of(u);
-    tmem_ld32(tS_of(u) + lane_base + kh * kHalf, x);
-    tmem_ld_wait();
+#pragma unroll
+    for (int q = 0; q < kHalf / 32; ++q) {
+      float y[32];
+      tmem_ld32(tS_of(u) + lane_base + kh * kHalf + q * 32, y);
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < 32; ++c) x[q * 32 + c] = y[c];
+    }
     if (t < nt_pre) {
       const int lim = P - t * kAtKeys - kh * kHalf;  // keys below lim are cached context
       if (lim < kHalf || !row_live) {
@@ -280,12 +291,12 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
         if (ok) ok = mbar_wait_suspend(&vbar[u & 1], ph, abort);
         if (ok) {  // O += P V: A = P from TMEM (16 keys = 8 columns per step)
           tc_fence_after_sync();
-          const uint32_t sV = smem_addr(smem + kAtOffV + (u & 1) * 16384);
+          const uint32_t sV = smem_addr(smem + kAtOffV + (u & 1) * (2 * kAtTileBytes));
           constexpr uint32_t id_o = idesc_bf16_f32(128, 128, 0, 1);
 #pragma unroll
           for (int s = 0; s < kAtKeys / 16; ++s) {
-            // MN-major V: the two 64-column atoms 8 KiB apart, 8-key groups 1 KiB apart
-            const uint64_t bd = smem_desc(sV + s * 2048, 8192, 1024, kSwizzle128B);
+            // MN-major V: the two 64-column atoms one tile half apart, 8-key groups 1 KiB apart
+            const uint64_t bd = smem_desc(sV + s * 2048, kAtTileBytes, 1024, kSwizzle128B);
             umma_bf16_tmem_a(tO, tS_of(u) + s * 8, bd, id_o, (u > 0 || s > 0) ? 1u : 0u);
           }
           umma_commit(&pvbar[u & 1]);
@@ -368,7 +379,13 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
         pw[i] = *reinterpret_cast<const uint32_t*>(&pp);
       }
       lsum += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-      tmem_st16(tS_of(u) + lane_base + kh * (kHalf / 2), pw);
+#pragma unroll
+      for (int q = 0; q < kHalf / 32; ++q) {
+        uint32_t w16[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) w16[c] = pw[q * 16 + c];
+        tmem_st16(tS_of(u) + lane_base + kh * (kHalf / 2) + q * 16, w16);
+      }
       tmem_st_wait();
       tc_fence_before_sync();
       __syncwarp();
@@ -511,17 +528,17 @@ static int at_sm_count() {
   return n;
 }
 
-// Context splits for this launch: enough CTAs for two per SM, at most 8, and at
+// Context splits for this launch: enough CTAs for one per SM, at most 8, and at
 // least 16 key tiles (1024 cached positions) per split, below which the merge costs
 // more than the split saves.
 static int attn_splits(const tgdn_tree& t, int H_q, int H_kv, int P_max) {
   const int G = H_q / H_kv;
   const long items = (long)t.B * H_kv * ((t.n_max * G + kAtRows - 1) / kAtRows);
   if (items <= 0) return 1;
-  long s = (2L * at_sm_count()) / items;
+  long s = (long)at_sm_count() / items;
   const long ctx_tiles = (P_max + kAtKeys - 1) / kAtKeys;
   if (s > 8) s = 8;
-  if (s > ctx_tiles / 16) s = ctx_tiles / 16;
+  if (s > ctx_tiles / (1024 / kAtKeys)) s = ctx_tiles / (1024 / kAtKeys);
   return s < 1 ? 1 : (int)s;
 }
 
@@ -573,7 +590,7 @@ cudaError_t launch_tree_attn(const tgdn_tree& t, int H_q, int H_kv, int P_max, f
   cudaError_t e = cudaFuncSetAttribute(tree_attn_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kAtSmemBytes);
   if (e != cudaSuccess) return e;
-  // the whole unified L1 / shared memory as shared memory: two CTAs per SM
+  // the whole unified L1 / shared memory as shared memory
   e = cudaFuncSetAttribute(tree_attn_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                            (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
