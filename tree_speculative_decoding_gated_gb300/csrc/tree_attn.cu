@@ -529,8 +529,8 @@ static int at_sm_count() {
 }
 
 // Context splits for this launch: enough CTAs for one per SM, at most 8, and at
-// least 16 key tiles (1024 cached positions) per split, below which the merge costs
-// more than the split saves.
+// least 1024 cached positions per split, below which the merge costs more than the
+// split saves.
 static int attn_splits(const tgdn_tree& t, int H_q, int H_kv, int P_max) {
   const int G = H_q / H_kv;
   const long items = (long)t.B * H_kv * ((t.n_max * G + kAtRows - 1) / kAtRows);
