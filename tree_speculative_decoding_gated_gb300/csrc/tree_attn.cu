@@ -11,8 +11,9 @@
 // two per row (= TMEM lane), each taking half of every key tile and half of the
 // output columns; the halves of a row's maximum are exchanged per tile between
 // the two warps that hold the row, and its normaliser merged once at the end.
-// A ninth warp owns no rows: its lane 0 issues every copy and product, so the
-// softmax warps never wait for an issuing thread among them.  One CTA per SM
+// Two more warps own no rows: lane 0 of one issues every tensor-core product,
+// lane 0 of the other every copy, so the softmax warps never wait for an issuing
+// thread among them and the products do not wait behind the copies.  One CTA per SM
 // (the 512 TMEM columns: two 128-column score buffers and the 128-column O).
 //
 // Keys come in tiles of 128: first the cached context (prefix_len[b] positions),
@@ -45,8 +46,9 @@
 namespace tgdn {
 
 constexpr int kAtThreads = 256;          // softmax threads: two per query row
-constexpr int kAtIssueWarp = kAtThreads / 32;  // the warp that issues every copy and product
-constexpr int kAtBlock = kAtThreads + 32;
+constexpr int kAtIssueWarp = kAtThreads / 32;  // the warp that issues every product
+constexpr int kAtCopyWarp = kAtIssueWarp + 1;  // the warp that issues every copy
+constexpr int kAtBlock = kAtThreads + 64;
 constexpr int kAtRows = 128;             // query rows per CTA
 constexpr float kRescaleGap = 8.f;       // lazy rescaling threshold (natural log units)
 constexpr int kAtKeys = 128;             // keys per tile
@@ -266,26 +268,36 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   const float c2 = a.scale * 1.4426950408889634f;
   const float gap_raw = kRescaleGap / a.scale;
   float lsum = 0.f;     // this thread's half of the row's sum of exp(logit - m)
-  if (warp == kAtIssueWarp) {
-    // ---- the issuing warp: S(u + 1) is issued while the softmax warps form P of
-    // tile u, then O += P V of tile u once every softmax warp has stored its P
+  if (warp == kAtCopyWarp) {
+    // ---- the copy warp: key tile u + 2 into key buffer u & 1 once S(u) is done,
+    // value tile u + 2 into value buffer u & 1 once P V of tile u is done
     if (lane == 0 && nt > 0) {
       issue_k(0);
       issue_v(0);
-      if (nt > 1) issue_k(1);
+      if (nt > 1) {
+        issue_k(1);
+        issue_v(1);
+      }
+      for (int u = 0; ok && u + 2 < nt; ++u) {
+        const uint32_t ph = (u >> 1) & 1;
+        ok = mbar_wait_suspend(&sbar[u & 1], ph, abort);
+        if (ok) issue_k(u + 2);
+        if (ok) ok = mbar_wait_suspend(&pvbar[u & 1], ph, abort);
+        if (ok) issue_v(u + 2);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kAtIssueWarp) {
+    // ---- the product warp: S(u + 1) is issued while the softmax warps form P of
+    // tile u, then O += P V of tile u once every softmax warp has stored its P
+    if (lane == 0 && nt > 0) {
       ok = score(0);
       for (int u = 0; ok && u < nt; ++u) {
         const uint32_t ph = (u >> 1) & 1;
         if (u + 1 < nt) {
-          // P V of tile u - 1 is done: score buffer (u + 1) & 1 and value buffer
-          // (u + 1) & 1 are free
+          // P V of tile u - 1 is done: score buffer (u + 1) & 1 is free
           if (u > 0) ok = mbar_wait_suspend(&pvbar[(u - 1) & 1], ((u - 1) >> 1) & 1, abort);
-          if (ok) issue_v(u + 1);
           if (ok) ok = score(u + 1);
-        }
-        if (ok && u + 2 < nt) {  // S(u) is done: key buffer u & 1 is free
-          ok = mbar_wait_suspend(&sbar[u & 1], ph, abort);
-          if (ok) issue_k(u + 2);
         }
         if (ok) ok = mbar_wait_suspend(&pready[u & 1], ph, abort);
         if (ok) ok = mbar_wait_suspend(&vbar[u & 1], ph, abort);
