@@ -545,35 +545,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     for (int j = 0; item < i_end; ++j, item += i_step) {
       const int slot = j & 1;
       ItemMeta& M = sh.meta[slot];
-      // the consumer has finished item j-2, the previous user of this half and slot
-      // (every wait is agreed on by the whole group before anyone leaves the loop)
-      if (j >= 2 && !group_wait(&sh.tmem_free[slot], ((j >> 1) + 1) & 1, kBarP, p == 0, abort))
-        break;
       const int bi = item / H_v, h = item % H_v;
       const int lo = pf.lo, N = pf.N;
       const int next = item + i_step;
-      bool ok = (pf.st == TGDN_SEQ_OK) && N > 0 && N <= kTcNodes;
-      // (small_only: sequences above 64 nodes belong to the 128-node kernel; their
-      // items pass through without state, solve or writes)
-      const bool skip = small_only && N > kTcNodes;
-      uint64_t my_anc = 0;
-      if (p == 0) {
-        M.lo = lo;
-        M.N = N;
-        M.h = h;
-        M.skip = skip;
-      }
-      if (ok && p < N) {
-        const bool v_ok = pf.dep >= 0 && pf.dep <= depth_max && pf.dep <= kTcDepth &&
-                          pf.pos >= 0 && pf.pos < N && pf.ord >= 0 && pf.ord < N;
-        ok = v_ok;
-        M.dep[p] = pf.dep;
-        M.pos[p] = pf.pos;
-        M.ord[p] = pf.ord;
-        M.gg[p] = pf.gg;
-        M.bb[p] = pf.bb;
-        if (v_ok) my_anc = anc[(size_t)(lo + pf.pos) * words];  // positions < 64: word 0
-      }
       if (fused) {
         // the previous step's commit: S = e^{G*} S + sum_l e^{G*-G_l} k_l u_l^T,
         // written back in place; the committed state is what gets verified
@@ -644,6 +618,33 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
           for (int r = 0; r < 16; ++r)
             reinterpret_cast<float4*>(dst + (size_t)(srow0 + r) * kTcDV)[sq] = sreg[r];
         }
+      }
+      // the consumer has finished item j-2, the previous user of this half and slot
+      // (every wait is agreed on by the whole group before anyone leaves the loop);
+      // the commit above touches neither, so it runs while the consumer finishes
+      if (j >= 2 && !group_wait(&sh.tmem_free[slot], ((j >> 1) + 1) & 1, kBarP, p == 0, abort))
+        break;
+      bool ok = (pf.st == TGDN_SEQ_OK) && N > 0 && N <= kTcNodes;
+      // (small_only: sequences above 64 nodes belong to the 128-node kernel; their
+      // items pass through without state, solve or writes)
+      const bool skip = small_only && N > kTcNodes;
+      uint64_t my_anc = 0;
+      if (p == 0) {
+        M.lo = lo;
+        M.N = N;
+        M.h = h;
+        M.skip = skip;
+      }
+      if (ok && p < N) {
+        const bool v_ok = pf.dep >= 0 && pf.dep <= depth_max && pf.dep <= kTcDepth &&
+                          pf.pos >= 0 && pf.pos < N && pf.ord >= 0 && pf.ord < N;
+        ok = v_ok;
+        M.dep[p] = pf.dep;
+        M.pos[p] = pf.pos;
+        M.ord[p] = pf.ord;
+        M.gg[p] = pf.gg;
+        M.bb[p] = pf.bb;
+        if (v_ok) my_anc = anc[(size_t)(lo + pf.pos) * words];  // positions < 64: word 0
       }
       // Without a pending commit the same hand-over happens here.
       bool step_ok = true;
