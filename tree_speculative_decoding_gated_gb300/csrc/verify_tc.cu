@@ -718,10 +718,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       }
       // the next item's state while this one is finished
       if (next < i_end && !(small_only && pf.N > kTcNodes)) load_s0(next);
-      ok = named_sync_and(kBarP, kGroup, ok);
       // root paths from the ancestor masks (bits = topological positions,
       // ascending = root first) and path-cumulative log-gates; the same tree as
-      // the previous item (another head) reuses its paths and only sums the gates
+      // the previous item (another head) reuses its paths and only sums the gates.
+      // This runs while the first product is being issued, before the group has
+      // agreed that every node's metadata is valid, so a node index read from
+      // another thread's metadata is range-checked before it is used.
       const bool reuse = prev_bi == bi;
       if (ok && p < N && reuse) {
         const int dn = M.dep[p];
@@ -750,6 +752,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             break;
           }
           const int s = M.ord[b];
+          if (s < 0 || s >= N) {
+            pk = false;
+            break;
+          }
           pk = M.dep[s] == i;
           prow[i] = static_cast<uint8_t>(s);
           acc += M.gg[s];
