@@ -172,3 +172,43 @@ def test_verify_fused_rejects_bad_arguments(L):
              None) == tgdn.EINVAL                                   # no previous tree
     assert f(ctypes.byref(t), ctypes.byref(d), *([FAKE] * 7), ws, ctypes.byref(pt), None,
              FAKE, FAKE, pws, None) == tgdn.EINVAL                  # no accepted nodes
+
+
+def test_tree_attention_rejects_bad_arguments(L):
+    """Host checks of tgdn_tree_attention: head counts, context length, the softmax scale
+    (positive and finite), the supported shapes and 16-byte alignment are checked before
+    anything is launched."""
+    t = ctree(B=2, T=10, n_max=8)
+    f = L.tgdn_tree_attention
+
+    def call(tree=t, H_q=8, H_kv=2, d=128, P_max=16, scale=0.088, q=FAKE):
+        return f(ctypes.byref(tree), H_q, H_kv, d, q, FAKE, FAKE, FAKE, FAKE, FAKE, P_max,
+                 scale, FAKE, None, 0, None)
+
+    assert call(H_q=0) == tgdn.EINVAL
+    assert call(H_kv=3) == tgdn.EINVAL                  # 8 query heads over 3 kv heads
+    assert call(P_max=-1) == tgdn.EINVAL
+    for bad in (0.0, -0.5, float("nan"), float("inf"), -float("inf")):
+        assert call(scale=bad) == tgdn.EINVAL, bad
+    assert call(d=64) == tgdn.EUNSUPPORTED              # head size other than 128
+    assert call(H_q=32, H_kv=1) == tgdn.EUNSUPPORTED    # 32 query heads per kv head
+    assert call(tree=ctree(B=2, T=300, n_max=129)) == tgdn.EUNSUPPORTED
+    assert call(q=FAKE + 2) == tgdn.EINVAL              # misaligned query rows
+
+
+def test_tree_build_rejects_bad_arguments(L):
+    """Host checks of tgdn_tree_build: sizes must be positive and within the library's
+    bounds, and no pointer may be null (nothing is launched)."""
+    f = L.tgdn_tree_build
+
+    def call(B=2, budget=16, K=4, w=2, depth_max=8, root=FAKE):
+        return f(B, budget, K, w, depth_max, root, *([FAKE] * 8), None)
+
+    assert call(budget=0) == tgdn.EINVAL
+    assert call(K=0) == tgdn.EINVAL
+    assert call(w=0) == tgdn.EINVAL
+    assert call(depth_max=-1) == tgdn.EINVAL
+    assert call(B=-1) == tgdn.EINVAL
+    assert call(budget=1 << 20) == tgdn.ETOOBIG
+    assert call(root=None) == tgdn.EINVAL
+    assert call(B=0, root=None) == tgdn.OK               # an empty batch is a no-op
