@@ -52,7 +52,9 @@
 // their own) and forms
 //   S = e^{G*} S_prev + sum_{s on the path} e^{G*-G_s} k_s u_s^T
 // in registers, writes it back in place (the committed state) and verifies
-// from it.  The state then crosses HBM once in each direction per step.
+// from it.  The state then crosses HBM once in each direction per step.  The
+// commit touches neither the TMEM half nor the metadata slot of its item, so
+// the producer does it before it waits for the consumer to free them.
 #include "tgdn_device.cuh"
 #include "tgdn_kernels.h"
 
