@@ -288,7 +288,8 @@ def tree_attention(tree: Tree, q, k_tree, v_tree, k_cache, v_cache, prefix_len, 
                    scale: float, ws=None, stream=None) -> None:
     """tgdn_tree_attention: each node attends to its sequence's cached context and its
     own root path.  q/o [T][H_q][d], k_tree/v_tree [T][H_kv][d], k_cache/v_cache
-    [B][P_max][H_kv][d] (bf16), prefix_len [B] int32.  ws: optional uint8 workspace of
+    [B][P_max][H_kv][d] (bf16), prefix_len [B] int32; scale positive and finite (the
+    logits are scale * q.k).  ws: optional uint8 workspace of
     tree_attention_workspace_bytes() bytes (splits the cached context over more CTAs)."""
     T, B = tree.T, tree.B
     H_q, d = q.shape[1], q.shape[2]
