@@ -64,8 +64,9 @@ typedef enum {
   TGDN_EUNSUPPORTED = -5  /* a valid combination this build does not run */
 } tgdn_status;
 
-/* Per-sequence status words written by tgdn_tree_prep (values 1-5) and by
- * the other calls (value 6).  The first failing check, in this order, wins. */
+/* Per-sequence status words written by tgdn_tree_prep (values 1-5 and 7) and
+ * by the other calls (value 6).  tgdn_tree_prep checks the row range first
+ * (value 7), then the values 1-5 in this order; the first failing check wins. */
 typedef enum {
   TGDN_SEQ_OK = 0,
   TGDN_SEQ_TOO_BIG = 1,     /* N_b > n_max */
@@ -73,8 +74,11 @@ typedef enum {
   TGDN_SEQ_ROOTS = 3,       /* N_b > 0 and not exactly one root */
   TGDN_SEQ_CYCLE = 4,       /* some node never reaches the root */
   TGDN_SEQ_TOO_DEEP = 5,    /* some depth > depth_max */
-  TGDN_SEQ_TIMEOUT = 6      /* a bounded device wait expired; outputs of the
+  TGDN_SEQ_TIMEOUT = 6,     /* a bounded device wait expired; outputs of the
                                sequence are unspecified */
+  TGDN_SEQ_BAD_RANGE = 7    /* cu_nodes[b] < 0, cu_nodes[b+1] < cu_nodes[b] or
+                               cu_nodes[b+1] > T: no call reads or writes any row
+                               of the sequence (only status[b] is written) */
 } tgdn_seq_status;
 
 /* Element type of q, k, v and o.  g, b, S0, the state and the workspace are
@@ -88,7 +92,10 @@ typedef enum { TGDN_F32 = 0, TGDN_BF16 = 1 } tgdn_dtype;
 
 /* A batch of draft trees and the metadata tgdn_tree_prep derives from it.
  *   B          number of sequences (>= 0)
- *   T          total nodes, = cu_nodes[B] (host copy, used for bounds only)
+ *   T          total rows of every [T]-leading array (host copy): tree prep
+ *              gives a sequence whose row range leaves [0, T) the status
+ *              TGDN_SEQ_BAD_RANGE, so a bad cu_nodes never makes a call touch
+ *              rows outside the arrays
  *   n_max      caller's bound on nodes per sequence, 1 .. TGDN_MAX_NODES
  *   depth_max  caller's bound on depth, 0 .. TGDN_MAX_DEPTH
  *   words      64-bit words per ancestor mask, must equal ceil(n_max / 64)
@@ -103,7 +110,10 @@ typedef enum { TGDN_F32 = 0, TGDN_BF16 = 1 } tgdn_dtype;
  *              for every s on the root path of n, n included
  *   status     [B] int32, tgdn_seq_status
  * For a sequence whose status is not TGDN_SEQ_OK, depth/order/pos are -1 and
- * anc rows are 0. */
+ * anc rows are 0, except under TGDN_SEQ_BAD_RANGE, where none of its rows is
+ * written.  Every other call skips a sequence whose status is not TGDN_SEQ_OK
+ * (zero outputs, state kept) and never touches the rows of one with
+ * TGDN_SEQ_BAD_RANGE. */
 typedef struct {
   int32_t B, T, n_max, depth_max, words;
   const int32_t* cu_nodes;

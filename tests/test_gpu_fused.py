@@ -91,8 +91,11 @@ def check_decode(problems, S0, n_max=None):
             es = rel_fro_blocks(fv[s], ref_S[s - 1])
             print(f"step {s}: fused committed state={es:.3e}")
             assert es <= TOL_BF16, (s, es)
-            # the fused pass computes the commit with the same operations as the separate one
-            np.testing.assert_allclose(fv[s], sv[s], rtol=1e-5, atol=1e-7)
+            # the fused pass commits with the same arithmetic as the separate one, in
+            # another order; the state then enters the next products as bf16, where a
+            # one-ulp difference can flip a rounding, so the two agree to well below the
+            # tolerance but not bit for bit
+            assert rel_fro_blocks(fv[s], sv[s]) <= 1e-4
         np.testing.assert_allclose(fo[s], so[s], rtol=2e-2, atol=1e-2)
     assert rel_fro_blocks(fS, ref_S[-1]) <= TOL_BF16
     return fo, fv, fS

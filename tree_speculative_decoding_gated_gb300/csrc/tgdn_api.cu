@@ -78,6 +78,30 @@ bool encode_rows_map(CUtensorMap* map, const void* base, long rows, int H, int b
 
 }  // namespace
 
+namespace tgdn {
+
+bool encode_out_maps(OutMaps* m, float* U, void* o, int T, int H_v) {
+  auto fn = encode_fn();
+  if (!fn || T < 1) return false;
+  const cuuint64_t dims[3] = {128, (cuuint64_t)H_v, (cuuint64_t)T};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const cuuint64_t su[2] = {128 * 4, (cuuint64_t)H_v * 128 * 4};
+  const cuuint64_t so[2] = {128 * 2, (cuuint64_t)H_v * 128 * 2};
+  auto enc = [&](CUtensorMap* map, CUtensorMapDataType ty, void* base, const cuuint64_t* str,
+                 cuuint32_t inner, cuuint32_t rows) {
+    const cuuint32_t box[3] = {inner, 1, rows};
+    return fn(map, ty, 3, base, dims, str, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  return enc(&m->u64, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, U, su, 32, 64) &&
+         enc(&m->u8, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, U, su, 32, 8) &&
+         enc(&m->o64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, o, so, 64, 64) &&
+         enc(&m->o8, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, o, so, 64, 8);
+}
+
+}  // namespace tgdn
+
 extern "C" {
 
 int tgdn_version(void) { return 100; }
@@ -123,23 +147,27 @@ int tgdn_verify(const tgdn_tree* tree, const tgdn_dims* dims, const void* q, con
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (tgdn::verify_tc_supported(t, d, q, k, v, S0, o)) {
     CUtensorMap qmap, kmap, vmap;
+    tgdn::OutMaps om;
     if (!encode_qk_map(&qmap, q, t.T, d.H_qk) || !encode_qk_map(&kmap, k, t.T, d.H_qk) ||
-        !encode_rows_map(&vmap, v, t.T, d.H_v, 1, 64))
-      return TGDN_ECUDA;  // the driver could not describe q/k/v for TMA
+        !encode_rows_map(&vmap, v, t.T, d.H_v, 1, 64) ||
+        !tgdn::encode_out_maps(&om, U, o, t.T, d.H_v))
+      return TGDN_ECUDA;  // the driver could not describe q/k/v/U/o for TMA
     const tgdn::PendingCommit none{};
-    return from_cuda(tgdn::launch_verify_tc(t, d, qmap, kmap, vmap, g, b, const_cast<float*>(S0),
-                                            o, U, G, none, false, s));
+    return from_cuda(tgdn::launch_verify_tc(t, d, qmap, kmap, vmap, om, g, b,
+                                            const_cast<float*>(S0), o, U, G, none, false, s));
   }
   if (tgdn::verify_tc128_supported(t, d, q, k, v, S0, o)) {
     CUtensorMap qmap, kmap, vmap;
+    tgdn::OutMaps om;
     if (!encode_qk_map(&qmap, q, t.T, d.H_qk) || !encode_qk_map(&kmap, k, t.T, d.H_qk) ||
-        !encode_rows_map(&vmap, v, t.T, d.H_v, 1, 64))
+        !encode_rows_map(&vmap, v, t.T, d.H_v, 1, 64) ||
+        !tgdn::encode_out_maps(&om, U, o, t.T, d.H_v))
       return TGDN_ECUDA;
     // sequences of at most 64 nodes on the 64-node kernel (two items in flight per SM),
     // the larger ones on the 128-node kernel; each kernel passes over the other's
     const tgdn::PendingCommit none{};
-    rc = from_cuda(tgdn::launch_verify_tc(t, d, qmap, kmap, vmap, g, b, const_cast<float*>(S0),
-                                          o, U, G, none, true, s));
+    rc = from_cuda(tgdn::launch_verify_tc(t, d, qmap, kmap, vmap, om, g, b,
+                                          const_cast<float*>(S0), o, U, G, none, true, s));
     if (rc != TGDN_OK) return rc;
     rc = from_cuda(
         tgdn::launch_verify_tc128(t, d, qmap, kmap, q, k, v, g, b, S0, o, U, G, true, s));
@@ -189,15 +217,18 @@ int tgdn_verify_fused(const tgdn_tree* tree, const tgdn_dims* dims, const void* 
                              : nullptr;
   if (t.T > 0 && pt.T > 0 && tgdn::verify_tc_supported(t, d, q, k, v, S, o) &&
       tgdn::pending_commit_tc_supported(pt, prev_k)) {
-    CUtensorMap qmap, kmap, vmap;
-    if (!encode_qk_map(&qmap, q, t.T, d.H_qk) || !encode_qk_map(&kmap, k, t.T, d.H_qk) ||
-        !encode_rows_map(&vmap, v, t.T, d.H_v, 1, 64))
-      return TGDN_ECUDA;
     float* U = reinterpret_cast<float*>(static_cast<char*>(ws) + L.u_off);
     float* G = reinterpret_cast<float*>(static_cast<char*>(ws) + L.g_off);
+    CUtensorMap qmap, kmap, vmap;
+    tgdn::OutMaps om;
+    if (!encode_qk_map(&qmap, q, t.T, d.H_qk) || !encode_qk_map(&kmap, k, t.T, d.H_qk) ||
+        !encode_rows_map(&vmap, v, t.T, d.H_v, 1, 64) ||
+        !tgdn::encode_out_maps(&om, U, o, t.T, d.H_v))
+      return TGDN_ECUDA;
     const tgdn::PendingCommit cm{pt.cu_nodes, pt.status, prev_path, pt.depth_max + 1,
                                  prev_k,      pU,        pG};
-    return from_cuda(tgdn::launch_verify_tc(t, d, qmap, kmap, vmap, g, b, S, o, U, G, cm, false, s));
+    return from_cuda(
+        tgdn::launch_verify_tc(t, d, qmap, kmap, vmap, om, g, b, S, o, U, G, cm, false, s));
   }
   // any other case: the commit as its own pass, then the verify
   if (pt.T > 0) {

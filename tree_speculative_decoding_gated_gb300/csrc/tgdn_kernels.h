@@ -65,15 +65,23 @@ cudaError_t launch_verify_tc128(const tgdn_tree& t, const tgdn_dims& d, const CU
                                 const void* v, const float* g,
                                 const float* b, const float* S0, void* o, float* U, float* G,
                                 bool big_only, cudaStream_t s);
+// Tensor maps of the verify outputs for TMA stores (128-byte swizzle): the factors
+// U [T][H_v][128] fp32 with boxes {32, 1, 64} and {32, 1, 8}, the outputs o
+// [T][H_v][128] bf16 with boxes {64, 1, 64} and {64, 1, 8}.
+struct OutMaps {
+  CUtensorMap u64, u8, o64, o8;
+};
+bool encode_out_maps(OutMaps* m, float* U, void* o, int T, int H_v);
 // Whether the tensor-core verify can also apply a pending commit of `prev`.
 bool pending_commit_tc_supported(const tgdn_tree& prev, const void* prev_k);
 // With cm.path set, S is first updated in place by the pending commit and the
 // committed state is verified; otherwise S is only read.  small_only (no pending
 // commit): only the sequences of at most 64 nodes are verified, the rest untouched.
 cudaError_t launch_verify_tc(const tgdn_tree& t, const tgdn_dims& d, const CUtensorMap& qmap,
-                             const CUtensorMap& kmap, const CUtensorMap& vmap, const float* g,
-                             const float* b, float* S, void* o, float* U, float* G,
-                             const PendingCommit& cm, bool small_only, cudaStream_t s);
+                             const CUtensorMap& kmap, const CUtensorMap& vmap,
+                             const OutMaps& om, const float* g, const float* b, float* S,
+                             void* o, float* U, float* G, const PendingCommit& cm,
+                             bool small_only, cudaStream_t s);
 
 // Per-branch recurrent verification (every root-to-leaf path replayed from S0).
 cudaError_t launch_verify_recurrent(const tgdn_tree& t, const tgdn_dims& d, const void* q,

@@ -15,7 +15,7 @@ constexpr int kTreeWarps = 4;
 constexpr unsigned kFull = 0xffffffffu;
 
 __global__ void __launch_bounds__(kTreeWarps * 32)
-tree_prep_kernel(int B, const int32_t* __restrict__ cu, const int32_t* __restrict__ parent,
+tree_prep_kernel(int B, int T, const int32_t* __restrict__ cu, const int32_t* __restrict__ parent,
                  int n_max, int depth_max, int words, int32_t* __restrict__ depth,
                  int32_t* __restrict__ order, int32_t* __restrict__ pos,
                  uint64_t* __restrict__ anc, int32_t* __restrict__ status) {
@@ -28,7 +28,13 @@ tree_prep_kernel(int B, const int32_t* __restrict__ cu, const int32_t* __restric
   int* par = s_par[warp];
   int* dep = s_dep[warp];
   int* ps = s_pos[warp];
-  const int lo = cu[b], N = cu[b + 1] - lo;
+  const int lo = cu[b], hi = cu[b + 1];
+  // A row range outside [0, T) is reported and nothing of the sequence is touched.
+  if (lo < 0 || hi < lo || hi > T) {
+    if (lane == 0) status[b] = TGDN_SEQ_BAD_RANGE;
+    return;
+  }
+  const int N = hi - lo;
 
   int st = TGDN_SEQ_OK;
   if (N > n_max) st = TGDN_SEQ_TOO_BIG;
@@ -167,7 +173,7 @@ accept_kernel(int B, const int32_t* __restrict__ cu, const int32_t* __restrict__
 cudaError_t launch_tree_prep(const tgdn_tree& t, cudaStream_t s) {
   if (t.B == 0) return cudaSuccess;
   const int grid = (t.B + kTreeWarps - 1) / kTreeWarps;
-  tree_prep_kernel<<<grid, kTreeWarps * 32, 0, s>>>(t.B, t.cu_nodes, t.parent, t.n_max,
+  tree_prep_kernel<<<grid, kTreeWarps * 32, 0, s>>>(t.B, t.T, t.cu_nodes, t.parent, t.n_max,
                                                     t.depth_max, t.words, t.depth, t.order,
                                                     t.pos, t.anc, t.status);
   return cudaGetLastError();

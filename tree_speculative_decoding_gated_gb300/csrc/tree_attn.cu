@@ -111,6 +111,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   const int npt = kAtRows / a.G;             // nodes per tile of query rows
   const int node0 = mt * npt;
   if (N <= 0 || node0 >= N) return;          // no rows of this tile exist
+  if (a.status[b] == TGDN_SEQ_BAD_RANGE) return;  // rows outside the arrays: untouched
   const int row = tid & (kAtRows - 1), kh = tid >> 7;  // TMEM lane; key / column half
   const int my_node = node0 + row / a.G, my_g = row % a.G;
   const bool row_live = my_node < N;

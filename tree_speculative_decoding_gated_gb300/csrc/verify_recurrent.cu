@@ -48,11 +48,12 @@ verify_recurrent_kernel(int n_max, int depth_max, int H_qk, int H_v, int dk, int
   const bool jlive = c0 + j < dv;
   const int i0 = warp * kRecRowsPerThread;  // first key row of this thread
   const int lo = cu[bi], N = cu[bi + 1] - lo;
-  if (N <= 0) return;
+  const int st = status[bi];
+  if (N <= 0 || st == TGDN_SEQ_BAD_RANGE) return;  // (a bad row range is never touched)
   const size_t orow_stride = (size_t)H_v * dv;
   T* obase = o + ((size_t)lo * H_v + h) * dv + c0;
 
-  if (status[bi] != TGDN_SEQ_OK || N > n_max) {
+  if (st != TGDN_SEQ_OK || N > n_max) {
     for (int e = tid; e < N * kRecCols; e += kRecThreads) {
       const int n = e / kRecCols, jj = e % kRecCols;
       if (c0 + jj < dv) Io<T>::store(obase + n * orow_stride + jj, 0.f);

@@ -92,8 +92,9 @@ verify_simt_kernel(int n_max, int depth_max, int H_qk, int H_v, int dk, int dv,
     const int c0 = c * kSimtCols;
     const int ncol = min(kSimtCols, dv - c0);
     const int lo = cu[bi], N = cu[bi + 1] - lo;
-    if (N <= 0) return;
-    if (tid == 0) s_bad = (status[bi] != TGDN_SEQ_OK) || (N > n_max);
+    const int st = status[bi];
+    if (N <= 0 || st == TGDN_SEQ_BAD_RANGE) return;  // (a bad row range is never touched)
+    if (tid == 0) s_bad = (st != TGDN_SEQ_OK) || (N > n_max);
     __syncthreads();
 
     auto orow = [&](int n) { return ((size_t)(lo + n) * H_v + h) * dv + c0; };

@@ -17,32 +17,33 @@
 // run per CTA with a pending commit, else dealt round robin); trees have at most
 // 64 nodes and depth at most 30.  Two items are in flight per SM:
 //   producer warps 0-7, item j+1:
-//     tree metadata (prefetched as raw values) -> root paths (reused for the
-//     next head of the same sequence) and path-cumulative gates;
-//     S0 (prefetched into registers; warp w holds rows 16 w .. 16 w + 15) ->
-//     bf16 hi + lo operands (~16-bit products);
-//     TMA of the item's key and query rows -> A = [K; Q] (128-byte swizzle);
-//     the group's last thread issues tcgen05.mma into TMEM half (j+1)&1:
-//        D[:, 0:128] = A (S0_hi + S0_lo),  D[:, 128:192] = A K^T
-//     while the others prefetch the next item and build the paths; the
-//     product's completion is awaited one item later, just before its operands
-//     are overwritten.
+//     S0 (loaded into registers an item ahead; warp w holds rows 16 w .. 16 w + 15)
+//     -> bf16 operand (MN-major, 128-byte swizzle), the next item's rows loaded
+//     into the registers each row frees; TMA of the item's key and query rows
+//     -> A = [K; Q]; then tree metadata (prefetched as raw values) -> root paths
+//     (reused for the next head of the same sequence) and path-cumulative gates.
 //   consumer warps 8-15, item j:
+//     thread 0 issues the first product of every item into TMEM half j & 1,
+//        D[:, 0:128] = A S0,  D[:, 128:192] = A K^T,
+//     once the producer has published the operands (while the previous item's
+//     solve runs when they are ready by then, else at the top of the item);
 //     Gram rows -> shared memory; V rows arrive by TMA in the R lo operand area
 //     and the key-lane warps form R = diag(b)(V - e^G K S0) there in place
 //     (bf16 hi/lo operand) while the query-lane warps substitute along the root
-//     paths with the partial sums in registers (depth <= 16: a node's T and W
-//     rows in one thread; deeper: one row per thread), writing straight into
-//     the [T; W] operand;
+//     paths, one T or W row per thread with the partial sums in registers,
+//     writing straight into the [T; W] operand;
 //     tcgen05.mma: D[:, 128:256] = [T; W] R;
 //     U (workspace) and O = e^G Q S0 + W R (bf16) leave through shared-memory
 //     staging and bulk copies.
-// The halves hand over through mbarriers: "stage 1 done" (the first product's
-// completion plus the producer's metadata) and "TMEM half free".  The kernel
-// is launched with programmatic stream serialization: its prologue may overlap
-// the previous kernel's tail and no input is read before griddepcontrol.wait.
+// The halves hand over through mbarriers: "operands ready" (producer -> the
+// issuing thread), "stage 1 done" (the first product's completion plus the
+// producer's metadata) and "TMEM half free".  The kernel is launched with
+// programmatic stream serialization: its prologue may overlap the previous
+// kernel's tail and no input is read before griddepcontrol.wait.
 // In a launch above 64 nodes it takes only the sequences of at most 64 nodes
 // (small_only) and passes over the others without touching them.
+// The state enters the tensor-core products as bf16 (fp32 accumulation); it is
+// read, updated and written back in fp32.
 //
 // Deferred commit folded into the next verify (Methodik 3, last bullet: the
 // state is committed once the accepted branch is known, in the following
@@ -51,10 +52,9 @@
 // and G_s by 16-byte asynchronous copies, one item ahead, into an area of
 // their own) and forms
 //   S = e^{G*} S_prev + sum_{s on the path} e^{G*-G_s} k_s u_s^T
-// in registers, writes it back in place (the committed state) and verifies
-// from it.  The state then crosses HBM once in each direction per step.  The
-// commit touches neither the TMEM half nor the metadata slot of its item, so
-// the producer does it before it waits for the consumer to free them.
+// in registers, writes it back in place (the committed state) row by row while
+// it builds the operand, and verifies from it.  The state then crosses HBM once
+// in each direction per step.
 #include "tgdn_device.cuh"
 #include "tgdn_kernels.h"
 
@@ -70,35 +70,51 @@ constexpr int kTcDepth = 30;   // depth bound on this kernel
 constexpr int kTcPath = kTcDepth + 1;  // entries of a root path
 constexpr int kPathBytes = 32;         // one root path: a byte per depth, zero past the node
 constexpr uint32_t kTmemCols = 512;    // two halves of 256 columns
-constexpr int kGramCol = 128;          // within a half: Gram rows, then [T; W] R
+constexpr int kGramCol = 128;          // within a half: [K;Q] S0 (0-127), Gram rows (128-191)
+// The 64 columns each half leaves free hold the pending commit's product D^T: value
+// column in the lane, key rows 0-63 at column 192 and rows 64-127 at column 448.
+constexpr uint32_t kCommitCol0 = 192, kCommitCol1 = 448;
 
 // Shared-memory map (bytes from a 1024-byte aligned base).
 constexpr int kOffA = 0;          // [K;Q] operand: [2 d_k halves][128 rows][128 B]      32 KiB
-constexpr int kOffS0hi = 32768;   // S0 operand, MN-major [2 col atoms][16 k-groups][8][128 B]
-constexpr int kOffS0lo = 65536;
-constexpr int kOffGR = 98304;     // Gram rows [128 lanes][64] fp32                        32 KiB
+constexpr int kOffS = 32768;      // S0^T operand (bf16), K-major [2 k halves][128 columns][128 B]
+// While the pending commit is formed the same area holds its operands (path padded to
+// 32 entries): (C U_p)^T hi and lo, MN-major [2 m chunks][4 k groups][8][128 B], and
+// K_p, MN-major [2 n chunks][4 k groups][8][128 B].
+constexpr int kOffCAhi = kOffS;
+constexpr int kOffCAlo = kOffS + 8192;
+constexpr int kOffCB = kOffS + 16384;
+// Pending-commit staging, an area of its own so that the next item's rows are in
+// flight while this item's operands are still being read:
+constexpr int kOffUP = 65536;                         // u_s rows [kTcPath][128] fp32   15.5 KiB
+constexpr int kOffKP = kOffUP + kTcPath * kTcDV * 4;  // k_s rows [kTcPath][128] bf16   7.75 KiB
+constexpr int kOffGP = kOffKP + kTcPath * kTcDK * 2;  // 16-byte chunks holding G_s [kTcPath]
+// Gram rows: K K^T rows [64][kKKStride] fp32 (padded: a column read by lanes that share
+// a row, or a row read at distinct columns, hits distinct banks), then Q K^T rows
+// [64][64] fp32 with the 16-byte chunks of row n rotated by n & 7.
+constexpr int kKKStride = 68;
+constexpr int kOffKK = 90112;
+constexpr int kOffQK = kOffKK + 64 * kKKStride * 4;
 constexpr int kOffRhi = 131072;   // R operand, MN-major [2 col atoms][8 node groups][8][128 B]
 constexpr int kOffRlo = 147456;
 constexpr int kOffA2hi = 163840;  // [T; W] operand, K-major [16 row groups][8][128 B]     16 KiB
 constexpr int kOffA2lo = 180224;
-// Pending-commit staging, an area of its own so that the next item's rows are in
-// flight while this item's operands are still being read:
-constexpr int kOffUP = 196608;                        // u_s rows [kTcPath][128] fp32   15.5 KiB
-constexpr int kOffKP = kOffUP + kTcPath * kTcDV * 4;  // k_s rows [kTcPath][128] bf16   7.75 KiB
-constexpr int kOffGP = kOffKP + kTcPath * kTcDK * 2;  // 16-byte chunks holding G_s [kTcPath]
-constexpr int kOffMeta = (kOffGP + kTcPath * 16 + 127) & ~127;
-// Output staging after the second product (its operand areas are free then):
-constexpr int kOffUst = kOffGR;     // U rows [64][528 B] fp32 (GR and the start of R hi)
-constexpr int kUstRow = 528;        // 512 B + 16: rows 8 apart share banks, no more
-constexpr int kOffOst = kOffA2hi;   // O rows [64][272 B] bf16 (the [T; W] operand area)
-constexpr int kOstRow = 272;
-static_assert(kOffUst + 64 * kUstRow <= kOffRlo, "U staging stays clear of the V rows");
-static_assert(kOffOst + 64 * kOstRow <= kOffUP, "O staging stays in the [T; W] area");
+static_assert(kOffGP + kTcPath * 16 <= kOffKK, "commit staging fits its area");
+static_assert(kOffQK + 64 * 64 * 4 <= kOffRhi, "Gram rows fit their area");
+constexpr int kOffMeta = 196608;
+// Output staging after the second product (its operand areas are free then), in the
+// 128-byte swizzled tile layout of the TMA stores that send it out:
+constexpr int kOffUst = kOffKK;     // U: 4 tiles (32 columns each) [64 rows][128 B] fp32
+constexpr int kOffOst = kOffA2hi;   // O: 2 tiles (64 columns each) [64 rows][128 B] bf16
+static_assert(kOffUst % 1024 == 0 && kOffUst + 4 * 8192 <= kOffRhi,
+              "U staging: 1024-byte aligned tiles in the Gram-row area");
+static_assert(kOffOst + 2 * 8192 <= kOffA2lo, "O staging stays in the [T; W] hi area");
 
 struct alignas(16) ItemMeta {
   uint8_t path[kTcNodes][kPathBytes];  // [node][depth]: the node's ancestor at that depth
   int lo, N, h, good;
-  int skip;  // a sequence above 64 nodes in a mixed launch: nothing to do here
+  int skip;   // a sequence above 64 nodes in a mixed launch: nothing to do here
+  int zrows;  // rows zero-filled when the item is not verified
   int dep[kTcNodes];
   int ord[kTcNodes];
   int pos[kTcNodes];
@@ -109,12 +125,17 @@ struct alignas(16) ItemMeta {
 struct TcShared {
   uint64_t tma_bar, mma1_bar, mma2_bar, v_bar;
   uint64_t s1_done[2];    // consumer waits: first product done + metadata written
+  uint64_t op_ready[2];   // consumer's issuing thread waits: the state operand is written
+  uint64_t cmt_bar;       // producer waits: the commit product is in TMEM
   uint64_t tmem_free[2];  // producer waits: consumer finished the item in this half
   uint32_t tmem_slot;
   int abort;
   int tma_issued;
   int v_issued;
   int mma1_issued;
+  int mma2_issued;
+  int cmt_issued;
+  int op_skip[2];         // the item in this half is passed over (no first product)
   int c_L[2];             // staged path length per item parity (0: nothing to commit)
   int c_row[2][kTcPath];  // previous-step node rows of the staged path
   int c_gi[2][kTcPath];   // index of G_s within its staged 16-byte chunk
@@ -195,24 +216,10 @@ __device__ __forceinline__ void path_update(float (&acc)[N], const uint32_t (&pw
   for (int j = 0; j < W; ++j) acc[j] = fmaf(s, row[path_at(pw, j) ^ x], acc[j]);
 }
 
-// The same for the T and W rows of one node (one Gram read, two sums).
-template <int W, int N>
-__device__ __forceinline__ void path_update2(float (&accT)[N], float (&accW)[N],
-                                             const uint32_t (&pw)[8], float sT, float sW,
-                                             const float* row, int x) {
-  static_assert(W <= N, "width within the partial sums");
-#pragma unroll
-  for (int j = 0; j < W; ++j) {
-    const float gk = row[path_at(pw, j) ^ x];
-    accT[j] = fmaf(sT, gk, accT[j]);
-    accW[j] = fmaf(sW, gk, accW[j]);
-  }
-}
-
 // One row of T (t_row) or W of the node sn at depth dn, by substitution along
 // its root path P = (p_0 = root, ..., p_dn = sn):
 //   r (I + X_P) = y,  X_P[i][j] = b_{p_i} e^{G_{p_i} - G_{p_j}} k_{p_i}.k_{p_j} (i > j),
-//   y = e_dn for T;  y_j = e^{G_n - G_{p_j}} q_n.k_{p_j} for W.
+//   y = e_dn for T;  y_j = e^{G_n - G_{p_j}} q_n.k_{p_j} for W (stored scaled, below).
 // With phi_i = e^{G_{p_i} - G_n} >= 1 and s_i = r_i b_{p_i} phi_i:
 //   r_j = y_j - (1 / phi_j) acc_j,  acc_j = sum_{i>j} s_i k_{p_i}.k_{p_j}.
 // Entries are settled from the node towards the root; once s_i is known it is
@@ -224,9 +231,9 @@ __device__ __forceinline__ void path_update2(float (&accT)[N], float (&accW)[N],
 // (phi is capped at e^80; the capped terms are below fp32 resolution.)  r_j is
 // written as bf16 hi + lo at column p_j of the [T; W] operand row.
 template <int D>
-__device__ __forceinline__ void solve_path_row(const ItemMeta& M, const float* GR,
-                                               uint8_t* smem, int sn, int dn, int wmax,
-                                               bool t_row) {
+__device__ __forceinline__ void solve_path_row(const ItemMeta& M, const float* KK,
+                                               const float* QK, uint8_t* smem, int sn, int dn,
+                                               int wmax, bool t_row) {
   constexpr int NA = D <= 16 ? 16 : 32;  // partial sums held (entries 0 .. NA-1)
   static_assert(D <= NA, "path fits the partial sums");
   const uint8_t* prow = M.path[sn];  // entries past the node are 0 (a valid node)
@@ -235,7 +242,10 @@ __device__ __forceinline__ void solve_path_row(const ItemMeta& M, const float* G
   const uint32_t pw[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
   const float Gn = M.G[sn];
   const int a2row = t_row ? sn : 64 + sn;
-  const float* GRq = GR + (64 + sn) * 64;  // q_n . k_s, row 64 + sn (same swizzle phase)
+  // a W row is stored times e^{-max(G_n, -60)}: the second product adds it onto
+  // Q S0 and the output is that sum times e^{max(G_n, -60)}
+  const float wscale = t_row ? 1.f : __expf(-fmaxf(Gn, -60.f));
+  const float* GRq = QK + sn * 64;  // q_n . k_s (chunks rotated by sn & 7)
   const int xq = (sn & 7) << 2;
   float acc[NA];
 #pragma unroll
@@ -251,9 +261,9 @@ __device__ __forceinline__ void solve_path_row(const ItemMeta& M, const float* G
     const int pnn = i > 1 ? prow[i - 2] : 0;
     const float Gnx = M.G[pn], bnx = M.bb[pn];
     const float qnx = t_row ? 0.f : GRq[pn ^ xq];
-    // Gram row p_i: element (p_i, c) sits at p_i * 64 + (c ^ ((p_i & 7) << 2))
-    const float* GRi = GR + pi * 64;
-    const int xi = (pi & 7) << 2;
+    // K K^T row p_i (padded, unrotated)
+    const float* GRi = KK + pi * kKKStride;
+    const int xi = 0;
     const float kn = GRi[pn ^ xi];  // k_{p_i}.k_{p_{i-1}}
     const float y = t_row ? (i == dn ? 1.f : 0.f) : __expf(Gn - Gi) * qi;
     const float inv_phi = __expf(fmaxf(Gn - Gi, -80.f));
@@ -263,8 +273,9 @@ __device__ __forceinline__ void solve_path_row(const ItemMeta& M, const float* G
     const bool own = i <= dn;
     const float s = own ? r * f : 0.f;
     if (own) {
-      const __nv_bfloat16 hi = __float2bfloat16_rn(r);
-      const __nv_bfloat16 lw = __float2bfloat16_rn(r - __bfloat162float(hi));
+      const float rw = r * wscale;
+      const __nv_bfloat16 hi = __float2bfloat16_rn(rw);
+      const __nv_bfloat16 lw = __float2bfloat16_rn(rw - __bfloat162float(hi));
       const int off = atom_off(a2row, pi >> 3) + (pi & 7) * 2;
       *reinterpret_cast<__nv_bfloat16*>(smem + kOffA2hi + off) = hi;
       *reinterpret_cast<__nv_bfloat16*>(smem + kOffA2lo + off) = lw;
@@ -288,84 +299,10 @@ __device__ __forceinline__ void solve_path_row(const ItemMeta& M, const float* G
   }
 }
 
-// The T row and the W row of node sn together (trees of depth <= 16): one path
-// walk, one Gram read per entry for both sums, the gate factors shared.
-template <int D>
-__device__ __forceinline__ void solve_path_pair(const ItemMeta& M, const float* GR,
-                                                uint8_t* smem, int sn, int dn, int wmax) {
-  static_assert(D <= 16, "paired rows keep 2 x 16 partial sums");
-  constexpr int NA = 16;
-  const uint8_t* prow = M.path[sn];  // entries past the node are 0 (a valid node)
-  const uint4* pr = reinterpret_cast<const uint4*>(prow);
-  const uint4 pa = pr[0], pb = pr[1];
-  const uint32_t pw[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
-  const float Gn = M.G[sn];
-  const float* GRq = GR + (64 + sn) * 64;  // q_n . k_s, row 64 + sn (same swizzle phase)
-  const int xq = (sn & 7) << 2;
-  float accT[NA], accW[NA];
-#pragma unroll
-  for (int k = 0; k < NA; ++k) {
-    accT[k] = 0.f;
-    accW[k] = 0.f;
-  }
-  float aiT = 0.f, aiW = 0.f;
-  int pi = prow[wmax];
-  int pn = wmax > 0 ? prow[wmax - 1] : 0;
-  float Gi = M.G[pi], bi = M.bb[pi], qi = GRq[pi ^ xq];
-  for (int i = wmax; i >= 0; --i) {
-    const int pnn = i > 1 ? prow[i - 2] : 0;
-    const float Gnx = M.G[pn], bnx = M.bb[pn], qnx = GRq[pn ^ xq];
-    const float* GRi = GR + pi * 64;
-    const int xi = (pi & 7) << 2;
-    const float kn = GRi[pn ^ xi];
-    const float yW = __expf(Gn - Gi) * qi;
-    const float inv_phi = __expf(fmaxf(Gn - Gi, -80.f));
-    const float f = bi * __expf(fminf(Gi - Gn, 80.f));
-    const float baseT = pick<NA>(accT, i - 1);
-    const float baseW = pick<NA>(accW, i - 1);
-    const float rT = (i == dn ? 1.f : 0.f) - inv_phi * aiT;
-    const float rW = yW - inv_phi * aiW;
-    const bool own = i <= dn;
-    const float sT = own ? rT * f : 0.f;
-    const float sW = own ? rW * f : 0.f;
-    if (own) {
-      const int col = (pi >> 3);
-      const int sub = (pi & 7) * 2;
-      const int offT = atom_off(sn, col) + sub;
-      const int offW = atom_off(64 + sn, col) + sub;
-      const __nv_bfloat16 hT = __float2bfloat16_rn(rT);
-      const __nv_bfloat16 hW = __float2bfloat16_rn(rW);
-      *reinterpret_cast<__nv_bfloat16*>(smem + kOffA2hi + offT) = hT;
-      *reinterpret_cast<__nv_bfloat16*>(smem + kOffA2lo + offT) =
-          __float2bfloat16_rn(rT - __bfloat162float(hT));
-      *reinterpret_cast<__nv_bfloat16*>(smem + kOffA2hi + offW) = hW;
-      *reinterpret_cast<__nv_bfloat16*>(smem + kOffA2lo + offW) =
-          __float2bfloat16_rn(rW - __bfloat162float(hW));
-    }
-    const int lim = i - 1;
-    if (lim <= 4) {
-      path_update2<4>(accT, accW, pw, sT, sW, GRi, xi);
-    } else if (lim <= 8) {
-      path_update2<8>(accT, accW, pw, sT, sW, GRi, xi);
-    } else if (lim <= 12) {
-      path_update2<12>(accT, accW, pw, sT, sW, GRi, xi);
-    } else {
-      path_update2<16>(accT, accW, pw, sT, sW, GRi, xi);
-    }
-    aiT = fmaf(sT, kn, baseT);
-    aiW = fmaf(sW, kn, baseW);
-    pi = pn;
-    pn = pnn;
-    Gi = Gnx;
-    bi = bnx;
-    qi = qnx;
-  }
-}
-
 template <int kSolveD>
 __global__ void __launch_bounds__(kTcThreads, 1)
 verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-                 const __grid_constant__ CUtensorMap vmap,
+                 const __grid_constant__ CUtensorMap vmap, const __grid_constant__ OutMaps om,
                  int n_items, int H_qk, int H_v, int depth_max, int words, int small_only,
                  const int32_t* __restrict__ cu,
                  const int32_t* __restrict__ depth, const int32_t* __restrict__ order,
@@ -405,6 +342,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     mbar_init(&sh.v_bar, 1);
     mbar_init(&sh.s1_done[0], 2);
     mbar_init(&sh.s1_done[1], 2);
+    mbar_init(&sh.op_ready[0], 1);
+    mbar_init(&sh.op_ready[1], 1);
+    mbar_init(&sh.cmt_bar, 1);
     mbar_init(&sh.tmem_free[0], 1);
     mbar_init(&sh.tmem_free[1], 1);
     fence_mbar_init();
@@ -413,6 +353,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     sh.tma_issued = 0;
     sh.v_issued = 0;
     sh.mma1_issued = 0;
+    sh.mma2_issued = 0;
+    sh.cmt_issued = 0;
   }
   if (warp == 0) tmem_alloc(&sh.tmem_slot, kTmemCols);
   tc_fence_before_sync();
@@ -447,16 +389,20 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       tma_load_3d(smem + kOffA + 24576, &qmap, &sh.tma_bar, 64, qh, row0);
       sh.tma_issued += 1;
     };
-    // S0 of one item: warp w holds rows 16 w .. 16 w + 15, lane p & 31 float4
-    // column p & 31 (plain loads: with a pending commit the kernel writes these
-    // rows back)
-    const int srow0 = (p >> 5) * 16, sq = p & 31;
-    float4 sreg[16];
+    // The state of one item, one value column per thread: warp w holds column
+    // jc = 32 (w & 3) + lane of key rows rb .. rb + 63, rb = 64 (w >> 2) (plain loads:
+    // with a pending commit the kernel writes these rows back).  A warp's access to
+    // one row is one 128-byte line, and the registers line up with the TMEM lanes
+    // of the commit product (lane = value column).
+    const int jc = 32 * ((p >> 5) & 3) + (p & 31);
+    const int rb = 64 * (p >> 7);
+    float sreg[64];
+    auto sptr = [&](int item, int i) {
+      return S + (size_t)item * kTcDK * kTcDV + (size_t)(rb + i) * kTcDV + jc;
+    };
     auto load_s0 = [&](int item) {
-      const float* src = S + (size_t)item * kTcDK * kTcDV;  // item = bi * H_v + h
 #pragma unroll
-      for (int r = 0; r < 16; ++r)
-        sreg[r] = reinterpret_cast<const float4*>(src + (size_t)(srow0 + r) * kTcDV)[sq];
+      for (int i = 0; i < 64; ++i) sreg[i] = *sptr(item, i);
     };
     // Warp 0, two items ahead of its staging: the item's accepted path in the
     // previous tree (lane l holds entry l) and that sequence's bounds and status.
@@ -518,7 +464,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       pf.lo = q_lo;
       pf.N = q_hi - q_lo;
       pf.st = q_st;
-      if (p < pf.N && p < kTcNodes) {
+      // (rows of a sequence whose bounds tree prep found bad are never touched)
+      if (pf.st == TGDN_SEQ_OK && p < pf.N && p < kTcNodes) {
         pf.dep = depth[pf.lo + p];
         pf.pos = pos[pf.lo + p];
         pf.ord = order[pf.lo + p];
@@ -544,120 +491,165 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     int prev_bi = -1;  // sequence of the previous item when its tree was valid
     int npr = 0;       // items processed so far (passed-over items excluded): one [K;Q]
                        // copy and one first product each, in order
+    int ncm = 0;       // commit products issued so far
     for (int j = 0; item < i_end; ++j, item += i_step) {
       const int slot = j & 1;
       ItemMeta& M = sh.meta[slot];
       const int bi = item / H_v, h = item % H_v;
       const int lo = pf.lo, N = pf.N;
       const int next = item + i_step;
-      if (fused) {
-        // the previous step's commit: S = e^{G*} S + sum_l e^{G*-G_l} k_l u_l^T,
-        // written back in place; the committed state is what gets verified
-        cp_async_wait_all();
-        if (p < 32 && next < i_end) publish_commit(slot ^ 1);  // the next item's path
-        // thread 0: the previous first product has completed, so its operands (the
-        // [K; Q] and S0 areas) are free; this item's key and query rows go out
-        bool w_ok = true;
-        if (p == 0) {
-          if (npr > 0) w_ok = mbar_wait_suspend(&sh.mma1_bar, (npr - 1) & 1, abort);
-          if (w_ok) issue_kq(item, lo);
-        }
-        if (!named_sync_and(kBarP, kGroup, w_ok && !*abort)) break;
-        const int L = sh.c_L[slot];
-        if (L > 0) {
-          const float4* UP = reinterpret_cast<const float4*>(smem + kOffUP);
-          const uint4* KP = reinterpret_cast<const uint4*>(smem + kOffKP);
-          const float* GP = reinterpret_cast<const float*>(smem + kOffGP);
-          const float Gstar = GP[(L - 1) * 4 + sh.c_gi[slot][L - 1]];
-          const float decay = __expf(Gstar);
-#pragma unroll
-          for (int r = 0; r < 16; ++r) {
-            sreg[r].x *= decay;
-            sreg[r].y *= decay;
-            sreg[r].z *= decay;
-            sreg[r].w *= decay;
-          }
-          // one path node per step; its u row, k rows and G_s are read a step ahead
-          const int kq = srow0 >> 3;  // 16-byte chunk of this warp's 16 rows of k
-          float4 un = UP[sq];
-          uint4 kan = KP[kq], kbn = KP[kq + 1];
-          float gn = GP[sh.c_gi[slot][0]];
-          for (int l = 0; l < L; ++l) {
-            float4 u = un;
-            const uint4 ka = kan, kb = kbn;
-            const float cl = __expf(Gstar - gn);
-            if (l + 1 < L) {
-              un = UP[(l + 1) * (kTcDV / 4) + sq];
-              kan = KP[(l + 1) * (kTcDK / 8) + kq];
-              kbn = KP[(l + 1) * (kTcDK / 8) + kq + 1];
-              gn = GP[(l + 1) * 4 + sh.c_gi[slot][l + 1]];
-            }
-            u.x *= cl;
-            u.y *= cl;
-            u.z *= cl;
-            u.w *= cl;
-            // k_l at this warp's 16 rows: 32 bytes, the same for the whole warp
-            const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {  // bf16 pair -> rows srow0 + 2 i, + 2 i + 1
-              const float k0 = __uint_as_float(kw[i] << 16);
-              const float k1 = __uint_as_float(kw[i] & 0xffff0000u);
-              float4& a0 = sreg[2 * i];
-              float4& a1 = sreg[2 * i + 1];
-              a0.x = fmaf(k0, u.x, a0.x);
-              a0.y = fmaf(k0, u.y, a0.y);
-              a0.z = fmaf(k0, u.z, a0.z);
-              a0.w = fmaf(k0, u.w, a0.w);
-              a1.x = fmaf(k1, u.x, a1.x);
-              a1.y = fmaf(k1, u.y, a1.y);
-              a1.z = fmaf(k1, u.z, a1.z);
-              a1.w = fmaf(k1, u.w, a1.w);
-            }
-          }
-          // the committed rows, written back in place (a warp stores whole rows)
-          float* dst = S + (size_t)item * kTcDK * kTcDV;
-#pragma unroll
-          for (int r = 0; r < 16; ++r)
-            reinterpret_cast<float4*>(dst + (size_t)(srow0 + r) * kTcDV)[sq] = sreg[r];
-        }
-      }
-      // the consumer has finished item j-2, the previous user of this half and slot
-      // (every wait is agreed on by the whole group before anyone leaves the loop);
-      // the commit above touches neither, so it runs while the consumer finishes
-      if (j >= 2 && !group_wait(&sh.tmem_free[slot], ((j >> 1) + 1) & 1, kBarP, p == 0, abort))
-        break;
-      bool ok = (pf.st == TGDN_SEQ_OK) && N > 0 && N <= kTcNodes;
       // (small_only: sequences above 64 nodes belong to the 128-node kernel; their
       // items pass through without state, solve or writes)
       const bool skip = small_only && N > kTcNodes;
+      bool ok = (pf.st == TGDN_SEQ_OK) && N > 0 && N <= kTcNodes;
+      // this node's ancestor-mask row (its position came with the prefetched
+      // metadata); used for the root paths at the end of the iteration
       uint64_t my_anc = 0;
+      if (ok && p < N) {
+        const bool v_ok = pf.dep >= 0 && pf.dep <= depth_max && pf.dep <= kTcDepth &&
+                          pf.pos >= 0 && pf.pos < N && pf.ord >= 0 && pf.ord < N;
+        if (v_ok) my_anc = anc[(size_t)(lo + pf.pos) * words];  // positions < 64: word 0
+        else ok = false;
+      }
+      int L = 0;
+      if (fused) {
+        cp_async_wait_all();
+        if (p < 32 && next < i_end) publish_commit(slot ^ 1);  // the next item's path
+        if (!named_sync_and(kBarP, kGroup, !*abort)) break;    // staged rows visible
+        L = sh.c_L[slot];
+      }
+      // thread 0: the previous first product has completed, so its operand areas are
+      // free: this item's key and query rows go out, and the state area may take the
+      // commit operands
+      bool step_ok = true;
+      if (p == 0 && !skip) {
+        if (npr > 0) step_ok = mbar_wait_suspend(&sh.mma1_bar, (npr - 1) & 1, abort);
+        if (step_ok) issue_kq(item, lo);
+      }
+      if (!named_sync_and(kBarP, kGroup, step_ok && !*abort)) break;
+      if (L > 0) {
+        // The previous step's commit, S = e^{G*} S + sum_l e^{G*-G_l} k_l u_l^T, on the
+        // tensor cores: D^T = (C U_p)^T K_p with C = diag(e^{G*-G_l}) (M = 128 value
+        // columns, N = 2 x 64 key rows, K = the path padded to 16 or 32; C U_p as bf16
+        // hi + lo, K_p exact), then S = e^{G*} S + D in registers.
+        const int kp = L <= 16 ? 16 : 32;
+        const int kcs = kp / 8 * 1024;  // bytes per 64-element chunk of an operand
+        const float* UP = reinterpret_cast<const float*>(smem + kOffUP);
+        const uint4* KP = reinterpret_cast<const uint4*>(smem + kOffKP);
+        const float* GP = reinterpret_cast<const float*>(smem + kOffGP);
+        const float Gstar = GP[(L - 1) * 4 + sh.c_gi[slot][L - 1]];
+        for (int u = p; u < kp * 16; u += kGroup) {
+          const int l = u >> 4, mc = u & 15;  // path entry; 8-element chunk of its row
+          const int off = (mc >> 3) * kcs + (l >> 3) * 1024 + (l & 7) * 128 +
+                          (((mc & 7) ^ (l & 7)) << 4);
+          uint4 ahi = make_uint4(0u, 0u, 0u, 0u), alo = ahi, bk = ahi;
+          if (l < L) {
+            const float cl = __expf(Gstar - GP[l * 4 + sh.c_gi[slot][l]]);
+            const float4 u0 = reinterpret_cast<const float4*>(UP + l * kTcDV)[2 * mc];
+            const float4 u1 = reinterpret_cast<const float4*>(UP + l * kTcDV)[2 * mc + 1];
+            const float x[8] = {cl * u0.x, cl * u0.y, cl * u0.z, cl * u0.w,
+                                cl * u1.x, cl * u1.y, cl * u1.z, cl * u1.w};
+            split8(x, ahi, alo);
+            bk = KP[l * (kTcDK / 8) + mc];
+          }
+          *reinterpret_cast<uint4*>(smem + kOffCAhi + off) = ahi;
+          *reinterpret_cast<uint4*>(smem + kOffCAlo + off) = alo;
+          *reinterpret_cast<uint4*>(smem + kOffCB + off) = bk;
+        }
+        fence_proxy_async_smem();
+        named_sync(kBarP, kGroup);  // the commit operands are written
+        if (p == 0) {
+          tc_fence_after_sync();
+          const uint32_t sAh = smem_addr(smem + kOffCAhi), sAl = smem_addr(smem + kOffCAlo);
+          const uint32_t sB = smem_addr(smem + kOffCB);
+          constexpr uint32_t id_c = idesc_bf16_f32(128, 64, 1, 1);
+          for (int ks = 0; ks < kp / 16; ++ks) {
+            // MN-major operands: 64-element chunks kcs apart, 8-entry k groups 1 KiB apart
+            const uint64_t ah = smem_desc(sAh + ks * 2048, kcs, 1024, kSwizzle128B);
+            const uint64_t al = smem_desc(sAl + ks * 2048, kcs, 1024, kSwizzle128B);
+#pragma unroll
+            for (int nh = 0; nh < 2; ++nh) {
+              const uint64_t bd = smem_desc(sB + nh * kcs + ks * 2048, kcs, 1024, kSwizzle128B);
+              const uint32_t d = tmem + (nh ? kCommitCol1 : kCommitCol0);
+              umma_bf16(d, ah, bd, id_c, ks > 0);
+              umma_bf16(d, al, bd, id_c, 1);
+            }
+          }
+          umma_commit(&sh.cmt_bar);
+          sh.cmt_issued += 1;
+        }
+        if (!group_wait(&sh.cmt_bar, ncm & 1, kBarP, p == 0, abort)) break;
+        ++ncm;
+        tc_fence_after_sync();
+        const float decay = __expf(Gstar);
+        const uint32_t tc0 = tmem + (static_cast<uint32_t>(32 * ((p >> 5) & 3)) << 16) +
+                             (rb == 0 ? kCommitCol0 : kCommitCol1);
+#pragma unroll
+        for (int hv = 0; hv < 2; ++hv) {
+          float d[32];
+          tmem_ld32(tc0 + hv * 32, d);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) sreg[hv * 32 + i] = fmaf(decay, sreg[hv * 32 + i], d[i]);
+        }
+      }
+      // Row by row: the committed value goes back in place (fused), its bf16 copy into
+      // the K-major state operand, and the next item's value is loaded into the freed
+      // register, so that stores, operand writes and loads interleave.  (The state
+      // enters the tensor-core product as bf16; it stays fp32 in memory.)
+      const bool load_next = next < i_end && !(small_only && q_hi - q_lo > kTcNodes);
+      if (!skip) {
+        uint8_t* op_row = smem + kOffS + (rb >> 6) * 16384 + jc * 128;
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {  // 8 key rows per 16-byte chunk
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = c8 * 8 + 2 * e;
+            if (L > 0) {
+              *sptr(item, i) = sreg[i];
+              *sptr(item, i + 1) = sreg[i + 1];
+            }
+            w[e] = pack_bf16x2(sreg[i], sreg[i + 1]);
+            if (load_next) {
+              sreg[i] = *sptr(next, i);
+              sreg[i + 1] = *sptr(next, i + 1);
+            }
+          }
+          *reinterpret_cast<uint4*>(op_row + ((c8 ^ (jc & 7)) << 4)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      } else if (load_next) {
+        load_s0(next);
+      }
+      fence_proxy_async_smem();
+      named_sync(kBarP, kGroup);  // the S operand is complete
+      if (p == 0) {
+        sh.op_skip[slot] = skip ? 1 : 0;
+        mbar_arrive(&sh.op_ready[slot]);  // the consumer's issuing thread takes it from here
+      }
+      // the consumer has finished item j-2, the previous user of this half and slot
+      // (every wait is agreed on by the whole group before anyone leaves the loop)
+      if (j >= 2 && !group_wait(&sh.tmem_free[slot], ((j >> 1) + 1) & 1, kBarP, p == 0, abort))
+        break;
       if (p == 0) {
         M.lo = lo;
         M.N = N;
         M.h = h;
         M.skip = skip;
+        // rows zero-filled for an item that is not verified: none for a passed-over
+        // item or for a sequence whose bounds tree prep found bad
+        M.zrows = (skip || pf.st == TGDN_SEQ_BAD_RANGE || N < 0) ? 0 : N;
       }
       if (ok && p < N) {
-        const bool v_ok = pf.dep >= 0 && pf.dep <= depth_max && pf.dep <= kTcDepth &&
-                          pf.pos >= 0 && pf.pos < N && pf.ord >= 0 && pf.ord < N;
-        ok = v_ok;
         M.dep[p] = pf.dep;
         M.pos[p] = pf.pos;
         M.ord[p] = pf.ord;
         M.gg[p] = pf.gg;
         M.bb[p] = pf.bb;
-        if (v_ok) my_anc = anc[(size_t)(lo + pf.pos) * words];  // positions < 64: word 0
       }
-      // Without a pending commit the same hand-over happens here.
-      bool step_ok = true;
-      if (!fused && p == 0 && !skip) {
-        if (npr > 0) step_ok = mbar_wait_suspend(&sh.mma1_bar, (npr - 1) & 1, abort);
-        if (step_ok) issue_kq(item, lo);
-      }
-      // (also: every thread has finished reading this item's staged commit)
-      if (!named_sync_and(kBarP, kGroup, step_ok && !*abort)) break;
-      // the next item's small loads go out before the operand stores, so that they
-      // wait neither behind those stores nor for their source registers
+      // the next item's small loads and its staged commit go out now; they land
+      // while this item's paths are built
       if (next < i_end) {
         load_meta(next);
         if (next + i_step < i_end) {
@@ -666,76 +658,22 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         }
       }
       if (fused && next < i_end) stage_commit(next, slot ^ 1);
-      // S0 registers -> bf16 hi/lo operand
-#pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        if (skip) break;  // (uniform)
-        const int kr = srow0 + r;
-        const float4 xv = sreg[r];
-        const float h0 = __bfloat162float(__float2bfloat16_rn(xv.x));
-        const float h1 = __bfloat162float(__float2bfloat16_rn(xv.y));
-        const float h2 = __bfloat162float(__float2bfloat16_rn(xv.z));
-        const float h3 = __bfloat162float(__float2bfloat16_rn(xv.w));
-        const int off = (sq >> 4) * 16384 + atom_off(kr, (sq & 15) >> 1) + (sq & 1) * 8;
-        *reinterpret_cast<uint2*>(smem + kOffS0hi + off) =
-            make_uint2(pack_bf16x2(h0, h1), pack_bf16x2(h2, h3));
-        *reinterpret_cast<uint2*>(smem + kOffS0lo + off) =
-            make_uint2(pack_bf16x2(xv.x - h0, xv.y - h1), pack_bf16x2(xv.z - h2, xv.w - h3));
-      }
-      fence_proxy_async_smem();
-      named_sync(kBarP, kGroup);  // the S0 operand is complete
-      // First product into TMEM half `slot`, issued by the group's last thread (no
-      // node of its own) while the others prefetch and build the paths; its
-      // completion is awaited in the next iteration.  Items found invalid below
-      // get the product too; the consumer ignores it and zero-fills.
-      if (p == kGroup - 1 && skip) {
-        mbar_arrive(&sh.s1_done[slot]);  // a passed-over item: no copy, no product
-      } else if (p == kGroup - 1) {
-        if (mbar_wait_suspend(&sh.tma_bar, npr & 1, abort)) {
-          tc_fence_after_sync();
-          const uint32_t tb = tmem + slot * 256;
-          const uint32_t sA = smem_addr(smem + kOffA);
-          const uint32_t sHi = smem_addr(smem + kOffS0hi);
-          const uint32_t sLo = smem_addr(smem + kOffS0lo);
-          constexpr uint32_t id_s0 = idesc_bf16_f32(128, 128, 0, 1);
-          constexpr uint32_t id_gram = idesc_bf16_f32(128, kTcNodes, 0, 0);
-#pragma unroll
-          for (int s = 0; s < kTcDK / 16; ++s) {
-            const uint64_t ad = smem_desc(sA + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024,
-                                          kSwizzle128B);
-            // MN-major S0: value-column atoms 16 KiB apart (leading byte offset),
-            // 8-row k groups 1 KiB apart (stride byte offset)
-            const uint64_t hd = smem_desc(sHi + s * 2048, 16384, 1024, kSwizzle128B);
-            const uint64_t ld = smem_desc(sLo + s * 2048, 16384, 1024, kSwizzle128B);
-            umma_bf16(tb, ad, hd, id_s0, s > 0);
-            umma_bf16(tb, ad, ld, id_s0, 1);
-            umma_bf16(tb + kGramCol, ad, ad, id_gram, s > 0);  // B = the key rows of A
-          }
-          umma_commit(&sh.mma1_bar);
-          umma_commit(&sh.s1_done[slot]);
-          sh.mma1_issued += 1;
-        } else {
-          mbar_arrive(&sh.s1_done[slot]);  // no product: the consumer zero-fills
-        }
-      }
-      // the next item's state while this one is finished
-      if (next < i_end && !(small_only && pf.N > kTcNodes)) load_s0(next);
+      named_sync(kBarP, kGroup);  // this slot's node metadata is written
       // root paths from the ancestor masks (bits = topological positions,
       // ascending = root first) and path-cumulative log-gates; the same tree as
       // the previous item (another head) reuses its paths and only sums the gates.
-      // This runs while the first product is being issued, before the group has
-      // agreed that every node's metadata is valid, so a node index read from
-      // another thread's metadata is range-checked before it is used.
+      // A node index read from another thread's metadata is range-checked before
+      // it is used (the group agrees on validity only after this).
       const bool reuse = prev_bi == bi;
       if (ok && p < N && reuse) {
         const int dn = M.dep[p];
-        const uint8_t* srow = sh.meta[slot ^ 1].path[p];
-        const uint4* src = reinterpret_cast<const uint4*>(srow);
+        const uint8_t* srow_p = sh.meta[slot ^ 1].path[p];
+        const uint4* src = reinterpret_cast<const uint4*>(srow_p);
         uint4* dst = reinterpret_cast<uint4*>(M.path[p]);
         dst[0] = src[0];
         dst[1] = src[1];
         float acc = 0.f;
-        for (int i = 0; i <= dn; ++i) acc += M.gg[srow[i]];
+        for (int i = 0; i <= dn; ++i) acc += M.gg[srow_p[i]];
         M.G[p] = acc;
       } else if (ok && p < N) {
         const int dn = M.dep[p];
@@ -799,26 +737,77 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       tma_load_3d(smem + kOffRlo + 8192, &vmap, &sh.v_bar, 64, item % H_v, cv_lo);
       sh.v_issued += 1;
     };
+    // Thread 0 also issues every first product (item jj into TMEM half jj & 1),
+    // once the producer has completed the item's state operand and its key and
+    // query rows have landed: D[:, 0:128] = [K;Q] S0,  D[:, 128:192] = [K;Q] K^T.
+    // It does so while the previous item's rows are being solved when the operands
+    // are ready by then, else at the top of the item; a passed-over item gets no
+    // product.  Returns false when the operands are not ready (block = false) or
+    // a wait expired (block = true).
+    int nkq = 0;  // [K;Q] copies consumed so far
+    auto issue_p1 = [&](int jj, bool block) -> bool {
+      const int sl = jj & 1;
+      const uint32_t par = (jj >> 1) & 1;
+      if (block) {
+        if (!mbar_wait_suspend(&sh.op_ready[sl], par, abort)) return false;
+      } else if (!mbar_test(&sh.op_ready[sl], par)) {
+        return false;
+      }
+      if (sh.op_skip[sl]) {
+        mbar_arrive(&sh.s1_done[sl]);  // a passed-over item: no copy, no product
+        return true;
+      }
+      if (block) {
+        if (!mbar_wait_suspend(&sh.tma_bar, nkq & 1, abort)) return false;
+      } else if (!mbar_test(&sh.tma_bar, nkq & 1)) {
+        return false;
+      }
+      tc_fence_after_sync();
+      const uint32_t tb = tmem + sl * 256;
+      const uint32_t sA = smem_addr(smem + kOffA);
+      const uint32_t sS = smem_addr(smem + kOffS);
+      constexpr uint32_t id_s0 = idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t id_gram = idesc_bf16_f32(128, kTcNodes, 0, 0);
+#pragma unroll
+      for (int s = 0; s < kTcDK / 16; ++s) {
+        const uint64_t ad = smem_desc(sA + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024,
+                                      kSwizzle128B);
+        // K-major S0^T: the same layout as A (64-element k halves 16 KiB apart)
+        const uint64_t hd = smem_desc(sS + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024,
+                                      kSwizzle128B);
+        umma_bf16(tb, ad, hd, id_s0, s > 0);
+        umma_bf16(tb + kGramCol, ad, ad, id_gram, s > 0);  // B = the key rows of A
+      }
+      umma_commit(&sh.mma1_bar);
+      umma_commit(&sh.s1_done[sl]);
+      sh.mma1_issued += 1;
+      ++nkq;
+      return true;
+    };
     int item = i_begin;
     if (c == 0) {
       load_vseq(item);
       if (v_wanted()) issue_v(item);
       if (item + i_step < i_end) load_vseq(item + i_step);
     }
+    int p1_next = 0;          // the next item whose first product is not yet issued
     uint32_t mma2_count = 0;  // second products issued so far (same in every thread)
     int nv = 0;               // V copies consumed so far (one per item not passed over)
     for (int j = 0; item < i_end; ++j, item += i_step) {
       const int slot = j & 1;
+      const int next = item + i_step;
       bulk_wait_read();  // the previous item's output rows have left shared memory
+      if (c == 0 && p1_next == j) {
+        if (issue_p1(j, true)) ++p1_next;  // (on expiry the wait below sees the abort)
+      }
       if (!group_wait(&sh.s1_done[slot], (j >> 1) & 1, kBarC, c == 0, abort)) break;
       tc_fence_after_sync();
       const ItemMeta& M = sh.meta[slot];
       const int lo = M.lo, N = M.N, h = M.h;
       const uint32_t tb = tmem + slot * 256;
-      const int next = item + i_step;
 
       if (!M.good) {  // bad or empty sequence: zero rows (none for a passed-on item)
-        const int nz = M.skip ? 0 : N;
+        const int nz = M.zrows;
         for (int e = c; e < nz * (kTcDV / 4); e += kGroup) {
           const int n = e >> 5, c4 = e & 31;
           const size_t row = ((size_t)(lo + n) * H_v + h) * kTcDV + c4 * 4;
@@ -833,6 +822,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             if (v_wanted()) issue_v(next);
             if (next + i_step < i_end) load_vseq(next + i_step);
           }
+          if (v_ok && next < i_end && p1_next == j + 1 && issue_p1(j + 1, false)) ++p1_next;
         }
         if (!M.skip) ++nv;
         if (!named_sync_and(kBarC, kGroup, v_ok)) break;
@@ -842,14 +832,22 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
 
       // ---- Gram rows -> shared memory; [T; W] operand zeroed
       {
-        float* GR = reinterpret_cast<float*>(smem + kOffGR);
         float r[32];
         tmem_ld32(tb + lane_base + kGramCol + chalf * 32, r);
         tmem_ld_wait();
+        if (key_lane) {  // K K^T row lane_row
+          float4* dst = reinterpret_cast<float4*>(smem + kOffKK) +
+                        (lane_row * kKKStride + chalf * 32) / 4;
 #pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4)
-          *reinterpret_cast<float4*>(GR + lane_row * 64 + swz(lane_row, chalf * 8 + c4) * 4) =
-              make_float4(r[c4 * 4], r[c4 * 4 + 1], r[c4 * 4 + 2], r[c4 * 4 + 3]);
+          for (int c4 = 0; c4 < 8; ++c4)
+            dst[c4] = make_float4(r[c4 * 4], r[c4 * 4 + 1], r[c4 * 4 + 2], r[c4 * 4 + 3]);
+        } else {  // Q K^T row lane_node
+          float* QK = reinterpret_cast<float*>(smem + kOffQK) + lane_node * 64;
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4)
+            *reinterpret_cast<float4*>(QK + swz(lane_node, chalf * 8 + c4) * 4) =
+                make_float4(r[c4 * 4], r[c4 * 4 + 1], r[c4 * 4 + 2], r[c4 * 4 + 3]);
+        }
         const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
         for (int i = 0; i < 8; ++i)  // 32 KiB of [T; W] hi + lo, consecutive 16 B per thread
@@ -857,23 +855,31 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       }
       named_sync(kBarC, kGroup);  // Gram rows stored, [T; W] operand zeroed
 
-      // Key-lane warps form R while the query-lane warps solve for T and W (the
-      // solve needs only the Gram rows and the metadata).
-      // ---- R = diag(b)(V - e^G K S0) as a bf16 hi/lo operand (key lanes)
+      // Warps 8 and 9 (lanes 0-63: the key rows) form R while four others solve for
+      // T and W, one on each scheduler (the solve needs only the Gram rows and the
+      // metadata); warps 14 and 15 wait.
+      // ---- R = diag(b)(V - e^G K S0) as a bf16 hi/lo operand, all 128 columns
       bool v_ok = true;
-      if (key_lane) {
+      if (cw < 2) {
         v_ok = mbar_wait_suspend(&sh.v_bar, nv & 1, abort);
         const bool live = lane_node < N;
         const float eG = live ? __expf(M.G[lane_node]) : 0.f;
         const float bn = live ? M.bb[lane_node] : 0.f;
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {  // 32 value columns at a time
+        for (int qq = 0; qq < 4; ++qq) {  // 32 value columns at a time
+          const int half = qq >> 1, q = qq & 1;
           float r[32];
-          tmem_ld32(tb + lane_base + chalf * 64 + q * 32, r);
+          tmem_ld32(tb + lane_base + half * 64 + q * 32, r);
           tmem_ld_wait();
+          {  // these K S0 columns become the accumulator of U = T R
+            float z[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) z[i] = 0.f;
+            tmem_st32(tb + lane_base + half * 64 + q * 32, z);
+          }
 #pragma unroll
           for (int c8 = 0; c8 < 4; ++c8) {  // 8 columns per 16-byte bf16 chunk
-            const int off = chalf * 8192 + atom_off(lane_node, q * 4 + c8);
+            const int off = half * 8192 + atom_off(lane_node, q * 4 + c8);
             const uint4 vv = *reinterpret_cast<const uint4*>(smem + kOffRlo + off);
             const __nv_bfloat162* vb = reinterpret_cast<const __nv_bfloat162*>(&vv);
             float xr[8];
@@ -889,39 +895,32 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             *reinterpret_cast<uint4*>(smem + kOffRlo + off) = lw;
           }
         }
-      }
-
-      // ---- the rows of T and W on the query-lane warps (solve_path_pair for
-      // trees of depth <= 16, else solve_path_row).  Rows are handed out in
-      // topological order so that a warp sees similar depths.
-      if (!key_lane) {
-        const float* GR = reinterpret_cast<const float*>(smem + kOffGR);
-        if constexpr (kSolveD <= 16) {
-          // warps 10 and 11 (one per scheduler): a node's T and W rows per thread
-          if (chalf == 0) {
-            const int spos = (lq - 2) * 32 + (c & 31);
-            const bool act = spos < N;
-            const int sn = act ? M.ord[spos] : 0;
-            const int dn = act ? M.dep[sn] : -1;
-            const int wmax = __reduce_max_sync(0xffffffffu, dn);
-            solve_path_pair<kSolveD>(M, GR, smem, sn, dn, wmax);
-          }
-        } else {
-          const int sc = (lq - 2) * 64 + chalf * 32 + (c & 31);  // solver index 0..127
-          const int spos = sc & 63;
-          const bool act = spos < N;
-          const int sn = act ? M.ord[spos] : 0;
-          const int dn = act ? M.dep[sn] : -1;
-          const int wmax = __reduce_max_sync(0xffffffffu, dn);
-          solve_path_row<kSolveD>(M, GR, smem, sn, dn, wmax, sc < 64);
-        }
+        tmem_st_wait();
+        // the R warps wait for the solve from here on: the next item's first product
+        // goes in now if its operands are ready, so that it has completed before this
+        // item's second product needs the tensor cores
+        if (c == 0 && next < i_end && p1_next == j + 1 && issue_p1(j + 1, false)) ++p1_next;
+      } else if (cw < 6) {
+        // ---- the rows of T (warps 10 and 12) and of W (warps 11 and 13), one row per
+        // thread.  Rows are handed out in topological order: warps 10 and 11 take the
+        // first 32 positions, warps 12 and 13 (the other two schedulers) the deeper 32.
+        const float* KK = reinterpret_cast<const float*>(smem + kOffKK);
+        const float* QK = reinterpret_cast<const float*>(smem + kOffQK);
+        const bool t_row = (cw & 1) == 0;
+        const int spos = (cw >> 2) * 32 + (c & 31);
+        const bool act = spos < N;
+        const int sn = act ? M.ord[spos] : 0;
+        const int dn = act ? M.dep[sn] : -1;
+        const int wmax = __reduce_max_sync(0xffffffffu, dn);
+        solve_path_row<kSolveD>(M, KK, QK, smem, sn, dn, wmax, t_row);
       }
       fence_proxy_async_smem();
       tc_fence_before_sync();
       if (!named_sync_and(kBarC, kGroup, v_ok)) break;
       tc_fence_after_sync();
 
-      // ---- second product: D[:, 128:256] = [T; W] R  (hi.hi + hi.lo + lo.hi)
+      // ---- second product, added onto columns 0-127: key lanes (zeroed) get U = T R,
+      // query lanes Q S0 + W' R with W' = e^{-max(G, -60)} W  (hi.hi + hi.lo + lo.hi)
       if (c == 0) {
         const uint32_t sA2hi = smem_addr(smem + kOffA2hi);
         const uint32_t sA2lo = smem_addr(smem + kOffA2lo);
@@ -935,12 +934,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
           // MN-major R: value-column atoms 8 KiB apart, 8-node groups 1 KiB apart
           const uint64_t bh = smem_desc(sRhi + s * 2048, 8192, 1024, kSwizzle128B);
           const uint64_t bl = smem_desc(sRlo + s * 2048, 8192, 1024, kSwizzle128B);
-          const uint32_t d = tb + kGramCol;
-          umma_bf16(d, ah, bh, id_r, s > 0);
-          umma_bf16(d, ah, bl, id_r, 1);
-          umma_bf16(d, al, bh, id_r, 1);
+          umma_bf16(tb, ah, bh, id_r, 1);
+          umma_bf16(tb, ah, bl, id_r, 1);
+          umma_bf16(tb, al, bh, id_r, 1);
         }
         umma_commit(&sh.mma2_bar);
+        sh.mma2_issued += 1;
       }
       const bool done2 = group_wait(&sh.mma2_bar, mma2_count & 1, kBarC, c == 0, abort);
       ++mma2_count;
@@ -953,59 +952,79 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         if (next + i_step < i_end) load_vseq(next + i_step);
       }
 
-      // ---- key lanes: U rows; query lanes: O = e^G Q S0 + W R (bf16).  Each
-      // thread stages its half row in shared memory (padded rows: conflict-free)
-      // and sends it to global memory with one bulk copy.
+      // ---- key lanes: U rows; query lanes: O = e^G Q S0 + W R (bf16).  Rows are
+      // staged in 128-byte swizzled tiles and leave by a few TMA tensor stores (a box
+      // of 64 rows, else boxes of 8); the last N mod 8 rows, which a box of 8 would
+      // overrun into the next sequence, go out from registers.
       {
         const bool live = lane_node < N;
+        const bool direct = live && lane_node >= (N & ~7);
+        const int sw = lane_node & 7;
         if (key_lane) {
-          float4* stg = reinterpret_cast<float4*>(smem + kOffUst + lane_node * kUstRow + chalf * 256);
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             float r[32];
-            tmem_ld32(tb + lane_base + kGramCol + chalf * 64 + q * 32, r);
+            tmem_ld32(tb + lane_base + chalf * 64 + q * 32, r);
             tmem_ld_wait();
+            uint8_t* row = smem + kOffUst + (chalf * 2 + q) * 8192 + lane_node * 128;
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              stg[q * 8 + i] = make_float4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+              *reinterpret_cast<float4*>(row + ((i ^ sw) << 4)) =
+                  make_float4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+            if (direct) {
+              float4* dst = reinterpret_cast<float4*>(
+                  Uws + ((size_t)(lo + lane_node) * H_v + h) * kTcDV + chalf * 64 + q * 32);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                dst[i] = make_float4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+            }
           }
-          if (live) {
-            fence_proxy_async_smem();
-            bulk_copy_s2g(Uws + ((size_t)(lo + lane_node) * H_v + h) * kTcDV + chalf * 64, stg,
-                          256);
-            bulk_commit();
-            if (chalf == 0) Gws[(size_t)(lo + lane_node) * H_v + h] = M.G[lane_node];
-          }
+          if (live && chalf == 0) Gws[(size_t)(lo + lane_node) * H_v + h] = M.G[lane_node];
         } else {
-          uint4* stg = reinterpret_cast<uint4*>(smem + kOffOst + lane_node * kOstRow + chalf * 128);
-          const float eG = live ? __expf(M.G[lane_node]) : 0.f;
+          uint8_t* row = smem + kOffOst + chalf * 8192 + lane_node * 128;
+          uint4* dst = reinterpret_cast<uint4*>(o + ((size_t)(lo + lane_node) * H_v + h) * kTcDV +
+                                                chalf * 64);
+          // O = e^{max(G, -60)} (Q S0 + W' R); below e^{-60} the Q S0 term is far
+          // under fp32 resolution of the W R term
+          const float eG = live ? __expf(fmaxf(M.G[lane_node], -60.f)) : 0.f;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {  // 16 value columns at a time
-            float a[16], w[16];
+            float a[16];
             tmem_ld16(tb + lane_base + chalf * 64 + q * 16, a);
-            tmem_ld16(tb + lane_base + kGramCol + chalf * 64 + q * 16, w);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
               const float* aa = a + 8 * i;
-              const float* ww = w + 8 * i;
-              stg[q * 2 + i] =
-                  make_uint4(pack_bf16x2(fmaf(eG, aa[0], ww[0]), fmaf(eG, aa[1], ww[1])),
-                             pack_bf16x2(fmaf(eG, aa[2], ww[2]), fmaf(eG, aa[3], ww[3])),
-                             pack_bf16x2(fmaf(eG, aa[4], ww[4]), fmaf(eG, aa[5], ww[5])),
-                             pack_bf16x2(fmaf(eG, aa[6], ww[6]), fmaf(eG, aa[7], ww[7])));
+              const uint4 pk = make_uint4(pack_bf16x2(eG * aa[0], eG * aa[1]),
+                                          pack_bf16x2(eG * aa[2], eG * aa[3]),
+                                          pack_bf16x2(eG * aa[4], eG * aa[5]),
+                                          pack_bf16x2(eG * aa[6], eG * aa[7]));
+              *reinterpret_cast<uint4*>(row + (((q * 2 + i) ^ sw) << 4)) = pk;
+              if (direct) dst[q * 2 + i] = pk;
             }
-          }
-          if (live) {
-            fence_proxy_async_smem();
-            bulk_copy_s2g(o + ((size_t)(lo + lane_node) * H_v + h) * kTcDV + chalf * 64, stg, 128);
-            bulk_commit();
           }
         }
       }
+      fence_proxy_async_smem();  // the staged rows are visible to the tensor stores
       tc_fence_before_sync();
       named_sync(kBarC, kGroup);
-      if (c == 0) mbar_arrive(&sh.tmem_free[slot]);  // this half is free again
+      if (c == 0) {
+        mbar_arrive(&sh.tmem_free[slot]);  // this half is free again
+        const int n8 = N & ~7;
+        for (int r0 = 0; r0 < n8;) {
+          const bool big = r0 == 0 && n8 == 64;
+          const CUtensorMap* um = big ? &om.u64 : &om.u8;
+          const CUtensorMap* omp = big ? &om.o64 : &om.o8;
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            tma_store_3d(um, smem + kOffUst + t * 8192 + r0 * 128, t * 32, h, lo + r0);
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+            tma_store_3d(omp, smem + kOffOst + t * 8192 + r0 * 128, t * 64, h, lo + r0);
+          r0 += big ? 64 : 8;
+        }
+        bulk_commit();
+      }
     }
     bulk_wait_all();  // this thread's output rows are written
   }
@@ -1020,8 +1039,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     if (sh.tma_issued > 0) (void)mbar_wait(&sh.tma_bar, (sh.tma_issued - 1) & 1);
     if (sh.v_issued > 0) (void)mbar_wait(&sh.v_bar, (sh.v_issued - 1) & 1);
   }
-  // the last first product, before TMEM and the operands are released (bounded)
+  // the last products, before TMEM and the operands are released (bounded)
   if (tid == 0 && sh.mma1_issued > 0) (void)mbar_wait(&sh.mma1_bar, (sh.mma1_issued - 1) & 1);
+  if (tid == 0 && sh.mma2_issued > 0) (void)mbar_wait(&sh.mma2_bar, (sh.mma2_issued - 1) & 1);
+  if (tid == 0 && sh.cmt_issued > 0) (void)mbar_wait(&sh.cmt_bar, (sh.cmt_issued - 1) & 1);
   __syncthreads();
   if (warp == 0) {
     tc_fence_after_sync();
@@ -1055,9 +1076,10 @@ static int sm_count() {
 }
 
 cudaError_t launch_verify_tc(const tgdn_tree& t, const tgdn_dims& d, const CUtensorMap& qmap,
-                             const CUtensorMap& kmap, const CUtensorMap& vmap, const float* g,
-                             const float* b, float* S, void* o, float* U, float* G,
-                             const PendingCommit& cm, bool small_only, cudaStream_t s) {
+                             const CUtensorMap& kmap, const CUtensorMap& vmap,
+                             const OutMaps& om, const float* g, const float* b, float* S,
+                             void* o, float* U, float* G, const PendingCommit& cm,
+                             bool small_only, cudaStream_t s) {
   // the path solve keeps depth_max + 1 partial sums in registers
   auto kern = t.depth_max <= 16 ? verify_tc_kernel<16> : verify_tc_kernel<kTcDepth>;
   cudaError_t e =
@@ -1080,7 +1102,7 @@ cudaError_t launch_verify_tc(const tgdn_tree& t, const tgdn_dims& d, const CUten
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  e = cudaLaunchKernelEx(&lc, kern, qmap, kmap, vmap, (int)items, d.H_qk, d.H_v, t.depth_max,
+  e = cudaLaunchKernelEx(&lc, kern, qmap, kmap, vmap, om, (int)items, d.H_qk, d.H_v, t.depth_max,
                          t.words, small_only ? 1 : 0, t.cu_nodes, t.depth, t.order, t.pos,
                          t.anc, t.status, g, b, S, static_cast<__nv_bfloat16*>(o), U, G, cm);
   if (e != cudaSuccess) return e;

@@ -153,7 +153,8 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
     nx_d0 = 0;
     // (an item this launch passes over, a sequence of at most 64 nodes when the
     // 64-node kernel takes those, is not pulled into L2)
-    if (it < n_items && nx_hi > nx_lo && !(big_only && nx_hi - nx_lo <= 64)) {
+    if (it < n_items && nx_st == TGDN_SEQ_OK && nx_hi > nx_lo &&
+        !(big_only && nx_hi - nx_lo <= 64)) {
       nx_d0 = depth[nx_lo];
       if (tid == 0) prefetch_l2(S0 + (size_t)it * kT8D * kT8D, kT8D * kT8D * 4);
       if (tid < nx_hi - nx_lo && tid <= kT8Nodes)
@@ -182,11 +183,13 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
     const int h = item % H_v, qh = h / grp;
     const int lo = nx_lo, N = nx_hi - nx_lo;
-    const bool st_ok = nx_st == TGDN_SEQ_OK;
+    const int st = nx_st;
+    const bool st_ok = st == TGDN_SEQ_OK;
     const int d0 = nx_d0;
     // the next item's bounds and L2 prefetches go out now and land during this item
     T8_PREFETCH(item + (int)gridDim.x)
     if (N <= 0) continue;  // uniform over the CTA
+    if (st == TGDN_SEQ_BAD_RANGE) continue;  // rows outside the arrays: untouched
     if (big_only && N <= 64) continue;  // the 64-node kernel's sequence
     const int fold = (st_ok && N == kT8Nodes + 1 && d0 == 0) ? 1 : 0;
     if (st_ok && N == kT8Nodes + 1 && !fold) continue;  // root elsewhere: the SIMT kernel's
