@@ -281,8 +281,12 @@ __device__ __forceinline__ void solve_path_row(const ItemMeta& M, const float* K
       *reinterpret_cast<__nv_bfloat16*>(smem + kOffA2lo + off) = lw;
     }
     const int lim = i - 1;  // entries 0 .. i-2 take their terms here
-    if (lim <= 8) {
+    if (lim <= 4) {
+      path_update<4>(acc, pw, s, GRi, xi);
+    } else if (lim <= 8) {
       path_update<8>(acc, pw, s, GRi, xi);
+    } else if (lim <= 12) {
+      path_update<12>(acc, pw, s, GRi, xi);
     } else if (lim <= 16) {
       path_update<16>(acc, pw, s, GRi, xi);
     } else if (lim <= 24) {
@@ -402,7 +406,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     };
     auto load_s0 = [&](int item) {
 #pragma unroll
-      for (int i = 0; i < 64; ++i) sreg[i] = *sptr(item, i);
+      for (int i = 0; i < 64; ++i) sreg[i] = __ldcg(sptr(item, i));
     };
     // Warp 0, two items ahead of its staging: the item's accepted path in the
     // previous tree (lane l holds entry l) and that sequence's bounds and status.
@@ -593,34 +597,19 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
           for (int i = 0; i < 32; ++i) sreg[hv * 32 + i] = fmaf(decay, sreg[hv * 32 + i], d[i]);
         }
       }
-      // Row by row: the committed value goes back in place (fused), its bf16 copy into
-      // the K-major state operand, and the next item's value is loaded into the freed
-      // register, so that stores, operand writes and loads interleave.  (The state
-      // enters the tensor-core product as bf16; it stays fp32 in memory.)
-      const bool load_next = next < i_end && !(small_only && q_hi - q_lo > kTcNodes);
+      // The bf16 copy of the (committed) state into the K-major operand; the state
+      // itself goes back and the next item's comes in after this item is handed over
+      // (the memory traffic then overlaps the consumer's work on this item).  (The
+      // state enters the tensor-core product as bf16; it stays fp32 in memory.)
       if (!skip) {
         uint8_t* op_row = smem + kOffS + (rb >> 6) * 16384 + jc * 128;
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {  // 8 key rows per 16-byte chunk
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i = c8 * 8 + 2 * e;
-            if (L > 0) {
-              *sptr(item, i) = sreg[i];
-              *sptr(item, i + 1) = sreg[i + 1];
-            }
-            w[e] = pack_bf16x2(sreg[i], sreg[i + 1]);
-            if (load_next) {
-              sreg[i] = *sptr(next, i);
-              sreg[i + 1] = *sptr(next, i + 1);
-            }
-          }
+        for (int c8 = 0; c8 < 8; ++c8)  // 8 key rows per 16-byte chunk
           *reinterpret_cast<uint4*>(op_row + ((c8 ^ (jc & 7)) << 4)) =
-              make_uint4(w[0], w[1], w[2], w[3]);
-        }
-      } else if (load_next) {
-        load_s0(next);
+              make_uint4(pack_bf16x2(sreg[c8 * 8], sreg[c8 * 8 + 1]),
+                         pack_bf16x2(sreg[c8 * 8 + 2], sreg[c8 * 8 + 3]),
+                         pack_bf16x2(sreg[c8 * 8 + 4], sreg[c8 * 8 + 5]),
+                         pack_bf16x2(sreg[c8 * 8 + 6], sreg[c8 * 8 + 7]));
       }
       fence_proxy_async_smem();
       named_sync(kBarP, kGroup);  // the S operand is complete
@@ -711,6 +700,24 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         mbar_arrive(&sh.s1_done[slot]);  // the metadata above is written
       }
       if (!skip) ++npr;
+      // the committed state back in place (fused) and the next item's state in, row
+      // by row into the registers each store frees
+      const bool load_next = next < i_end && !(small_only && pf.N > kTcNodes);
+      // (L2-only accesses: the state is touched once per step and never by this SM
+      // again within the launch)
+      if (L > 0) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          __stcg(sptr(item, i), sreg[i]);
+          if (load_next) sreg[i] = __ldcg(sptr(next, i));
+        }
+      } else if (load_next) {
+        load_s0(next);
+      }
+      // A block boundary here keeps the compiler from moving the next iteration's work
+      // in among these memory instructions (measured: that interleaving made the
+      // launch ~7% slower; a plain memory clobber is not enough, a branch is).
+      if (p == 0) asm volatile("" ::: "memory");
     }
   } else {
     // =================================================== consumer warps 8-15
@@ -855,31 +862,31 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       }
       named_sync(kBarC, kGroup);  // Gram rows stored, [T; W] operand zeroed
 
-      // Warps 8 and 9 (lanes 0-63: the key rows) form R while four others solve for
-      // T and W, one on each scheduler (the solve needs only the Gram rows and the
-      // metadata); warps 14 and 15 wait.
-      // ---- R = diag(b)(V - e^G K S0) as a bf16 hi/lo operand, all 128 columns
+      // Key-lane warps form R while the query-lane warps solve for T and W (the
+      // solve needs only the Gram rows and the metadata).
+      // ---- R = diag(b)(V - e^G K S0) as a bf16 hi/lo operand (key lanes, a column
+      // half per warp); the K S0 columns are zeroed once read: the second product
+      // accumulates U = T R there
       bool v_ok = true;
-      if (cw < 2) {
+      if (key_lane) {
         v_ok = mbar_wait_suspend(&sh.v_bar, nv & 1, abort);
         const bool live = lane_node < N;
         const float eG = live ? __expf(M.G[lane_node]) : 0.f;
         const float bn = live ? M.bb[lane_node] : 0.f;
 #pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {  // 32 value columns at a time
-          const int half = qq >> 1, q = qq & 1;
+        for (int q = 0; q < 2; ++q) {  // 32 value columns at a time
           float r[32];
-          tmem_ld32(tb + lane_base + half * 64 + q * 32, r);
+          tmem_ld32(tb + lane_base + chalf * 64 + q * 32, r);
           tmem_ld_wait();
-          {  // these K S0 columns become the accumulator of U = T R
+          {
             float z[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) z[i] = 0.f;
-            tmem_st32(tb + lane_base + half * 64 + q * 32, z);
+            tmem_st32(tb + lane_base + chalf * 64 + q * 32, z);
           }
 #pragma unroll
           for (int c8 = 0; c8 < 4; ++c8) {  // 8 columns per 16-byte bf16 chunk
-            const int off = half * 8192 + atom_off(lane_node, q * 4 + c8);
+            const int off = chalf * 8192 + atom_off(lane_node, q * 4 + c8);
             const uint4 vv = *reinterpret_cast<const uint4*>(smem + kOffRlo + off);
             const __nv_bfloat162* vb = reinterpret_cast<const __nv_bfloat162*>(&vv);
             float xr[8];
@@ -896,18 +903,19 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
           }
         }
         tmem_st_wait();
-        // the R warps wait for the solve from here on: the next item's first product
-        // goes in now if its operands are ready, so that it has completed before this
-        // item's second product needs the tensor cores
+        // the key-lane warps wait for the solve from here on: the next item's first
+        // product goes in now if its operands are ready, so that it has completed
+        // before this item's second product needs the tensor cores
         if (c == 0 && next < i_end && p1_next == j + 1 && issue_p1(j + 1, false)) ++p1_next;
-      } else if (cw < 6) {
-        // ---- the rows of T (warps 10 and 12) and of W (warps 11 and 13), one row per
-        // thread.  Rows are handed out in topological order: warps 10 and 11 take the
-        // first 32 positions, warps 12 and 13 (the other two schedulers) the deeper 32.
+      } else {
+        // ---- the rows of T (lane quarter 2) and of W (lane quarter 3), one row per
+        // thread.  Rows are handed out in topological order: the column-half-0 warps
+        // take the first 32 positions, the others the deeper 32, so each scheduler
+        // runs one shallow and one deep solve.
         const float* KK = reinterpret_cast<const float*>(smem + kOffKK);
         const float* QK = reinterpret_cast<const float*>(smem + kOffQK);
-        const bool t_row = (cw & 1) == 0;
-        const int spos = (cw >> 2) * 32 + (c & 31);
+        const bool t_row = lq == 2;
+        const int spos = chalf * 32 + (c & 31);
         const bool act = spos < N;
         const int sn = act ? M.ord[spos] : 0;
         const int dn = act ? M.dep[sn] : -1;
@@ -940,6 +948,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         }
         umma_commit(&sh.mma2_bar);
         sh.mma2_issued += 1;
+        // (another chance for the next item's first product, behind this product)
+        if (next < i_end && p1_next == j + 1 && issue_p1(j + 1, false)) ++p1_next;
       }
       const bool done2 = group_wait(&sh.mma2_bar, mma2_count & 1, kBarC, c == 0, abort);
       ++mma2_count;
