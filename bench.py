@@ -45,10 +45,20 @@ METRIC = "verified tree nodes/sec per GDN layer (1 GB300); achieved HBM GB/s % o
 UNIT = "nodes/s/layer"
 S0_BYTES_PER_SEQ = 32 * 128 * 128 * 4                     # one layer's state of one sequence
 NODE_BYTES = 2 * 16 * 128 * 2 + 32 * 128 * 2 + 2 * 32 * 4 + 32 * 128 * 2   # q,k,v,g,b in + o out
-# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant kernel, from the
-# ncu capture summarised in profiles/verify_tc_stack36_layer.md (fused step).  Reset to None
-# whenever that kernel changes, until it is captured again.
-PROFILED_TRAFFIC = {"fused": 107_537_152 + 58_144_256, "separate": None}
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant kernel from an ncu
+# capture, with the first 16 hex digits of the SHA-256 of the kernel source it was taken on;
+# the line reports it only while the source still has that hash (null otherwise).
+PROFILED_TRAFFIC = {"fused": (None, ""), "separate": (None, "")}
+KERNEL_SOURCE = os.path.join(ROOT, "tree_speculative_decoding_gated_gb300", "csrc", "verify_tc.cu")
+
+
+def profiled_traffic(mode: str):
+    import hashlib
+    value, digest = PROFILED_TRAFFIC[mode]
+    if value is None:
+        return None
+    with open(KERNEL_SOURCE, "rb") as f:
+        return value if hashlib.sha256(f.read()).hexdigest()[:16] == digest else None
 
 
 def parse():
@@ -62,6 +72,8 @@ def parse():
                          "next step's inputs while the current step runs)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the one-layer workload summary of the default line")
     ap.add_argument("--cpu-sample-seqs", type=int, default=4)
     ap.add_argument("--layers", type=int, default=36,
                     help="GDN layers per step (fewer only for small profiler captures)")
@@ -237,42 +249,32 @@ def run_gpu(args, rank, world, local):
             for _ in range(n_ws)]
 
     stream = torch.cuda.Stream(device)
-    ev = {"v0": [torch.cuda.Event(enable_timing=True) for _ in range(L)],
-          "v1": [torch.cuda.Event(enable_timing=True) for _ in range(L)],
-          "c0": [torch.cuda.Event(enable_timing=True) for _ in range(L)],
-          "c1": [torch.cuda.Event(enable_timing=True) for _ in range(L)]}
 
-    def step_separate(r: int, timed_kernels=False):
+    def step_separate(r: int, verifies_only=False, commits_only=False):
         inp = inputs[r]
-        tgdn.tree_prep(inp.tree, stream)
+        if not commits_only:
+            if not verifies_only:
+                tgdn.tree_prep(inp.tree, stream)
+            for l in range(L):
+                tgdn.verify(inp.tree, dims, inp.q[l], inp.k[l], inp.v[l], inp.g[l], inp.b[l],
+                            states[l], outs[l], ws[0][l], stream)
+            if verifies_only:
+                return
+            tgdn.accept(inp.tree, inp.draft, inp.target, an[0], al[0], path[0], stream)
         for l in range(L):
-            if timed_kernels:
-                ev["v0"][l].record(stream)
-            tgdn.verify(inp.tree, dims, inp.q[l], inp.k[l], inp.v[l], inp.g[l], inp.b[l],
-                        states[l], outs[l], ws[0][l], stream)
-            if timed_kernels:
-                ev["v1"][l].record(stream)
-        tgdn.accept(inp.tree, inp.draft, inp.target, an[0], al[0], path[0], stream)
-        for l in range(L):
-            if timed_kernels:
-                ev["c0"][l].record(stream)
             tgdn.commit(inp.tree, dims, an[0], inp.k[l], ws[0][l], states[l], states[l], stream)
-            if timed_kernels:
-                ev["c1"][l].record(stream)
 
-    def step_fused(r: int, timed_kernels=False):
+    def step_fused(r: int, verifies_only=False):
         inp, pr = inputs[r], (r - 1) % R
         prev = inputs[pr]
-        tgdn.tree_prep(inp.tree, stream)
+        if not verifies_only:
+            tgdn.tree_prep(inp.tree, stream)
         for l in range(L):
-            if timed_kernels:
-                ev["v0"][l].record(stream)
             tgdn.verify_fused(inp.tree, dims, inp.q[l], inp.k[l], inp.v[l], inp.g[l], inp.b[l],
                               states[l], outs[l], ws[r][l], prev.tree, an[pr], path[pr],
                               prev.k[l], ws[pr][l], stream)
-            if timed_kernels:
-                ev["v1"][l].record(stream)
-        tgdn.accept(inp.tree, inp.draft, inp.target, an[r], al[r], path[r], stream)
+        if not verifies_only:
+            tgdn.accept(inp.tree, inp.draft, inp.target, an[r], al[r], path[r], stream)
 
     def first_step(r: int):
         """A plain verify + accept of input r, so that the step after it has a commit pending."""
@@ -298,6 +300,11 @@ def run_gpu(args, rank, world, local):
             with torch.cuda.graph(g, stream=stream):
                 step(r)
             graphs.append(g)
+        # the verify launches of one step alone (as in the step graph, programmatic
+        # dependent launch between them), for the dominant kernel's per-launch time
+        vgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(vgraph, stream=stream):
+            step(0, verifies_only=True)
         if fused:                 # leave input R - 1 as the last step run
             for r in range(R):
                 step(r)
@@ -310,13 +317,15 @@ def run_gpu(args, rank, world, local):
         torch.cuda.synchronize()
 
     def timed(fn, K, W):
+        """W warm-up steps, then K timed ones; step s runs input s % R, so the inputs follow
+        each other in order across the warm-up and the timed region."""
         for s in range(W):
             fn(s)
         barrier()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
-        for s in range(K):
+        for s in range(W, W + K):
             fn(s)
         t1.record(stream)
         barrier()
@@ -325,9 +334,9 @@ def run_gpu(args, rank, world, local):
     clocks = ClockSampler(local)
     clocks.start()
     torch.cuda.nvtx.range_push("timed")
-    # W + K replays from input 0 on; with W + K a multiple of R the last replay is input R - 1
-    K = args.steps
-    W = args.warmup + (-(args.warmup + K)) % R
+    # W warm-up and K timed replays in input order from input 0 (the setup left input
+    # R - 1 as the last step run, so each step commits its predecessor's acceptance)
+    K, W = args.steps, args.warmup
 
     def replay(s):
         with torch.cuda.stream(stream):   # a graph replays on the current stream
@@ -336,26 +345,36 @@ def run_gpu(args, rank, world, local):
     ms = timed(replay, K, W)
     torch.cuda.nvtx.range_pop()
     clk = clocks.stop()
+    with torch.cuda.stream(stream):       # end again on input R - 1 (for the legs below)
+        for s in range(W + K, W + K + (-(W + K)) % R):
+            graphs[s % R].replay()
+    stream.synchronize()
 
-    # Per-kernel durations: the same step run eagerly with CUDA events around every launch.
-    # A spin kernel first holds the stream so that all launches of the step are queued
-    # before the GPU reaches them: they then run back to back, as in the graph.
-    kv, kc = [], []
-    for s in range(max(3, min(K, 8))):
-        r = s % R
+    # The dominant kernel's launch time: the graph of one step's verify launches replayed
+    # (back to back, as inside the step graph), divided by the launches it holds.
+    def graph_us(g, n, reps=10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
-            torch.cuda._sleep(50_000_000)
-            step(r, timed_kernels=True)
+            g.replay()
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
         stream.synchronize()
-        kv += [ev["v0"][l].elapsed_time(ev["v1"][l]) for l in range(L)]
-        if not fused:
-            kc += [ev["c0"][l].elapsed_time(ev["c1"][l]) for l in range(L)]
-    if fused and (max(3, min(K, 8)) % R):   # end again on input R - 1 (for the e2e leg)
+        return 1e3 * e0.elapsed_time(e1) / (reps * n)
+
+    verify_us = graph_us(vgraph, L)
+    if not fused:
+        cgraph = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
-            for r in range(max(3, min(K, 8)) % R, R):
-                step(r)
+            with torch.cuda.graph(cgraph, stream=stream):
+                step_separate(0, commits_only=True)
+        commit_us = graph_us(cgraph, L)
+    if fused:                              # the verify-only replays used input 0's step
+        with torch.cuda.stream(stream):
+            for r in range(1, R):
+                graphs[r].replay()
         stream.synchronize()
-    verify_us = 1e3 * statistics.mean(kv)
 
     total_nodes = L * B * Nn * K * world
     value = total_nodes / (ms / 1e3)
@@ -370,7 +389,6 @@ def run_gpu(args, rank, world, local):
                    bytes=fv_bytes, gbs=fv_bytes / (verify_us * 1e-6) / 1e9)
         other = None
     else:
-        commit_us = 1e3 * statistics.mean(kc)
         v_gbs = verify_bytes / (verify_us * 1e-6) / 1e9
         c_gbs = commit_bytes / (commit_us * 1e-6) / 1e9
         vd = dict(kernel="verify_tc_kernel", us=verify_us, bytes=verify_bytes, gbs=v_gbs)
@@ -386,7 +404,7 @@ def run_gpu(args, rank, world, local):
                  if fused else f"prep + {L} verify + accept + {L} in-place commit")
     roof = {"bound": "hbm", "kernel": dom["kernel"], "achieved": dom["gbs"], "peak": hbm,
             "peak_kind": peak_kind, "unit": "GB/s", "frac": dom["gbs"] / hbm,
-            "traffic": PROFILED_TRAFFIC[args.mode],
+            "traffic": profiled_traffic(args.mode),
             "algorithmic_bytes_per_launch": dom["bytes"], "launch_us": dom["us"]}
     if other is not None:
         roof["other"] = {"kernel": other["kernel"], "achieved": other["gbs"],
@@ -397,7 +415,9 @@ def run_gpu(args, rank, world, local):
         "warmup": W, "ms_per_step": ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{L}-layer GDN stack, B={B} per GPU, 64-node random trees "
-                               f"(depth<=12), H_qk=16 H_v=32 d=128, 50-step decode",
+                               f"(depth<=12), H_qk=16 H_v=32 d=128; {K} decode steps timed "
+                               f"after {W} warm-up steps",
+                   "timed_steps": K, "warmup_steps": W,
                    "layers": L, "batch_per_gpu": B, "nodes_per_tree": Nn, "depth_max": 12,
                    "H_qk": 16, "H_v": 32, "d_k": 128, "d_v": 128, "io": "bf16",
                    "state": "fp32", "accumulate": "fp32", "mode": args.mode,
@@ -452,8 +472,8 @@ def run_e2e(args, inputs, graphs, stream, an, al, path, timed, torch, R, L, B, N
                 ev_done[r].record(stream)
                 done_recorded[r] = True
 
-    # warm-up ends on input R - 1, so that the first timed step's pending commit is its own
-    ms = timed(fn, args.steps, args.warmup + (-args.warmup) % R)
+    # the previous leg ended on input R - 1, so step 0 (input 0) commits its own predecessor
+    ms = timed(fn, args.steps, args.warmup)
     value = L * B * Nn * args.steps * world / (ms / 1e3)
     return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": ms / args.steps,
@@ -502,11 +522,23 @@ def cpu_baseline(min_seconds: float = 10.0, max_layers: int = 36):
         dt += time.perf_counter() - t0
         nodes += t.T
         layers += 1
+    # one core, on 2 sequences of layer 0 (the same work per node)
+    p = synth.select_sequences(synth.make_problem(CONFIG, step=0, layer=0), range(2))
+    t, i = p.trees, p.inputs
+    t0 = time.perf_counter()
+    oracle.verify(t.cu_nodes, t.parent, t.n_max, t.depth_max, i.q, i.k, i.v, i.g, i.b, p.S0, 1)
+    acc = oracle.accept(t.cu_nodes, t.parent, t.n_max, t.depth_max, p.draft_ids, p.target_ids)
+    oracle.commit(t.cu_nodes, t.parent, t.n_max, t.depth_max, i.k, i.v, i.g, i.b, p.S0,
+                  acc["accept_node"], 1)
+    dt1 = time.perf_counter() - t0
     return {"value": nodes / dt, "unit": UNIT, "cores": used, "kind": "oracle",
             "sample": f"{layers} of 36 layers of step 0, all {cfg.B} sequences x 64 nodes x "
                       f"32 v-heads: verify + accept + commit by fp64 path replay "
                       f"({dt:.1f} s)",
-            "seconds": dt}
+            "seconds": dt,
+            "one_core": {"value": t.T / dt1, "unit": UNIT, "cores": 1,
+                         "sample": f"2 sequences of layer 0, step 0 ({t.T} nodes x 32 v-heads, "
+                                   f"{dt1:.1f} s)"}}
 
 
 def run_reference(args, rank, world):
@@ -685,6 +717,83 @@ def run_attention_times(args):
             "peak_hbm_gbs": hbm, "peak_kind": kind, "cases": out}
 
 
+def per_config_summary(hbm):
+    """Verify and commit per launch on the one-layer workloads of 16 sequences of 64-node
+    trees and of 64 mixed sequences (17-node chains and 129-node trees), L2 flushed before
+    every launch, as fractions of the measured HBM bandwidth; and single-pass vs
+    per-branch recurrent verification at tree size 128."""
+    import torch
+    from tree_speculative_decoding_gated_gb300 import tgdn
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(dev)
+    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    out = {}
+    for name in ("cfg3", "cfg4"):
+        cfg = synth.CONFIGS[name]
+        trees = synth.make_trees(cfg, 0)
+        tree = tgdn.Tree.from_host(trees.cu_nodes, trees.parent, trees.n_max, trees.depth_max,
+                                   dev)
+        dims = tgdn.Dims(cfg.H_qk, cfg.H_v, cfg.dk, cfg.dv, tgdn.BF16)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(synth.BASE_SEED + cfg.number + 1000)
+        q, k, v, g, b = synth.make_node_inputs_device(cfg, trees.T, gen, dev)
+        S0 = synth.make_state_device(cfg, trees.B, gen, dev)
+        o = torch.empty((trees.T, cfg.H_v, cfg.dv), dtype=torch.bfloat16, device=dev)
+        ws = tgdn.alloc_workspace(tree, dims, dev)
+        S = torch.empty_like(S0)
+        an = torch.zeros(trees.B, dtype=torch.int32, device=dev)
+        with torch.cuda.stream(stream):
+            tgdn.tree_prep(tree, stream)
+        fv = lambda: tgdn.verify(tree, dims, q, k, v, g, b, S0, o, ws, stream)
+        fc = lambda: tgdn.commit(tree, dims, an, k, ws, S0, S, stream)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fv()
+                fc()
+        tv = _launch_times(torch, stream, fv, 20, flush)
+        tcm = _launch_times(torch, stream, fc, 20, flush)
+        vb = trees.B * S0_BYTES_PER_SEQ + trees.T * NODE_BYTES
+        cb = 2 * trees.B * S0_BYTES_PER_SEQ
+        out[name] = {"verify_us": tv, "verify_frac_hbm": vb / (tv * 1e-6) / 1e9 / hbm,
+                     "commit_us": tcm, "commit_frac_hbm": cb / (tcm * 1e-6) / 1e9 / hbm}
+    out["recurrent_vs_single_pass_128"] = recurrent_ratio(128)
+    return out
+
+
+def recurrent_ratio(n_nodes: int):
+    """Per-branch recurrent over single-pass verification time, one layer of 16 sequences of
+    n_nodes-node random trees (depth <= 16), L2 flushed before every launch."""
+    import torch
+    from tree_speculative_decoding_gated_gb300 import tgdn
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(dev)
+    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    cfg = synth.CONFIGS["cfg3"]
+    rng = np.random.default_rng(synth.BASE_SEED + 78)
+    parents = [synth.random_recursive_tree(rng, n_nodes, 16) for _ in range(16)]
+    trees = synth.pack_trees(parents, n_nodes, 16)
+    tree = tgdn.Tree.from_host(trees.cu_nodes, trees.parent, trees.n_max, trees.depth_max, dev)
+    dims = tgdn.Dims(cfg.H_qk, cfg.H_v, cfg.dk, cfg.dv, tgdn.BF16)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(synth.BASE_SEED + 77)
+    q, k, v, g, b = synth.make_node_inputs_device(cfg, trees.T, gen, dev)
+    S0 = synth.make_state_device(cfg, 16, gen, dev)
+    o = torch.empty((trees.T, cfg.H_v, cfg.dv), dtype=torch.bfloat16, device=dev)
+    ws = tgdn.alloc_workspace(tree, dims, dev)
+    with torch.cuda.stream(stream):
+        tgdn.tree_prep(tree, stream)
+    f1 = lambda: tgdn.verify(tree, dims, q, k, v, g, b, S0, o, ws, stream)
+    f2 = lambda: tgdn.verify_recurrent(tree, dims, q, k, v, g, b, S0, o, stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            f1()
+            f2()
+    t1 = _launch_times(torch, stream, f1, 10, flush)
+    t2 = _launch_times(torch, stream, f2, 10, flush)
+    return {"nodes": n_nodes, "single_pass_us": t1, "recurrent_us": t2, "ratio": t2 / t1,
+            "pages": "7.1x at tree size 128 on a B200 (Experimentelle Ergebnisse)"}
+
+
 def run_config_times(args):
     """tgdn_verify and tgdn_commit per launch on the single-layer workloads (one B=1 top-4
     tree; 16 x 64-node random trees; 64 mixed chains and 129-node top-8 trees), against the
@@ -769,6 +878,8 @@ def main():
         torch.cuda.set_device(local)
         torch.distributed.init_process_group("nccl")
     res = run_gpu(args, rank, world, local)
+    if rank == 0 and world == 1 and not args.no_per_config:
+        res["per_config"] = per_config_summary(peaks()[0])
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline()
     if rank == 0:

@@ -313,9 +313,11 @@ int tgdn_verify_fused(const tgdn_tree* tree, const tgdn_dims* dims, const void* 
  *   - Sizes: tgdn_verify_workspace_bytes(tree, dims) must not exceed
  *     TGDN_NOALLOC_SCRATCH_BYTES, otherwise TGDN_ETOOBIG is returned and
  *     nothing is enqueued.
- *   - Device: the stream must belong to the current device.  The first call
- *     on each device looks up the array's device address (cudaGetSymbolAddress)
- *     with that device current; make that first call before any stream capture.
+ *   - Device: every call looks up the array's device address
+ *     (cudaGetSymbolAddress) in the calling thread's current context, so the stream
+ *     must belong to that context's device.  The first call on a device may load
+ *     the library's device code (which holds the array); make it before any
+ *     stream capture.
  *   - Sharing: every call on a device uses the same array and leaves its
  *     contents behind.  Calls whose kernels overlap on the GPU (different
  *     streams without ordering) race on it; order them on one stream.
@@ -327,6 +329,22 @@ int tgdn_verify_fused(const tgdn_tree* tree, const tgdn_dims* dims, const void* 
 int tgdn_verify_noalloc(const tgdn_tree* tree, const tgdn_dims* dims, const void* q,
                         const void* k, const void* v, const float* g, const float* b,
                         const float* S0, void* o, tgdn_stream_t stream);
+
+/* Test hook for the bounded device waits; the paper has no counterpart and it is
+ * not meant for production use.  Every device wait of the library gives up after
+ * 2 s, marks the affected sequences TGDN_SEQ_TIMEOUT and lets the kernel return
+ * (nothing traps or hangs).  From the next launch on, the tensor-core verification
+ * kernel for trees of at most 64 nodes (tgdn_verify, tgdn_verify_fused,
+ * tgdn_verify_noalloc) uses wait_limit_ns instead (0: the 2 s default), and when
+ * withhold_item >= 0 its producer warps never hand over the operands of work item
+ * withhold_item (sequence withhold_item / H_v, value head withhold_item % H_v), so
+ * that the consumer's wait for them expires: the CTA that owns that item stops,
+ * reports every item it owns as TGDN_SEQ_TIMEOUT, waits for its own copies and
+ * products to finish and returns; other CTAs are unaffected.  Process-wide, not
+ * thread-safe with concurrent launches; tgdn_debug_set_wait_hooks(0, -1) restores
+ * the defaults.  Returns TGDN_OK, or TGDN_EINVAL for wait_limit_ns above 2 s or
+ * withhold_item < -1. */
+int tgdn_debug_set_wait_hooks(uint64_t wait_limit_ns, int32_t withhold_item);
 
 /* Static, human-readable text for a tgdn_status value. */
 const char* tgdn_status_string(int code);

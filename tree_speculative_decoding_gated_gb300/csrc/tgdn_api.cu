@@ -1,7 +1,10 @@
 // tgdn_api.cu — the C ABI (include/tgdn.h): host-side argument checks,
 // kernel selection and TMA descriptor encoding.  No call allocates memory.
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
+#include <atomic>
+#include <cmath>
 #include <mutex>
 
 #include "tgdn_device.cuh"
@@ -10,6 +13,13 @@
 namespace {
 
 using tgdn::WsLayout;
+
+// An NVTX range around each call of the C ABI (a no-op unless a profiler listens), so
+// that a timeline shows which library call enqueued which kernels.
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+};
 
 int check_tree(const tgdn_tree* t) {
   if (!t) return TGDN_EINVAL;
@@ -80,6 +90,28 @@ bool encode_rows_map(CUtensorMap* map, const void* base, long rows, int H, int b
 
 namespace tgdn {
 
+namespace {
+std::atomic<unsigned long long> g_hook_wait_ns{0};
+std::atomic<int> g_hook_item{-1};
+}  // namespace
+
+WaitHooks wait_hooks() { return WaitHooks{g_hook_wait_ns.load(), g_hook_item.load()}; }
+
+int device_sm_count() {
+  constexpr int kDevices = 64;
+  static std::atomic<int> cache[kDevices];  // 0: not looked up yet
+  int dev = 0, c = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev >= 0 && dev < kDevices) {
+    const int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+  }
+  if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c < 1)
+    return 1;
+  if (dev >= 0 && dev < kDevices) cache[dev].store(c, std::memory_order_relaxed);
+  return c;
+}
+
 bool encode_out_maps(OutMaps* m, float* U, void* o, int T, int H_v) {
   auto fn = encode_fn();
   if (!fn || T < 1) return false;
@@ -106,6 +138,13 @@ extern "C" {
 
 int tgdn_version(void) { return 100; }
 
+int tgdn_debug_set_wait_hooks(uint64_t wait_limit_ns, int32_t withhold_item) {
+  if (wait_limit_ns > tgdn::kWaitLimitNs || withhold_item < -1) return TGDN_EINVAL;
+  tgdn::g_hook_wait_ns.store(wait_limit_ns);
+  tgdn::g_hook_item.store(withhold_item);
+  return TGDN_OK;
+}
+
 const char* tgdn_status_string(int code) {
   switch (code) {
     case TGDN_OK: return "ok";
@@ -118,6 +157,7 @@ const char* tgdn_status_string(int code) {
 }
 
 int tgdn_tree_prep(const tgdn_tree* tree, tgdn_stream_t stream) {
+  CallRange range_("tgdn_tree_prep");
   int rc = check_tree(tree);
   if (rc != TGDN_OK) return rc;
   return from_cuda(tgdn::launch_tree_prep(*tree, reinterpret_cast<cudaStream_t>(stream)));
@@ -131,6 +171,7 @@ size_t tgdn_verify_workspace_bytes(const tgdn_tree* tree, const tgdn_dims* dims)
 int tgdn_verify(const tgdn_tree* tree, const tgdn_dims* dims, const void* q, const void* k,
                 const void* v, const float* g, const float* b, const float* S0, void* o,
                 void* ws, tgdn_stream_t stream) {
+  CallRange range_("tgdn_verify");
   int rc = check_tree(tree);
   if (rc != TGDN_OK) return rc;
   rc = check_dims(dims);
@@ -184,6 +225,7 @@ int tgdn_verify_fused(const tgdn_tree* tree, const tgdn_dims* dims, const void* 
                       void* o, void* ws, const tgdn_tree* prev_tree,
                       const int32_t* prev_accept_node, const int32_t* prev_path,
                       const void* prev_k, const void* prev_ws, tgdn_stream_t stream) {
+  CallRange range_("tgdn_verify_fused");
   int rc = check_tree(tree);
   if (rc != TGDN_OK) return rc;
   rc = check_tree(prev_tree);
@@ -241,6 +283,7 @@ int tgdn_verify_fused(const tgdn_tree* tree, const tgdn_dims* dims, const void* 
 int tgdn_verify_recurrent(const tgdn_tree* tree, const tgdn_dims* dims, const void* q,
                           const void* k, const void* v, const float* g, const float* b,
                           const float* S0, void* o, tgdn_stream_t stream) {
+  CallRange range_("tgdn_verify_recurrent");
   int rc = check_tree(tree);
   if (rc != TGDN_OK) return rc;
   rc = check_dims(dims);
@@ -257,6 +300,7 @@ int tgdn_tree_build(int32_t B, int32_t budget, int32_t K, int32_t w, int32_t dep
                     const int32_t* root_token, const float* child_logp,
                     const int32_t* child_token, int32_t* parent, int32_t* token, float* score,
                     int32_t* depth, int32_t* n_nodes, int32_t* rounds, tgdn_stream_t stream) {
+  CallRange range_("tgdn_tree_build");
   if (B < 0 || budget < 1 || K < 1 || w < 1 || depth_max < 0) return TGDN_EINVAL;
   if (budget > TGDN_MAX_NODES || K > TGDN_BUILD_MAX_K || depth_max > TGDN_MAX_DEPTH)
     return TGDN_ETOOBIG;
@@ -282,11 +326,12 @@ int tgdn_tree_attention(const tgdn_tree* tree, int32_t H_q, int32_t H_kv, int32_
                         const void* k_cache, const void* v_cache, const int32_t* prefix_len,
                         int32_t P_max, float scale, void* o, void* ws, size_t ws_bytes,
                         tgdn_stream_t stream) {
+  CallRange range_("tgdn_tree_attention");
   int rc = check_tree(tree);
   if (rc != TGDN_OK) return rc;
   const tgdn_tree& t = *tree;
   if (H_q < 1 || H_kv < 1 || H_q % H_kv != 0 || d < 1 || P_max < 0) return TGDN_EINVAL;
-  if (!(scale > 0.f && scale <= 3.0e38f)) return TGDN_EINVAL;  // positive and finite
+  if (!(scale > 0.f && isfinite(scale))) return TGDN_EINVAL;  // positive and finite
   if (!tgdn::tree_attn_supported(t, H_q, H_kv, d)) return TGDN_EUNSUPPORTED;
   if (t.B > 0 && (!prefix_len || (P_max > 0 && (!k_cache || !v_cache)))) return TGDN_EINVAL;
   if (t.T > 0 && (!q || !k_tree || !v_tree || !o)) return TGDN_EINVAL;
@@ -315,6 +360,7 @@ int tgdn_tree_attention(const tgdn_tree* tree, int32_t H_q, int32_t H_kv, int32_
 int tgdn_accept(const tgdn_tree* tree, const int32_t* draft_ids, const int32_t* target_ids,
                 int32_t* accept_node, int32_t* accept_len, int32_t* path,
                 tgdn_stream_t stream) {
+  CallRange range_("tgdn_accept");
   int rc = check_tree(tree);
   if (rc != TGDN_OK) return rc;
   if (tree->B > 0 && (!accept_node || !accept_len || !path)) return TGDN_EINVAL;
@@ -326,6 +372,7 @@ int tgdn_accept(const tgdn_tree* tree, const int32_t* draft_ids, const int32_t* 
 int tgdn_commit(const tgdn_tree* tree, const tgdn_dims* dims, const int32_t* accept_node,
                 const void* k, const void* ws, const float* S_in, float* S_out,
                 tgdn_stream_t stream) {
+  CallRange range_("tgdn_commit");
   int rc = check_tree(tree);
   if (rc != TGDN_OK) return rc;
   rc = check_dims(dims);
@@ -361,23 +408,14 @@ namespace {
 // looked up once per device with cudaGetSymbolAddress and passed to kernels.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[TGDN_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kMaxDevices] = {};
-
-// Device address of the array on the current device (set up on first use).
+// Device address of the array in the current context.  It is looked up on every
+// call (cheap once the library's device code is loaded): an address cached per
+// device would go stale after cudaDeviceReset or under another context.
 int noalloc_scratch(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return TGDN_ECUDA;
-  if (dev < 0 || dev >= kMaxDevices) return TGDN_EUNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
-      return TGDN_ECUDA;
-    g_noalloc_ptr[dev] = p;
-  }
-  *out = g_noalloc_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+    return TGDN_ECUDA;
+  *out = p;
   return TGDN_OK;
 }
 
@@ -387,6 +425,7 @@ extern "C" int tgdn_verify_noalloc(const tgdn_tree* tree, const tgdn_dims* dims,
                                    const void* k, const void* v, const float* g,
                                    const float* b, const float* S0, void* o,
                                    tgdn_stream_t stream) {
+  CallRange range_("tgdn_verify_noalloc");
   int rc = check_tree(tree);
   if (rc != TGDN_OK) return rc;
   rc = check_dims(dims);

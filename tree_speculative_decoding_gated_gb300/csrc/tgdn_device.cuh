@@ -31,7 +31,8 @@ template <> struct Io<__nv_bfloat16> {
 
 // ---------------------------------------------------------------- time bound
 // Every device wait in this library gives up after this many nanoseconds of
-// global time, marks the sequence TGDN_SEQ_TIMEOUT and unwinds.
+// global time (or a shorter limit a kernel is given), marks the sequence
+// TGDN_SEQ_TIMEOUT and unwinds.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ uint64_t global_ns() {
@@ -73,13 +74,14 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete; false on expiry.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_test(bar, parity)) return true;
     if ((it & 63u) == 0) {
-      if (global_ns() - t0 > kWaitLimitNs) return false;
+      if (global_ns() - t0 > limit_ns) return false;
       __nanosleep(64);
     }
   }
@@ -100,15 +102,16 @@ __device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
 }
 
 // Suspending wait for one thread; false when *abort is raised elsewhere or
-// after kWaitLimitNs (then it raises *abort itself).
+// after limit_ns (then it raises *abort itself).
 __device__ __forceinline__ bool mbar_wait_suspend(uint64_t* bar, uint32_t parity,
-                                                  volatile int* abort) {
+                                                  volatile int* abort,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
     if (mbar_try(bar, parity)) return true;
     if (*abort) return false;
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (global_ns() - t0 > limit_ns) {
       *abort = 1;
       return false;
     }

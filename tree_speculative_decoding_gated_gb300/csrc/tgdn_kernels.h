@@ -10,6 +10,10 @@
 
 namespace tgdn {
 
+// Streaming multiprocessors of the current device (cached per device; safe to call
+// from several host threads).  1 if the device cannot be queried.
+int device_sm_count();
+
 // Workspace layout shared by verify (writer) and commit (reader).
 struct WsLayout {
   size_t u_off, g_off, bytes;
@@ -72,6 +76,14 @@ struct OutMaps {
   CUtensorMap u64, u8, o64, o8;
 };
 bool encode_out_maps(OutMaps* m, float* U, void* o, int T, int H_v);
+// Test hooks of the bounded device waits (tgdn_debug_set_wait_hooks): a shorter wait
+// limit (0: the default) and a work item whose hand-over the 64-node kernel's producer
+// withholds (-1: none).
+struct WaitHooks {
+  uint64_t wait_ns;
+  int hold_item;
+};
+WaitHooks wait_hooks();
 // Whether the tensor-core verify can also apply a pending commit of `prev`.
 bool pending_commit_tc_supported(const tgdn_tree& prev, const void* prev_k);
 // With cm.path set, S is first updated in place by the pending commit and the

@@ -528,18 +528,6 @@ tree_attn_combine_kernel(const AtArgs a) {
   }
 }
 
-static int at_sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0, c = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && c > 0)
-      n = c;
-    else
-      return 1;
-  }
-  return n;
-}
 
 // Context splits for this launch: enough CTAs for one per SM, at most 8, and at
 // least 1024 cached positions per split, below which the merge costs more than the
@@ -548,7 +536,7 @@ static int attn_splits(const tgdn_tree& t, int H_q, int H_kv, int P_max) {
   const int G = H_q / H_kv;
   const long items = (long)t.B * H_kv * ((t.n_max * G + kAtRows - 1) / kAtRows);
   if (items <= 0) return 1;
-  long s = (long)at_sm_count() / items;
+  long s = (long)device_sm_count() / items;
   const long ctx_tiles = (P_max + kAtKeys - 1) / kAtKeys;
   if (s > 8) s = 8;
   if (s > ctx_tiles / (1024 / kAtKeys)) s = ctx_tiles / (1024 / kAtKeys);

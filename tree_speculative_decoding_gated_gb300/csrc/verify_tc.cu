@@ -171,9 +171,9 @@ __device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo) {
 // rest of the group parks on the group's hardware barrier, which also makes
 // the outcome the same for every thread of the group.
 __device__ __forceinline__ bool group_wait(uint64_t* bar, uint32_t parity, int bar_id,
-                                           bool leader, volatile int* abort) {
+                                           bool leader, volatile int* abort, uint64_t limit_ns) {
   bool ok = true;
-  if (leader) ok = mbar_wait_suspend(bar, parity, abort);
+  if (leader) ok = mbar_wait_suspend(bar, parity, abort, limit_ns);
   return named_sync_and(bar_id, kGroup, ok);
 }
 
@@ -314,7 +314,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                  int32_t* __restrict__ status,
                  const float* __restrict__ g, const float* __restrict__ bta, float* S,
                  __nv_bfloat16* __restrict__ o, float* __restrict__ Uws,
-                 float* __restrict__ Gws, const PendingCommit cm) {
+                 float* __restrict__ Gws, const PendingCommit cm, const uint64_t wait_ns,
+                 const int hold_item) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -527,7 +528,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       // commit operands
       bool step_ok = true;
       if (p == 0 && !skip) {
-        if (npr > 0) step_ok = mbar_wait_suspend(&sh.mma1_bar, (npr - 1) & 1, abort);
+        if (npr > 0) step_ok = mbar_wait_suspend(&sh.mma1_bar, (npr - 1) & 1, abort, wait_ns);
         if (step_ok) issue_kq(item, lo);
       }
       if (!named_sync_and(kBarP, kGroup, step_ok && !*abort)) break;
@@ -582,7 +583,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
           umma_commit(&sh.cmt_bar);
           sh.cmt_issued += 1;
         }
-        if (!group_wait(&sh.cmt_bar, ncm & 1, kBarP, p == 0, abort)) break;
+        if (!group_wait(&sh.cmt_bar, ncm & 1, kBarP, p == 0, abort, wait_ns)) break;
         ++ncm;
         tc_fence_after_sync();
         const float decay = __expf(Gstar);
@@ -615,11 +616,13 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       named_sync(kBarP, kGroup);  // the S operand is complete
       if (p == 0) {
         sh.op_skip[slot] = skip ? 1 : 0;
-        mbar_arrive(&sh.op_ready[slot]);  // the consumer's issuing thread takes it from here
+        // (a test hook can withhold one item's hand-over: the consumer's bounded wait
+        // for it then expires)
+        if (item != hold_item) mbar_arrive(&sh.op_ready[slot]);
       }
       // the consumer has finished item j-2, the previous user of this half and slot
       // (every wait is agreed on by the whole group before anyone leaves the loop)
-      if (j >= 2 && !group_wait(&sh.tmem_free[slot], ((j >> 1) + 1) & 1, kBarP, p == 0, abort))
+      if (j >= 2 && !group_wait(&sh.tmem_free[slot], ((j >> 1) + 1) & 1, kBarP, p == 0, abort, wait_ns))
         break;
       if (p == 0) {
         M.lo = lo;
@@ -756,7 +759,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       const int sl = jj & 1;
       const uint32_t par = (jj >> 1) & 1;
       if (block) {
-        if (!mbar_wait_suspend(&sh.op_ready[sl], par, abort)) return false;
+        if (!mbar_wait_suspend(&sh.op_ready[sl], par, abort, wait_ns)) return false;
       } else if (!mbar_test(&sh.op_ready[sl], par)) {
         return false;
       }
@@ -765,7 +768,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         return true;
       }
       if (block) {
-        if (!mbar_wait_suspend(&sh.tma_bar, nkq & 1, abort)) return false;
+        if (!mbar_wait_suspend(&sh.tma_bar, nkq & 1, abort, wait_ns)) return false;
       } else if (!mbar_test(&sh.tma_bar, nkq & 1)) {
         return false;
       }
@@ -807,7 +810,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       if (c == 0 && p1_next == j) {
         if (issue_p1(j, true)) ++p1_next;  // (on expiry the wait below sees the abort)
       }
-      if (!group_wait(&sh.s1_done[slot], (j >> 1) & 1, kBarC, c == 0, abort)) break;
+      if (!group_wait(&sh.s1_done[slot], (j >> 1) & 1, kBarC, c == 0, abort, wait_ns)) break;
       tc_fence_after_sync();
       const ItemMeta& M = sh.meta[slot];
       const int lo = M.lo, N = M.N, h = M.h;
@@ -824,7 +827,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         for (int n = c; n < nz; n += kGroup) Gws[(size_t)(lo + n) * H_v + h] = 0.f;
         bool v_ok = true;
         if (c == 0) {  // this item's V rows have landed: the area is free for the next
-          if (!M.skip) v_ok = mbar_wait_suspend(&sh.v_bar, nv & 1, abort);
+          if (!M.skip) v_ok = mbar_wait_suspend(&sh.v_bar, nv & 1, abort, wait_ns);
           if (v_ok && next < i_end) {
             if (v_wanted()) issue_v(next);
             if (next + i_step < i_end) load_vseq(next + i_step);
@@ -869,7 +872,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       // accumulates U = T R there
       bool v_ok = true;
       if (key_lane) {
-        v_ok = mbar_wait_suspend(&sh.v_bar, nv & 1, abort);
+        v_ok = mbar_wait_suspend(&sh.v_bar, nv & 1, abort, wait_ns);
         const bool live = lane_node < N;
         const float eG = live ? __expf(M.G[lane_node]) : 0.f;
         const float bn = live ? M.bb[lane_node] : 0.f;
@@ -951,7 +954,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         // (another chance for the next item's first product, behind this product)
         if (next < i_end && p1_next == j + 1 && issue_p1(j + 1, false)) ++p1_next;
       }
-      const bool done2 = group_wait(&sh.mma2_bar, mma2_count & 1, kBarC, c == 0, abort);
+      const bool done2 = group_wait(&sh.mma2_bar, mma2_count & 1, kBarC, c == 0, abort, wait_ns);
       ++mma2_count;
       if (!done2) break;
       tc_fence_after_sync();
@@ -1046,13 +1049,13 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
   if (sh.abort && tid == 0) {
     for (int it2 = i_begin; it2 < i_end; it2 += i_step)
       atomicCAS(&status[it2 / H_v], TGDN_SEQ_OK, TGDN_SEQ_TIMEOUT);
-    if (sh.tma_issued > 0) (void)mbar_wait(&sh.tma_bar, (sh.tma_issued - 1) & 1);
-    if (sh.v_issued > 0) (void)mbar_wait(&sh.v_bar, (sh.v_issued - 1) & 1);
+    if (sh.tma_issued > 0) (void)mbar_wait(&sh.tma_bar, (sh.tma_issued - 1) & 1, wait_ns);
+    if (sh.v_issued > 0) (void)mbar_wait(&sh.v_bar, (sh.v_issued - 1) & 1, wait_ns);
   }
   // the last products, before TMEM and the operands are released (bounded)
-  if (tid == 0 && sh.mma1_issued > 0) (void)mbar_wait(&sh.mma1_bar, (sh.mma1_issued - 1) & 1);
-  if (tid == 0 && sh.mma2_issued > 0) (void)mbar_wait(&sh.mma2_bar, (sh.mma2_issued - 1) & 1);
-  if (tid == 0 && sh.cmt_issued > 0) (void)mbar_wait(&sh.cmt_bar, (sh.cmt_issued - 1) & 1);
+  if (tid == 0 && sh.mma1_issued > 0) (void)mbar_wait(&sh.mma1_bar, (sh.mma1_issued - 1) & 1, wait_ns);
+  if (tid == 0 && sh.mma2_issued > 0) (void)mbar_wait(&sh.mma2_bar, (sh.mma2_issued - 1) & 1, wait_ns);
+  if (tid == 0 && sh.cmt_issued > 0) (void)mbar_wait(&sh.cmt_bar, (sh.cmt_issued - 1) & 1, wait_ns);
   __syncthreads();
   if (warp == 0) {
     tc_fence_after_sync();
@@ -1072,18 +1075,6 @@ bool verify_tc_supported(const tgdn_tree& t, const tgdn_dims& d, const void* q, 
          al(k, 16) && al(v, 16) && al(S0, 16) && al(o, 16);
 }
 
-static int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0, c = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && c > 0)
-      n = c;
-    else
-      return 1;
-  }
-  return n;
-}
 
 cudaError_t launch_verify_tc(const tgdn_tree& t, const tgdn_dims& d, const CUtensorMap& qmap,
                              const CUtensorMap& kmap, const CUtensorMap& vmap,
@@ -1098,7 +1089,7 @@ cudaError_t launch_verify_tc(const tgdn_tree& t, const tgdn_dims& d, const CUten
   const long items = (long)t.B * d.H_v;
   if (items == 0) return cudaSuccess;
   if (items > 0x7fffffffL) return cudaErrorInvalidConfiguration;
-  const int sms = sm_count();
+  const int sms = device_sm_count();
   const int grid = (int)(items < sms ? items : sms);
   // programmatic stream serialization: the kernel's prologue may overlap the
   // previous kernel's tail (it waits for that kernel before reading any input)
@@ -1112,9 +1103,11 @@ cudaError_t launch_verify_tc(const tgdn_tree& t, const tgdn_dims& d, const CUten
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
+  const WaitHooks hk = wait_hooks();
   e = cudaLaunchKernelEx(&lc, kern, qmap, kmap, vmap, om, (int)items, d.H_qk, d.H_v, t.depth_max,
                          t.words, small_only ? 1 : 0, t.cu_nodes, t.depth, t.order, t.pos,
-                         t.anc, t.status, g, b, S, static_cast<__nv_bfloat16*>(o), U, G, cm);
+                         t.anc, t.status, g, b, S, static_cast<__nv_bfloat16*>(o), U, G, cm,
+                         hk.wait_ns ? hk.wait_ns : kWaitLimitNs, hk.hold_item);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -561,18 +561,6 @@ bool verify_tc128_supported(const tgdn_tree& t, const tgdn_dims& d, const void* 
          al(o, 16);
 }
 
-static int t8_sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0, c = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && c > 0)
-      n = c;
-    else
-      return 1;
-  }
-  return n;
-}
 
 cudaError_t launch_verify_tc128(const tgdn_tree& t, const tgdn_dims& d, const CUtensorMap& qmap,
                                 const CUtensorMap& kmap, const void* q, const void* k,
@@ -585,7 +573,7 @@ cudaError_t launch_verify_tc128(const tgdn_tree& t, const tgdn_dims& d, const CU
   const long items = (long)t.B * d.H_v;
   if (items == 0) return cudaSuccess;
   if (items > 0x7fffffffL) return cudaErrorInvalidConfiguration;
-  const int sms = t8_sm_count();
+  const int sms = device_sm_count();
   const int grid = (int)(items < sms ? items : sms);
   verify_tc128_kernel<<<grid, kT8Threads, kT8SmemBytes, s>>>(
       qmap, kmap, (int)items, d.H_qk, d.H_v, t.depth_max, t.words, t.cu_nodes, t.depth, t.order,

@@ -83,6 +83,8 @@ def lib() -> ctypes.CDLL:
         L.tgdn_tree_attention.restype = ctypes.c_int
         L.tgdn_tree_attention_workspace_bytes.argtypes = [P(CTree), i32, i32, i32, i32]
         L.tgdn_tree_attention_workspace_bytes.restype = ctypes.c_size_t
+        L.tgdn_debug_set_wait_hooks.argtypes = [ctypes.c_uint64, ctypes.c_int32]
+        L.tgdn_debug_set_wait_hooks.restype = ctypes.c_int
         L.tgdn_status_string.argtypes = [i32]
         L.tgdn_status_string.restype = ctypes.c_char_p
         L.tgdn_version.argtypes = []
@@ -350,3 +352,12 @@ def verify_noalloc(tree: Tree, dims: Dims, q, k, v, g, b, S0, o, stream=None) ->
             _dev(o, io, T * dims.H_v * dims.d_v, "o"))
     _check(lib().tgdn_verify_noalloc(ctypes.byref(ct), ctypes.byref(cd), *args, _stream(stream)),
            "tgdn_verify_noalloc")
+
+
+def debug_set_wait_hooks(wait_limit_ns: int = 0, withhold_item: int = -1) -> None:
+    """tgdn_debug_set_wait_hooks: a test hook that shortens the bounded device waits of the
+    64-node verification kernel and makes its producer withhold one work item's
+    hand-over, so that the consumer's wait expires (TGDN_SEQ_TIMEOUT, no fault or hang).
+    debug_set_wait_hooks() restores the defaults."""
+    _check(lib().tgdn_debug_set_wait_hooks(int(wait_limit_ns), int(withhold_item)),
+           "tgdn_debug_set_wait_hooks")
