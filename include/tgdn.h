@@ -336,9 +336,10 @@ int tgdn_verify_noalloc(const tgdn_tree* tree, const tgdn_dims* dims, const void
  * (nothing traps or hangs).  From the next launch on, the tensor-core verification
  * kernel for trees of at most 64 nodes (tgdn_verify, tgdn_verify_fused,
  * tgdn_verify_noalloc) uses wait_limit_ns instead (0: the 2 s default), and when
- * withhold_item >= 0 its producer warps never hand over the operands of work item
- * withhold_item (sequence withhold_item / H_v, value head withhold_item % H_v), so
- * that the consumer's wait for them expires: the CTA that owns that item stops,
+ * withhold_item >= 0 its producer warps never issue the first tensor-core product of
+ * work item withhold_item (sequence withhold_item / H_v, value head
+ * withhold_item % H_v), so that the consumer's wait for it expires: the CTA that owns
+ * that item stops,
  * reports every item it owns as TGDN_SEQ_TIMEOUT, waits for its own copies and
  * products to finish and returns; other CTAs are unaffected.  Process-wide, not
  * thread-safe with concurrent launches; tgdn_debug_set_wait_hooks(0, -1) restores

@@ -4,8 +4,8 @@ Every wait of the tensor-core verification kernel gives up after a limit, marks
 the sequences of every work item its CTA owns TGDN_SEQ_TIMEOUT, waits for its own
 copies and products to finish, frees its tensor memory and returns.  A test hook
 (tgdn_debug_set_wait_hooks) shortens the limit to 1 ms and makes the producer
-warps withhold the hand-over of one work item, so the consumer's wait for it
-expires -- a flag that nothing sets, not a fault.  The test checks the statuses,
+warps withhold the first tensor-core product of one work item, so the consumer's
+wait for it expires -- a flag that nothing sets, not a fault.  The test checks the statuses,
 that every other sequence still matches the fp64 oracle, that the launch returns
 promptly, and that the context stays usable for a normal verification afterwards.
 """

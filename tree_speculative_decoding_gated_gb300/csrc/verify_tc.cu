@@ -17,29 +17,39 @@
 // run per CTA with a pending commit, else dealt round robin); trees have at most
 // 64 nodes and depth at most 30.  Two items are in flight per SM:
 //   producer warps 0-7, item j+1:
-//     S0 (loaded into registers an item ahead; warp w holds rows 16 w .. 16 w + 15)
-//     -> bf16 operand (MN-major, 128-byte swizzle), the next item's rows loaded
-//     into the registers each row frees; TMA of the item's key and query rows
-//     -> A = [K; Q]; then tree metadata (prefetched as raw values) -> root paths
-//     (reused for the next head of the same sequence) and path-cumulative gates.
-//   consumer warps 8-15, item j:
-//     thread 0 issues the first product of every item into TMEM half j & 1,
+//     the item's fp32 state [128][128] arrives by one 64 KiB bulk copy over the
+//     [K;Q] and state-operand areas; each thread takes one value column, 64 key
+//     rows, into registers;
+//     with a commit pending, the commit's product D^T = (C U_p)^T K_p runs on the
+//     tensor cores (128 value columns x 64 key rows, twice, into the TMEM
+//     columns the halves leave free) and each thread forms S = e^{G*} S + D;
+//     S -> bf16 operand (K-major, 128-byte swizzle); TMA of the item's key and
+//     query rows -> A = [K; Q]; tree metadata (prefetched as raw values) ->
+//     root paths (reused for the next head of the same sequence) and
+//     path-cumulative gates; the committed state goes back to HBM last;
+//   the producer's thread 255, item j+1, while the others build the metadata:
+//     the first product into TMEM half (j+1) & 1,
 //        D[:, 0:128] = A S0,  D[:, 128:192] = A K^T,
-//     once the producer has published the operands (while the previous item's
-//     solve runs when they are ready by then, else at the top of the item);
-//     Gram rows -> shared memory; V rows arrive by TMA in the R lo operand area
-//     and the key-lane warps form R = diag(b)(V - e^G K S0) there in place
-//     (bf16 hi/lo operand) while the query-lane warps substitute along the root
-//     paths, one T or W row per thread with the partial sums in registers,
-//     writing straight into the [T; W] operand;
-//     tcgen05.mma: D[:, 128:256] = [T; W] R;
-//     U (workspace) and O = e^G Q S0 + W R (bf16) leave through shared-memory
-//     staging and bulk copies.
-// The halves hand over through mbarriers: "operands ready" (producer -> the
-// issuing thread), "stage 1 done" (the first product's completion plus the
-// producer's metadata) and "TMEM half free".  The kernel is launched with
-// programmatic stream serialization: its prologue may overlap the previous
-// kernel's tail and no input is read before griddepcontrol.wait.
+//     and, once it has read A and the operand, the bulk copy of the next item's
+//     state into those areas;
+//   consumer warps 8-15, item j:
+//     Gram rows -> shared memory; V rows arrive by TMA and the key-lane warps
+//     form R = diag(b)(V - e^G K S0) (bf16 hi/lo operand), clearing K S0 in
+//     TMEM, while the query-lane warps substitute along the root paths, one T
+//     or W row per thread with the partial sums in registers, writing straight
+//     into the [T; W] operand;
+//     tcgen05.mma accumulates [T; W'] R onto D[:, 0:128]: the key lanes end
+//     with U = T R, the query lanes with Q S0 + W' R, W' = e^{-max(G,-60)} W,
+//     so that O = e^{max(G,-60)} D;
+//     U (workspace, fp32) and O (bf16) leave through swizzled shared-memory
+//     staging and TMA tensor stores.
+// The halves hand over through mbarriers: "stage 1 done" (the first product's
+// completion plus the producer's metadata) and "TMEM half free".  Every wait is
+// bounded: past the limit the CTA marks its items' sequences TGDN_SEQ_TIMEOUT,
+// waits (bounded) for its own copies and products, frees its tensor memory
+// and returns.  The kernel is launched with programmatic stream serialization:
+// its prologue may overlap the previous kernel's tail and no input is read
+// before griddepcontrol.wait.
 // In a launch above 64 nodes it takes only the sequences of at most 64 nodes
 // (small_only) and passes over the others without touching them.
 // The state enters the tensor-core products as bf16 (fp32 accumulation); it is
@@ -52,9 +62,9 @@
 // and G_s by 16-byte asynchronous copies, one item ahead, into an area of
 // their own) and forms
 //   S = e^{G*} S_prev + sum_{s on the path} e^{G*-G_s} k_s u_s^T
-// in registers, writes it back in place (the committed state) row by row while
-// it builds the operand, and verifies from it.  The state then crosses HBM once
-// in each direction per step.
+// with the sum as one tensor-core product, writes it back in place (the
+// committed state) and verifies from it.  The state then crosses HBM once in
+// each direction per step.
 #include "tgdn_device.cuh"
 #include "tgdn_kernels.h"
 
@@ -77,6 +87,10 @@ constexpr uint32_t kCommitCol0 = 192, kCommitCol1 = 448;
 
 // Shared-memory map (bytes from a 1024-byte aligned base).
 constexpr int kOffA = 0;          // [K;Q] operand: [2 d_k halves][128 rows][128 B]      32 KiB
+// Before an item's [K;Q] rows and operand arrive, its fp32 state [128][128] (64 KiB)
+// sits over both areas: one bulk copy, issued once the previous item's first product
+// has read them.
+constexpr int kOffState = 0;
 constexpr int kOffS = 32768;      // S0^T operand (bf16), K-major [2 k halves][128 columns][128 B]
 // While the pending commit is formed the same area holds its operands (path padded to
 // 32 entries): (C U_p)^T hi and lo, MN-major [2 m chunks][4 k groups][8][128 B], and
@@ -125,8 +139,8 @@ struct alignas(16) ItemMeta {
 struct TcShared {
   uint64_t tma_bar, mma1_bar, mma2_bar, v_bar;
   uint64_t s1_done[2];    // consumer waits: first product done + metadata written
-  uint64_t op_ready[2];   // consumer's issuing thread waits: the state operand is written
   uint64_t cmt_bar;       // producer waits: the commit product is in TMEM
+  uint64_t st_bar;        // producer waits: an item's state has landed
   uint64_t tmem_free[2];  // producer waits: consumer finished the item in this half
   uint32_t tmem_slot;
   int abort;
@@ -135,7 +149,7 @@ struct TcShared {
   int mma1_issued;
   int mma2_issued;
   int cmt_issued;
-  int op_skip[2];         // the item in this half is passed over (no first product)
+  int st_issued;
   int c_L[2];             // staged path length per item parity (0: nothing to commit)
   int c_row[2][kTcPath];  // previous-step node rows of the staged path
   int c_gi[2][kTcPath];   // index of G_s within its staged 16-byte chunk
@@ -219,17 +233,21 @@ __device__ __forceinline__ void path_update(float (&acc)[N], const uint32_t (&pw
 // One row of T (t_row) or W of the node sn at depth dn, by substitution along
 // its root path P = (p_0 = root, ..., p_dn = sn):
 //   r (I + X_P) = y,  X_P[i][j] = b_{p_i} e^{G_{p_i} - G_{p_j}} k_{p_i}.k_{p_j} (i > j),
-//   y = e_dn for T;  y_j = e^{G_n - G_{p_j}} q_n.k_{p_j} for W (stored scaled, below).
-// With phi_i = e^{G_{p_i} - G_n} >= 1 and s_i = r_i b_{p_i} phi_i:
-//   r_j = y_j - (1 / phi_j) acc_j,  acc_j = sum_{i>j} s_i k_{p_i}.k_{p_j}.
-// Entries are settled from the node towards the root; once s_i is known it is
-// added into every acc_j (j < i) at once.  acc lives in registers; the loop
-// runs from the warp's deepest row, so the step index i is the same in every
-// lane.  The next entry's sum is taken out of acc before the update and only
-// its own term is added, so the chain from one entry to the next is a few
-// dependent operations; the Gram reads and the other updates are off it.
-// (phi is capped at e^80; the capped terms are below fp32 resolution.)  r_j is
-// written as bf16 hi + lo at column p_j of the [T; W] operand row.
+//   y = e_dn for T;  y_j = e^{G_n - G_{p_j}} q_n.k_{p_j} for W.
+// The gates leave the recurrence once each entry is rescaled to
+// rho_j = r_j e^{G_{p_j} - G_n}:
+//   rho_j = y'_j - acc_j,  acc_j = sum_{i>j} b_{p_i} rho_i k_{p_i}.k_{p_j},
+//   y' = e_dn for T;  y'_j = q_n.k_{p_j} for W,
+// and r_j = rho_j e^{G_n - G_{p_j}} (at most 1 for non-positive gates) is only
+// formed for the store, off the chain of dependent operations.
+// Entries are settled from the node towards the root; once s_i = b_{p_i} rho_i
+// is known it is added into every acc_j (j < i) at once.  acc lives in
+// registers; the loop runs from the warp's deepest row, so the step index i is
+// the same in every lane.  The next entry's sum is taken out of acc before the
+// update and only its own term is added, so the chain from one entry to the
+// next is a subtract, a multiply and a fused multiply-add; the Gram reads and
+// the other updates are off it.  r_j is written as bf16 hi + lo at column p_j
+// of the [T; W] operand row.
 template <int D>
 __device__ __forceinline__ void solve_path_row(const ItemMeta& M, const float* KK,
                                                const float* QK, uint8_t* smem, int sn, int dn,
@@ -244,7 +262,7 @@ __device__ __forceinline__ void solve_path_row(const ItemMeta& M, const float* K
   const int a2row = t_row ? sn : 64 + sn;
   // a W row is stored times e^{-max(G_n, -60)}: the second product adds it onto
   // Q S0 and the output is that sum times e^{max(G_n, -60)}
-  const float wscale = t_row ? 1.f : __expf(-fmaxf(Gn, -60.f));
+  const float gofs = t_row ? Gn : Gn - fmaxf(Gn, -60.f);
   const float* GRq = QK + sn * 64;  // q_n . k_s (chunks rotated by sn & 7)
   const int xq = (sn & 7) << 2;
   float acc[NA];
@@ -261,19 +279,15 @@ __device__ __forceinline__ void solve_path_row(const ItemMeta& M, const float* K
     const int pnn = i > 1 ? prow[i - 2] : 0;
     const float Gnx = M.G[pn], bnx = M.bb[pn];
     const float qnx = t_row ? 0.f : GRq[pn ^ xq];
-    // K K^T row p_i (padded, unrotated)
-    const float* GRi = KK + pi * kKKStride;
-    const int xi = 0;
-    const float kn = GRi[pn ^ xi];  // k_{p_i}.k_{p_{i-1}}
-    const float y = t_row ? (i == dn ? 1.f : 0.f) : __expf(Gn - Gi) * qi;
-    const float inv_phi = __expf(fmaxf(Gn - Gi, -80.f));
-    const float f = bi * __expf(fminf(Gi - Gn, 80.f));
+    const float* GRi = KK + pi * kKKStride;  // K K^T row p_i (padded, unrotated)
+    const float kn = GRi[pn];                // k_{p_i}.k_{p_{i-1}}
+    const float yp = t_row ? (i == dn ? 1.f : 0.f) : qi;
     const float base = pick<NA>(acc, i - 1);  // acc_{i-1} before this step's term
-    const float r = y - inv_phi * ai;
+    const float rho = yp - ai;
     const bool own = i <= dn;
-    const float s = own ? r * f : 0.f;
+    const float s = own ? rho * bi : 0.f;
     if (own) {
-      const float rw = r * wscale;
+      const float rw = rho * __expf(gofs - Gi);
       const __nv_bfloat16 hi = __float2bfloat16_rn(rw);
       const __nv_bfloat16 lw = __float2bfloat16_rn(rw - __bfloat162float(hi));
       const int off = atom_off(a2row, pi >> 3) + (pi & 7) * 2;
@@ -282,17 +296,17 @@ __device__ __forceinline__ void solve_path_row(const ItemMeta& M, const float* K
     }
     const int lim = i - 1;  // entries 0 .. i-2 take their terms here
     if (lim <= 4) {
-      path_update<4>(acc, pw, s, GRi, xi);
+      path_update<4>(acc, pw, s, GRi, 0);
     } else if (lim <= 8) {
-      path_update<8>(acc, pw, s, GRi, xi);
+      path_update<8>(acc, pw, s, GRi, 0);
     } else if (lim <= 12) {
-      path_update<12>(acc, pw, s, GRi, xi);
+      path_update<12>(acc, pw, s, GRi, 0);
     } else if (lim <= 16) {
-      path_update<16>(acc, pw, s, GRi, xi);
+      path_update<16>(acc, pw, s, GRi, 0);
     } else if (lim <= 24) {
-      path_update<(NA < 24 ? NA : 24)>(acc, pw, s, GRi, xi);
+      path_update<(NA < 24 ? NA : 24)>(acc, pw, s, GRi, 0);
     } else {
-      path_update<NA>(acc, pw, s, GRi, xi);
+      path_update<NA>(acc, pw, s, GRi, 0);
     }
     ai = fmaf(s, kn, base);
     pi = pn;
@@ -347,9 +361,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     mbar_init(&sh.v_bar, 1);
     mbar_init(&sh.s1_done[0], 2);
     mbar_init(&sh.s1_done[1], 2);
-    mbar_init(&sh.op_ready[0], 1);
-    mbar_init(&sh.op_ready[1], 1);
     mbar_init(&sh.cmt_bar, 1);
+    mbar_init(&sh.st_bar, 1);
     mbar_init(&sh.tmem_free[0], 1);
     mbar_init(&sh.tmem_free[1], 1);
     fence_mbar_init();
@@ -360,6 +373,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     sh.mma1_issued = 0;
     sh.mma2_issued = 0;
     sh.cmt_issued = 0;
+    sh.st_issued = 0;
   }
   if (warp == 0) tmem_alloc(&sh.tmem_slot, kTmemCols);
   tc_fence_before_sync();
@@ -395,19 +409,22 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       sh.tma_issued += 1;
     };
     // The state of one item, one value column per thread: warp w holds column
-    // jc = 32 (w & 3) + lane of key rows rb .. rb + 63, rb = 64 (w >> 2) (plain loads:
-    // with a pending commit the kernel writes these rows back).  A warp's access to
-    // one row is one 128-byte line, and the registers line up with the TMEM lanes
-    // of the commit product (lane = value column).
+    // jc = 32 (w & 3) + lane of key rows rb .. rb + 63, rb = 64 (w >> 2), read from the
+    // bulk copy in shared memory (with a pending commit the kernel writes these rows
+    // back from registers).  A warp's access to one row is one 128-byte line, and the
+    // registers line up with the TMEM lanes of the commit product (lane = value
+    // column).
     const int jc = 32 * ((p >> 5) & 3) + (p & 31);
     const int rb = 64 * (p >> 7);
     float sreg[64];
     auto sptr = [&](int item, int i) {
       return S + (size_t)item * kTcDK * kTcDV + (size_t)(rb + i) * kTcDV + jc;
     };
-    auto load_s0 = [&](int item) {
-#pragma unroll
-      for (int i = 0; i < 64; ++i) sreg[i] = __ldcg(sptr(item, i));
+    auto issue_state = [&](int item) {  // thread 0 only
+      mbar_arrive_expect_tx(&sh.st_bar, kTcDK * kTcDV * 4);
+      bulk_load(smem + kOffState, S + (size_t)item * kTcDK * kTcDV, kTcDK * kTcDV * 4,
+                &sh.st_bar);
+      sh.st_issued += 1;
     };
     // Warp 0, two items ahead of its staging: the item's accepted path in the
     // previous tree (lane l holds entry l) and that sequence's bounds and status.
@@ -482,7 +499,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     load_seq(item);
     load_meta(item);
     if (item + i_step < i_end) load_seq(item + i_step);
-    if (!(small_only && pf.N > kTcNodes)) load_s0(item);
+    if (p == 0 && !(small_only && pf.N > kTcNodes)) issue_state(item);
     if (fused) {
       if (p < 32) {
         load_commit_meta(item);
@@ -497,6 +514,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     int npr = 0;       // items processed so far (passed-over items excluded): one [K;Q]
                        // copy and one first product each, in order
     int ncm = 0;       // commit products issued so far
+    int nst = 0;       // state copies consumed so far
     for (int j = 0; item < i_end; ++j, item += i_step) {
       const int slot = j & 1;
       ItemMeta& M = sh.meta[slot];
@@ -516,22 +534,25 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         if (v_ok) my_anc = anc[(size_t)(lo + pf.pos) * words];  // positions < 64: word 0
         else ok = false;
       }
+      // this item's state, from the bulk copy into the [K;Q] and operand areas
+      if (!skip) {
+        if (!group_wait(&sh.st_bar, nst & 1, kBarP, p == 0, abort, wait_ns)) break;
+        ++nst;
+        const float* st = reinterpret_cast<const float*>(smem + kOffState) + rb * kTcDV + jc;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) sreg[i] = st[i * kTcDV];
+      }
       int L = 0;
       if (fused) {
         cp_async_wait_all();
         if (p < 32 && next < i_end) publish_commit(slot ^ 1);  // the next item's path
-        if (!named_sync_and(kBarP, kGroup, !*abort)) break;    // staged rows visible
-        L = sh.c_L[slot];
       }
-      // thread 0: the previous first product has completed, so its operand areas are
-      // free: this item's key and query rows go out, and the state area may take the
-      // commit operands
-      bool step_ok = true;
-      if (p == 0 && !skip) {
-        if (npr > 0) step_ok = mbar_wait_suspend(&sh.mma1_bar, (npr - 1) & 1, abort, wait_ns);
-        if (step_ok) issue_kq(item, lo);
-      }
-      if (!named_sync_and(kBarP, kGroup, step_ok && !*abort)) break;
+      // every thread has read its state rows (and the staged commit rows are visible):
+      // the areas are free for this item's [K;Q] rows and the commit operands
+      fence_proxy_async_smem();
+      if (!named_sync_and(kBarP, kGroup, !*abort)) break;
+      if (fused) L = sh.c_L[slot];
+      if (p == 0 && !skip) issue_kq(item, lo);
       if (L > 0) {
         // The previous step's commit, S = e^{G*} S + sum_l e^{G*-G_l} k_l u_l^T, on the
         // tensor cores: D^T = (C U_p)^T K_p with C = diag(e^{G*-G_l}) (M = 128 value
@@ -614,16 +635,49 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       }
       fence_proxy_async_smem();
       named_sync(kBarP, kGroup);  // the S operand is complete
-      if (p == 0) {
-        sh.op_skip[slot] = skip ? 1 : 0;
-        // (a test hook can withhold one item's hand-over: the consumer's bounded wait
-        // for it then expires)
-        if (item != hold_item) mbar_arrive(&sh.op_ready[slot]);
-      }
       // the consumer has finished item j-2, the previous user of this half and slot
       // (every wait is agreed on by the whole group before anyone leaves the loop)
       if (j >= 2 && !group_wait(&sh.tmem_free[slot], ((j >> 1) + 1) & 1, kBarP, p == 0, abort, wait_ns))
         break;
+      // Thread 255 (no node of its own) issues the first product into TMEM half `slot`
+      // once this item's key and query rows have landed,
+      //   D[:, 0:128] = [K;Q] S0,  D[:, 128:192] = [K;Q] K^T,
+      // and, once that product has read the [K;Q] and operand areas, copies the next
+      // item's state there; meanwhile the other threads build the metadata.  A
+      // passed-over item gets no product.  (A test hook can withhold one item's
+      // product: the consumer's bounded wait for it then expires.)
+      if (p == kGroup - 1) {
+        bool ok255 = true;
+        if (item == hold_item) {
+          ok255 = false;
+        } else if (skip) {
+          mbar_arrive(&sh.s1_done[slot]);
+        } else if ((ok255 = mbar_wait_suspend(&sh.tma_bar, npr & 1, abort, wait_ns))) {
+          tc_fence_after_sync();
+          const uint32_t tb1 = tmem + slot * 256;
+          const uint32_t sA = smem_addr(smem + kOffA);
+          const uint32_t sS = smem_addr(smem + kOffS);
+          constexpr uint32_t id_s0 = idesc_bf16_f32(128, 128, 0, 0);
+          constexpr uint32_t id_gram = idesc_bf16_f32(128, kTcNodes, 0, 0);
+#pragma unroll
+          for (int s2 = 0; s2 < kTcDK / 16; ++s2) {
+            const uint64_t ad = smem_desc(sA + (s2 >> 2) * 16384 + (s2 & 3) * 32, 16, 1024,
+                                          kSwizzle128B);
+            // K-major S0^T: the same layout as A (64-element k halves 16 KiB apart)
+            const uint64_t hd = smem_desc(sS + (s2 >> 2) * 16384 + (s2 & 3) * 32, 16, 1024,
+                                          kSwizzle128B);
+            umma_bf16(tb1, ad, hd, id_s0, s2 > 0);
+            umma_bf16(tb1 + kGramCol, ad, ad, id_gram, s2 > 0);  // B = the key rows of A
+          }
+          umma_commit(&sh.mma1_bar);
+          umma_commit(&sh.s1_done[slot]);
+          sh.mma1_issued += 1;
+        }
+        const int n1 = npr + (skip ? 0 : 1);  // first products issued so far
+        if (ok255 && next < i_end && !(small_only && q_hi - q_lo > kTcNodes) &&
+            (n1 == 0 || mbar_wait_suspend(&sh.mma1_bar, (n1 - 1) & 1, abort, wait_ns)))
+          issue_state(next);
+      }
       if (p == 0) {
         M.lo = lo;
         M.N = N;
@@ -703,19 +757,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         mbar_arrive(&sh.s1_done[slot]);  // the metadata above is written
       }
       if (!skip) ++npr;
-      // the committed state back in place (fused) and the next item's state in, row
-      // by row into the registers each store frees
-      const bool load_next = next < i_end && !(small_only && pf.N > kTcNodes);
-      // (L2-only accesses: the state is touched once per step and never by this SM
-      // again within the launch)
+      // the committed state back in place (fused; L2-only stores: the state is touched
+      // once per step and never by this SM again within the launch)
       if (L > 0) {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          __stcg(sptr(item, i), sreg[i]);
-          if (load_next) sreg[i] = __ldcg(sptr(next, i));
-        }
-      } else if (load_next) {
-        load_s0(next);
+        for (int i = 0; i < 64; ++i) __stcg(sptr(item, i), sreg[i]);
       }
       // A block boundary here keeps the compiler from moving the next iteration's work
       // in among these memory instructions (measured: that interleaving made the
@@ -747,69 +793,18 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       tma_load_3d(smem + kOffRlo + 8192, &vmap, &sh.v_bar, 64, item % H_v, cv_lo);
       sh.v_issued += 1;
     };
-    // Thread 0 also issues every first product (item jj into TMEM half jj & 1),
-    // once the producer has completed the item's state operand and its key and
-    // query rows have landed: D[:, 0:128] = [K;Q] S0,  D[:, 128:192] = [K;Q] K^T.
-    // It does so while the previous item's rows are being solved when the operands
-    // are ready by then, else at the top of the item; a passed-over item gets no
-    // product.  Returns false when the operands are not ready (block = false) or
-    // a wait expired (block = true).
-    int nkq = 0;  // [K;Q] copies consumed so far
-    auto issue_p1 = [&](int jj, bool block) -> bool {
-      const int sl = jj & 1;
-      const uint32_t par = (jj >> 1) & 1;
-      if (block) {
-        if (!mbar_wait_suspend(&sh.op_ready[sl], par, abort, wait_ns)) return false;
-      } else if (!mbar_test(&sh.op_ready[sl], par)) {
-        return false;
-      }
-      if (sh.op_skip[sl]) {
-        mbar_arrive(&sh.s1_done[sl]);  // a passed-over item: no copy, no product
-        return true;
-      }
-      if (block) {
-        if (!mbar_wait_suspend(&sh.tma_bar, nkq & 1, abort, wait_ns)) return false;
-      } else if (!mbar_test(&sh.tma_bar, nkq & 1)) {
-        return false;
-      }
-      tc_fence_after_sync();
-      const uint32_t tb = tmem + sl * 256;
-      const uint32_t sA = smem_addr(smem + kOffA);
-      const uint32_t sS = smem_addr(smem + kOffS);
-      constexpr uint32_t id_s0 = idesc_bf16_f32(128, 128, 0, 0);
-      constexpr uint32_t id_gram = idesc_bf16_f32(128, kTcNodes, 0, 0);
-#pragma unroll
-      for (int s = 0; s < kTcDK / 16; ++s) {
-        const uint64_t ad = smem_desc(sA + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024,
-                                      kSwizzle128B);
-        // K-major S0^T: the same layout as A (64-element k halves 16 KiB apart)
-        const uint64_t hd = smem_desc(sS + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024,
-                                      kSwizzle128B);
-        umma_bf16(tb, ad, hd, id_s0, s > 0);
-        umma_bf16(tb + kGramCol, ad, ad, id_gram, s > 0);  // B = the key rows of A
-      }
-      umma_commit(&sh.mma1_bar);
-      umma_commit(&sh.s1_done[sl]);
-      sh.mma1_issued += 1;
-      ++nkq;
-      return true;
-    };
     int item = i_begin;
     if (c == 0) {
       load_vseq(item);
       if (v_wanted()) issue_v(item);
       if (item + i_step < i_end) load_vseq(item + i_step);
     }
-    int p1_next = 0;          // the next item whose first product is not yet issued
     uint32_t mma2_count = 0;  // second products issued so far (same in every thread)
     int nv = 0;               // V copies consumed so far (one per item not passed over)
     for (int j = 0; item < i_end; ++j, item += i_step) {
       const int slot = j & 1;
       const int next = item + i_step;
       bulk_wait_read();  // the previous item's output rows have left shared memory
-      if (c == 0 && p1_next == j) {
-        if (issue_p1(j, true)) ++p1_next;  // (on expiry the wait below sees the abort)
-      }
       if (!group_wait(&sh.s1_done[slot], (j >> 1) & 1, kBarC, c == 0, abort, wait_ns)) break;
       tc_fence_after_sync();
       const ItemMeta& M = sh.meta[slot];
@@ -832,7 +827,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             if (v_wanted()) issue_v(next);
             if (next + i_step < i_end) load_vseq(next + i_step);
           }
-          if (v_ok && next < i_end && p1_next == j + 1 && issue_p1(j + 1, false)) ++p1_next;
         }
         if (!M.skip) ++nv;
         if (!named_sync_and(kBarC, kGroup, v_ok)) break;
@@ -906,10 +900,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
           }
         }
         tmem_st_wait();
-        // the key-lane warps wait for the solve from here on: the next item's first
-        // product goes in now if its operands are ready, so that it has completed
-        // before this item's second product needs the tensor cores
-        if (c == 0 && next < i_end && p1_next == j + 1 && issue_p1(j + 1, false)) ++p1_next;
       } else {
         // ---- the rows of T (lane quarter 2) and of W (lane quarter 3), one row per
         // thread.  Rows are handed out in topological order: the column-half-0 warps
@@ -951,8 +941,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         }
         umma_commit(&sh.mma2_bar);
         sh.mma2_issued += 1;
-        // (another chance for the next item's first product, behind this product)
-        if (next < i_end && p1_next == j + 1 && issue_p1(j + 1, false)) ++p1_next;
       }
       const bool done2 = group_wait(&sh.mma2_bar, mma2_count & 1, kBarC, c == 0, abort, wait_ns);
       ++mma2_count;
@@ -1056,6 +1044,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
   if (tid == 0 && sh.mma1_issued > 0) (void)mbar_wait(&sh.mma1_bar, (sh.mma1_issued - 1) & 1, wait_ns);
   if (tid == 0 && sh.mma2_issued > 0) (void)mbar_wait(&sh.mma2_bar, (sh.mma2_issued - 1) & 1, wait_ns);
   if (tid == 0 && sh.cmt_issued > 0) (void)mbar_wait(&sh.cmt_bar, (sh.cmt_issued - 1) & 1, wait_ns);
+  if (tid == 0 && sh.st_issued > 0) (void)mbar_wait(&sh.st_bar, (sh.st_issued - 1) & 1, wait_ns);
   __syncthreads();
   if (warp == 0) {
     tc_fence_after_sync();

@@ -454,9 +454,10 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
     }
 
     // ---- rows of T (solver 0..127) and W (128..255) by back substitution on the
-    // root path P = (p_0 = root, ..., p_d = n):
-    //   r_j = y_j - (1 / phi_j) sum_{i>j} s_i k_{p_i}.k_{p_j},  s_i = r_i b_{p_i} phi_i,
-    //   phi_i = e^{G_{p_i} - G_n};  y = e_d for T,  y_j = e^{G_n - G_{p_j}} q_n.k_{p_j} for W.
+    // root path P = (p_0 = root, ..., p_d = n), with each entry rescaled to
+    // rho_j = r_j e^{G_{p_j} - G_n} so that the gates leave the recurrence:
+    //   rho_j = y'_j - sum_{i>j} b_{p_i} rho_i k_{p_i}.k_{p_j},
+    //   y' = e_d for T,  y'_j = q_n.k_{p_j} for W;  r_j = rho_j e^{G_n - G_{p_j}}.
     // k_{p_i}.k_{p_j} is entry j of p_i's compressed row (p_j is its ancestor at depth j).
     if (tid < 2 * kT8Nodes) {
       const bool t_row = tid < kT8Nodes;
@@ -469,16 +470,14 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
         const float Gn = M.G[sn];
         for (int jj = dn; jj >= 0; --jj) {
           const int pj = M.anc_at[jj][sn];
-          const float Gj = M.G[pj];
-          const float inv_phi = __expf(fmaxf(Gn - Gj, -80.f));
-          const float y = t_row ? ((jj == dn) ? 1.f : 0.f) : __expf(Gn - Gj) * GQ[sn * kT8Path + jj];
+          const float y = t_row ? ((jj == dn) ? 1.f : 0.f) : GQ[sn * kT8Path + jj];
           float acc = 0.f;
 #pragma unroll 4
           for (int i = jj + 1; i <= dn; ++i)
             acc = fmaf(SS[i], GK[M.anc_at[i][sn] * kT8Path + jj], acc);
-          const float rj = y - inv_phi * acc;
-          SS[jj] = rj * M.bb[pj] * __expf(fminf(Gj - Gn, 80.f));
-          coef[jj] = rj;
+          const float rho = y - acc;
+          SS[jj] = rho * M.bb[pj];
+          coef[jj] = rho * __expf(Gn - M.G[pj]);
         }
       }
     }

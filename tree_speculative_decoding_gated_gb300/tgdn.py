@@ -356,8 +356,8 @@ def verify_noalloc(tree: Tree, dims: Dims, q, k, v, g, b, S0, o, stream=None) ->
 
 def debug_set_wait_hooks(wait_limit_ns: int = 0, withhold_item: int = -1) -> None:
     """tgdn_debug_set_wait_hooks: a test hook that shortens the bounded device waits of the
-    64-node verification kernel and makes its producer withhold one work item's
-    hand-over, so that the consumer's wait expires (TGDN_SEQ_TIMEOUT, no fault or hang).
+    64-node verification kernel and makes its producer withhold one work item's first
+    product, so that the consumer's wait expires (TGDN_SEQ_TIMEOUT, no fault or hang).
     debug_set_wait_hooks() restores the defaults."""
     _check(lib().tgdn_debug_set_wait_hooks(int(wait_limit_ns), int(withhold_item)),
            "tgdn_debug_set_wait_hooks")
