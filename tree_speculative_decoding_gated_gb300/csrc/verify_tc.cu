@@ -73,6 +73,8 @@ namespace tgdn {
 constexpr int kTcThreads = 512;
 constexpr int kGroup = 256;    // threads per warp group (producer / consumer)
 constexpr int kBarP = 1, kBarC = 2;  // hardware barrier ids of the two groups
+constexpr int kBarM = 3;             // producer warps 0-1 (node metadata and root paths)
+constexpr int kMetaThreads = 64;     // one node per thread
 constexpr int kTcNodes = 64;   // nodes per tree on this kernel
 constexpr int kTcDK = 128;
 constexpr int kTcDV = 128;
@@ -189,6 +191,14 @@ __device__ __forceinline__ bool group_wait(uint64_t* bar, uint32_t parity, int b
   bool ok = true;
   if (leader) ok = mbar_wait_suspend(bar, parity, abort, limit_ns);
   return named_sync_and(bar_id, kGroup, ok);
+}
+
+// The same over a named barrier of n threads.
+__device__ __forceinline__ bool group_wait_n(uint64_t* bar, uint32_t parity, int bar_id, int n,
+                                             bool leader, volatile int* abort, uint64_t limit_ns) {
+  bool ok = true;
+  if (leader) ok = mbar_wait_suspend(bar, parity, abort, limit_ns);
+  return named_sync_and(bar_id, n, ok);
 }
 
 // Everything the producer prefetches for one item (one node per thread < 64).
@@ -635,24 +645,28 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       }
       fence_proxy_async_smem();
       named_sync(kBarP, kGroup);  // the S operand is complete
-      // the consumer has finished item j-2, the previous user of this half and slot
-      // (every wait is agreed on by the whole group before anyone leaves the loop)
-      if (j >= 2 && !group_wait(&sh.tmem_free[slot], ((j >> 1) + 1) & 1, kBarP, p == 0, abort, wait_ns))
-        break;
+      // From here the group splits three ways until the next item's state has landed:
+      // thread 255 issues the first product, warps 0-1 (one node per thread) build the
+      // metadata and root paths, and warps 2-7 send their committed state back at once.
+      // A wait that gives up raises *abort; the group then leaves together at the
+      // next item's first barrier (or the loop ends).
+      //
       // Thread 255 (no node of its own) issues the first product into TMEM half `slot`
-      // once this item's key and query rows have landed,
+      // once the consumer has finished item j-2 (the previous user of the half) and
+      // this item's key and query rows have landed,
       //   D[:, 0:128] = [K;Q] S0,  D[:, 128:192] = [K;Q] K^T,
       // and, once that product has read the [K;Q] and operand areas, copies the next
-      // item's state there; meanwhile the other threads build the metadata.  A
-      // passed-over item gets no product.  (A test hook can withhold one item's
-      // product: the consumer's bounded wait for it then expires.)
+      // item's state there.  A passed-over item gets no product.  (A test hook can
+      // withhold one item's product: the consumer's bounded wait for it then expires.)
       if (p == kGroup - 1) {
         bool ok255 = true;
         if (item == hold_item) {
           ok255 = false;
         } else if (skip) {
           mbar_arrive(&sh.s1_done[slot]);
-        } else if ((ok255 = mbar_wait_suspend(&sh.tma_bar, npr & 1, abort, wait_ns))) {
+        } else if ((ok255 = (j < 2 || mbar_wait_suspend(&sh.tmem_free[slot], ((j >> 1) + 1) & 1,
+                                                         abort, wait_ns)) &&
+                            mbar_wait_suspend(&sh.tma_bar, npr & 1, abort, wait_ns))) {
           tc_fence_after_sync();
           const uint32_t tb1 = tmem + slot * 256;
           const uint32_t sA = smem_addr(smem + kOffA);
@@ -678,84 +692,93 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             (n1 == 0 || mbar_wait_suspend(&sh.mma1_bar, (n1 - 1) & 1, abort, wait_ns)))
           issue_state(next);
       }
-      if (p == 0) {
-        M.lo = lo;
-        M.N = N;
-        M.h = h;
-        M.skip = skip;
-        // rows zero-filled for an item that is not verified: none for a passed-over
-        // item or for a sequence whose bounds tree prep found bad
-        M.zrows = (skip || pf.st == TGDN_SEQ_BAD_RANGE || N < 0) ? 0 : N;
-      }
-      if (ok && p < N) {
-        M.dep[p] = pf.dep;
-        M.pos[p] = pf.pos;
-        M.ord[p] = pf.ord;
-        M.gg[p] = pf.gg;
-        M.bb[p] = pf.bb;
-      }
-      // the next item's small loads and its staged commit go out now; they land
-      // while this item's paths are built
-      if (next < i_end) {
-        load_meta(next);
-        if (next + i_step < i_end) {
-          load_seq(next + i_step);
-          if (fused && p < 32) load_commit_meta(next + i_step);
+      if (p < kMetaThreads) {
+        // Warps 0-1: this slot's node metadata once the consumer is done with item j-2
+        // (its previous user), then the root paths.
+        bool go = j < 2 || group_wait_n(&sh.tmem_free[slot], ((j >> 1) + 1) & 1, kBarM,
+                                        kMetaThreads, p == 0, abort, wait_ns);
+        if (go) {
+          if (p == 0) {
+            M.lo = lo;
+            M.N = N;
+            M.h = h;
+            M.skip = skip;
+            // rows zero-filled for an item that is not verified: none for a passed-over
+            // item or for a sequence whose bounds tree prep found bad
+            M.zrows = (skip || pf.st == TGDN_SEQ_BAD_RANGE || N < 0) ? 0 : N;
+          }
+          if (ok && p < N) {
+            M.dep[p] = pf.dep;
+            M.pos[p] = pf.pos;
+            M.ord[p] = pf.ord;
+            M.gg[p] = pf.gg;
+            M.bb[p] = pf.bb;
+          }
+        }
+        // the next item's small loads and commit bounds go out now; they land while
+        // this item's paths are built
+        if (next < i_end) load_meta(next);
+        if (p < 32 && fused && next + i_step < i_end) load_commit_meta(next + i_step);
+        if (go) {
+          named_sync(kBarM, kMetaThreads);  // this slot's node metadata is written
+          // root paths from the ancestor masks (bits = topological positions,
+          // ascending = root first) and path-cumulative log-gates; the same tree as
+          // the previous item (another head) reuses its paths and only sums the gates.
+          // A node index read from another thread's metadata is range-checked before
+          // it is used (the group agrees on validity only after this).
+          const bool reuse = prev_bi == bi;
+          if (ok && p < N && reuse) {
+            const int dn = M.dep[p];
+            const uint8_t* srow_p = sh.meta[slot ^ 1].path[p];
+            const uint4* src = reinterpret_cast<const uint4*>(srow_p);
+            uint4* dst = reinterpret_cast<uint4*>(M.path[p]);
+            dst[0] = src[0];
+            dst[1] = src[1];
+            float acc = 0.f;
+            for (int i = 0; i <= dn; ++i) acc += M.gg[srow_p[i]];
+            M.G[p] = acc;
+          } else if (ok && p < N) {
+            const int dn = M.dep[p];
+            uint64_t mk = my_anc;
+            bool pk = __popcll(mk) == dn + 1 && ((mk >> M.pos[p]) & 1ull);
+            uint8_t* prow = M.path[p];
+            reinterpret_cast<uint4*>(prow)[0] = make_uint4(0u, 0u, 0u, 0u);
+            reinterpret_cast<uint4*>(prow)[1] = make_uint4(0u, 0u, 0u, 0u);
+            float acc = 0.f;
+            int last = -1;
+            for (int i = 0; pk && i <= dn; ++i) {
+              const int b = __ffsll(static_cast<long long>(mk)) - 1;
+              mk &= mk - 1;
+              if (b >= N) {
+                pk = false;
+                break;
+              }
+              const int s = M.ord[b];
+              if (s < 0 || s >= N) {
+                pk = false;
+                break;
+              }
+              pk = M.dep[s] == i;
+              prow[i] = static_cast<uint8_t>(s);
+              acc += M.gg[s];
+              last = s;
+            }
+            if (!pk || last != p) ok = false;
+            M.G[p] = acc;
+          }
+          ok = named_sync_and(kBarM, kMetaThreads, ok);
+          prev_bi = ok ? bi : -1;
+          if (p == 0) {
+            M.good = ok;
+            mbar_arrive(&sh.s1_done[slot]);  // the metadata above is written
+          }
         }
       }
+      // (every thread takes the next item's bounds and status, which decide whether
+      // it is passed over; only warps 0-1 load node metadata)
+      if (p >= kMetaThreads && next < i_end) load_meta(next);
+      if (next < i_end && next + i_step < i_end) load_seq(next + i_step);
       if (fused && next < i_end) stage_commit(next, slot ^ 1);
-      named_sync(kBarP, kGroup);  // this slot's node metadata is written
-      // root paths from the ancestor masks (bits = topological positions,
-      // ascending = root first) and path-cumulative log-gates; the same tree as
-      // the previous item (another head) reuses its paths and only sums the gates.
-      // A node index read from another thread's metadata is range-checked before
-      // it is used (the group agrees on validity only after this).
-      const bool reuse = prev_bi == bi;
-      if (ok && p < N && reuse) {
-        const int dn = M.dep[p];
-        const uint8_t* srow_p = sh.meta[slot ^ 1].path[p];
-        const uint4* src = reinterpret_cast<const uint4*>(srow_p);
-        uint4* dst = reinterpret_cast<uint4*>(M.path[p]);
-        dst[0] = src[0];
-        dst[1] = src[1];
-        float acc = 0.f;
-        for (int i = 0; i <= dn; ++i) acc += M.gg[srow_p[i]];
-        M.G[p] = acc;
-      } else if (ok && p < N) {
-        const int dn = M.dep[p];
-        uint64_t mk = my_anc;
-        bool pk = __popcll(mk) == dn + 1 && ((mk >> M.pos[p]) & 1ull);
-        uint8_t* prow = M.path[p];
-        reinterpret_cast<uint4*>(prow)[0] = make_uint4(0u, 0u, 0u, 0u);
-        reinterpret_cast<uint4*>(prow)[1] = make_uint4(0u, 0u, 0u, 0u);
-        float acc = 0.f;
-        int last = -1;
-        for (int i = 0; pk && i <= dn; ++i) {
-          const int b = __ffsll(static_cast<long long>(mk)) - 1;
-          mk &= mk - 1;
-          if (b >= N) {
-            pk = false;
-            break;
-          }
-          const int s = M.ord[b];
-          if (s < 0 || s >= N) {
-            pk = false;
-            break;
-          }
-          pk = M.dep[s] == i;
-          prow[i] = static_cast<uint8_t>(s);
-          acc += M.gg[s];
-          last = s;
-        }
-        if (!pk || last != p) ok = false;
-        M.G[p] = acc;
-      }
-      ok = named_sync_and(kBarP, kGroup, ok);
-      prev_bi = ok ? bi : -1;
-      if (p == 0) {
-        M.good = ok;
-        mbar_arrive(&sh.s1_done[slot]);  // the metadata above is written
-      }
       if (!skip) ++npr;
       // the committed state back in place (fused; L2-only stores: the state is touched
       // once per step and never by this SM again within the launch)
