@@ -75,6 +75,7 @@ constexpr int kGroup = 256;    // threads per warp group (producer / consumer)
 constexpr int kBarP = 1, kBarC = 2;  // hardware barrier ids of the two groups
 constexpr int kBarM = 3;             // producer warps 0-1 (node metadata and root paths)
 constexpr int kMetaThreads = 64;     // one node per thread
+constexpr int kBarW = 4;             // all producer threads: paths done, state write-back
 constexpr int kTcNodes = 64;   // nodes per tree on this kernel
 constexpr int kTcDK = 128;
 constexpr int kTcDV = 128;
@@ -118,13 +119,13 @@ constexpr int kOffA2lo = 180224;
 static_assert(kOffGP + kTcPath * 16 <= kOffKK, "commit staging fits its area");
 static_assert(kOffQK + 64 * 64 * 4 <= kOffRhi, "Gram rows fit their area");
 constexpr int kOffMeta = 196608;
-// Output staging after the second product (its operand areas are free then), in the
-// 128-byte swizzled tile layout of the TMA stores that send it out:
+// Output staging after the second product, in the 128-byte swizzled tile layout of
+// the TMA stores that send it out: U in the Gram-row area (free once the solve is
+// done), O in an area of its own after the shared state (below), so that the next
+// item only waits for the U tiles to be read before it stores its Gram rows.
 constexpr int kOffUst = kOffKK;     // U: 4 tiles (32 columns each) [64 rows][128 B] fp32
-constexpr int kOffOst = kOffA2hi;   // O: 2 tiles (64 columns each) [64 rows][128 B] bf16
 static_assert(kOffUst % 1024 == 0 && kOffUst + 4 * 8192 <= kOffRhi,
               "U staging: 1024-byte aligned tiles in the Gram-row area");
-static_assert(kOffOst + 2 * 8192 <= kOffA2lo, "O staging stays in the [T; W] hi area");
 
 struct alignas(16) ItemMeta {
   uint8_t path[kTcNodes][kPathBytes];  // [node][depth]: the node's ancestor at that depth
@@ -157,7 +158,9 @@ struct TcShared {
   int c_gi[2][kTcPath];   // index of G_s within its staged 16-byte chunk
   ItemMeta meta[2];
 };
-constexpr int kTcSmemBytes = kOffMeta + (int)sizeof(TcShared) + 1024;  // + alignment slack
+// O: 2 tiles (64 columns each) [64 rows][128 B] bf16, 1024-byte aligned
+constexpr int kOffOst = (kOffMeta + (int)sizeof(TcShared) + 1023) / 1024 * 1024;
+constexpr int kTcSmemBytes = kOffOst + 2 * 8192 + 1024;  // + alignment slack
 static_assert(kTcSmemBytes <= 227 * 1024, "fits one CTA per SM");
 
 // 16-byte chunk swizzle of the 128-byte-row operands (TMA and tcgen05
@@ -229,15 +232,21 @@ __device__ __forceinline__ int path_at(const uint32_t (&pw)[8], int j) {
   return static_cast<int>((pw[j >> 2] >> (8 * (j & 3))) & 0xffu);
 }
 
-// acc[j] += s * row[p_j ^ x] for j < W.  Only j < i - 1 matter at step i; the
-// other entries are either the next one (taken out before) or settled ones,
-// never read again, so the width only has to cover i - 1 (no per-entry test).
+// acc[j] += s * row[p_j] for j < W (row: a shared-memory address).  Only j < i - 1
+// matter at step i; the other entries are either the next one (taken out before) or
+// settled ones, never read again, so the width only has to cover i - 1 (no per-entry
+// test).  The W loads are issued back to back before the first multiply-add, so
+// their latencies overlap.
 template <int W, int N>
 __device__ __forceinline__ void path_update(float (&acc)[N], const uint32_t (&pw)[8], float s,
-                                            const float* row, int x) {
+                                            uint32_t row) {
   static_assert(W <= N, "width within the partial sums");
+  float v[W];
 #pragma unroll
-  for (int j = 0; j < W; ++j) acc[j] = fmaf(s, row[path_at(pw, j) ^ x], acc[j]);
+  for (int j = 0; j < W; ++j)
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v[j]) : "r"(row + 4u * path_at(pw, j)));
+#pragma unroll
+  for (int j = 0; j < W; ++j) acc[j] = fmaf(s, v[j], acc[j]);
 }
 
 // One row of T (t_row) or W of the node sn at depth dn, by substitution along
@@ -290,6 +299,7 @@ __device__ __forceinline__ void solve_path_row(const ItemMeta& M, const float* K
     const float Gnx = M.G[pn], bnx = M.bb[pn];
     const float qnx = t_row ? 0.f : GRq[pn ^ xq];
     const float* GRi = KK + pi * kKKStride;  // K K^T row p_i (padded, unrotated)
+    const uint32_t GRs = smem_addr(GRi);
     const float kn = GRi[pn];                // k_{p_i}.k_{p_{i-1}}
     const float yp = t_row ? (i == dn ? 1.f : 0.f) : qi;
     const float base = pick<NA>(acc, i - 1);  // acc_{i-1} before this step's term
@@ -306,17 +316,17 @@ __device__ __forceinline__ void solve_path_row(const ItemMeta& M, const float* K
     }
     const int lim = i - 1;  // entries 0 .. i-2 take their terms here
     if (lim <= 4) {
-      path_update<4>(acc, pw, s, GRi, 0);
+      path_update<4>(acc, pw, s, GRs);
     } else if (lim <= 8) {
-      path_update<8>(acc, pw, s, GRi, 0);
+      path_update<8>(acc, pw, s, GRs);
     } else if (lim <= 12) {
-      path_update<12>(acc, pw, s, GRi, 0);
+      path_update<12>(acc, pw, s, GRs);
     } else if (lim <= 16) {
-      path_update<16>(acc, pw, s, GRi, 0);
+      path_update<16>(acc, pw, s, GRs);
     } else if (lim <= 24) {
-      path_update<(NA < 24 ? NA : 24)>(acc, pw, s, GRi, 0);
+      path_update<(NA < 24 ? NA : 24)>(acc, pw, s, GRs);
     } else {
-      path_update<NA>(acc, pw, s, GRi, 0);
+      path_update<NA>(acc, pw, s, GRs);
     }
     ai = fmaf(s, kn, base);
     pi = pn;
@@ -645,9 +655,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       }
       fence_proxy_async_smem();
       named_sync(kBarP, kGroup);  // the S operand is complete
-      // From here the group splits three ways until the next item's state has landed:
+      // From here the group splits three ways until warps 0-1 have their paths:
       // thread 255 issues the first product, warps 0-1 (one node per thread) build the
-      // metadata and root paths, and warps 2-7 send their committed state back at once.
+      // metadata and root paths, and warps 2-7 wait to send their committed state back.
       // A wait that gives up raises *abort; the group then leaves together at the
       // next item's first barrier (or the loop ends).
       //
@@ -773,7 +783,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             mbar_arrive(&sh.s1_done[slot]);  // the metadata above is written
           }
         }
+        named_sync(kBarW, kGroup);
       }
+      // The state goes back only once warps 0-1 have their paths: a burst of stores
+      // issued earlier sits in the load/store queue ahead of their metadata loads
+      // (measured: the metadata phase then took up to twice as long).
+      if (p >= kMetaThreads) named_sync(kBarW, kGroup);
       // (every thread takes the next item's bounds and status, which decide whether
       // it is passed over; only warps 0-1 load node metadata)
       if (p >= kMetaThreads && next < i_end) load_meta(next);
@@ -827,7 +842,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     for (int j = 0; item < i_end; ++j, item += i_step) {
       const int slot = j & 1;
       const int next = item + i_step;
-      bulk_wait_read();  // the previous item's output rows have left shared memory
       if (!group_wait(&sh.s1_done[slot], (j >> 1) & 1, kBarC, c == 0, abort, wait_ns)) break;
       tc_fence_after_sync();
       const ItemMeta& M = sh.meta[slot];
@@ -862,6 +876,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         float r[32];
         tmem_ld32(tb + lane_base + kGramCol + chalf * 32, r);
         tmem_ld_wait();
+        // the previous item's U tiles (the older of its two store groups) have been
+        // read out of the Gram-row area
+        if (c == 0) bulk_wait_read_but_last();
+        named_sync(kBarC, kGroup);
         if (key_lane) {  // K K^T row lane_row
           float4* dst = reinterpret_cast<float4*>(smem + kOffKK) +
                         (lane_row * kKKStride + chalf * 32) / 4;
@@ -965,6 +983,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         umma_commit(&sh.mma2_bar);
         sh.mma2_issued += 1;
       }
+      if (c == 0) bulk_wait_read();  // the previous item's O tiles have left their staging
       const bool done2 = group_wait(&sh.mma2_bar, mma2_count & 1, kBarC, c == 0, abort, wait_ns);
       ++mma2_count;
       if (!done2) break;
@@ -1035,13 +1054,19 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       if (c == 0) {
         mbar_arrive(&sh.tmem_free[slot]);  // this half is free again
         const int n8 = N & ~7;
+        // two store groups, U first: the next item waits only for the U tiles
         for (int r0 = 0; r0 < n8;) {
           const bool big = r0 == 0 && n8 == 64;
           const CUtensorMap* um = big ? &om.u64 : &om.u8;
-          const CUtensorMap* omp = big ? &om.o64 : &om.o8;
 #pragma unroll
           for (int t = 0; t < 4; ++t)
             tma_store_3d(um, smem + kOffUst + t * 8192 + r0 * 128, t * 32, h, lo + r0);
+          r0 += big ? 64 : 8;
+        }
+        bulk_commit();
+        for (int r0 = 0; r0 < n8;) {
+          const bool big = r0 == 0 && n8 == 64;
+          const CUtensorMap* omp = big ? &om.o64 : &om.o8;
 #pragma unroll
           for (int t = 0; t < 2; ++t)
             tma_store_3d(omp, smem + kOffOst + t * 8192 + r0 * 128, t * 64, h, lo + r0);
