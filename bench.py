@@ -48,7 +48,7 @@ NODE_BYTES = 2 * 16 * 128 * 2 + 32 * 128 * 2 + 2 * 32 * 4 + 32 * 128 * 2   # q,k
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant kernel from an ncu
 # capture, with the first 16 hex digits of the SHA-256 of the kernel source it was taken on;
 # the line reports it only while the source still has that hash (null otherwise).
-PROFILED_TRAFFIC = {"fused": (None, ""), "separate": (None, "")}
+PROFILED_TRAFFIC = {"fused": (167191040, "ae03c9eee148f57e"), "separate": (None, "")}
 KERNEL_SOURCE = os.path.join(ROOT, "tree_speculative_decoding_gated_gb300", "csrc", "verify_tc.cu")
 
 
@@ -400,6 +400,7 @@ def run_gpu(args, rank, world, local):
         e2e = run_e2e(args, inputs, graphs, stream, an, al, path, timed, torch, R, L, B, Nn,
                       world)
 
+    touched_gb = L * (dom["bytes"] + (0 if fused else commit_bytes)) / 1e9
     step_desc = (f"prep + {L} verify with the previous step's commit folded in + accept"
                  if fused else f"prep + {L} verify + accept + {L} in-place commit")
     roof = {"bound": "hbm", "kernel": dom["kernel"], "achieved": dom["gbs"], "peak": hbm,
@@ -422,13 +423,17 @@ def run_gpu(args, rank, world, local):
                    "H_qk": 16, "H_v": 32, "d_k": 128, "d_v": 128, "io": "bf16",
                    "state": "fp32", "accumulate": "fp32", "mode": args.mode,
                    "step": f"{step_desc} (CUDA graph)",
-                   "l2": "inputs larger than L2 (~9 GB touched per step, L2 129 MB)",
+                   "l2": f"inputs larger than L2 (~{touched_gb:.1f} GB touched per step, "
+                         f"L2 129 MB)",
                    "distinct_step_inputs": R, "parallelism": f"dp{world} (sequences)"},
         "roofline": roof,
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
     }
     if e2e is not None:
+        # the end-to-end step can be no faster than its host-to-device bytes at the
+        # measured link rate, nor than the device step
+        e2e["bound_ms_per_step"] = max(ms / K, e2e["link_ms_per_step"])
         result["e2e"] = e2e
     return result
 
@@ -472,11 +477,24 @@ def run_e2e(args, inputs, graphs, stream, an, al, path, timed, torch, R, L, B, N
                 ev_done[r].record(stream)
                 done_recorded[r] = True
 
+    # The host link's own rate: one step's inputs, pinned, in one copy (best of 3, untimed
+    # for the metric); then input 0's buffer is restored from its host copy.
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    link_ms = float("inf")
+    with torch.cuda.stream(copy_stream):
+        for _ in range(3):
+            e0.record(copy_stream)
+            inputs[0].flat.copy_(host[0], non_blocking=True)
+            e1.record(copy_stream)
+            copy_stream.synchronize()
+            link_ms = min(link_ms, e0.elapsed_time(e1))
+    torch.cuda.synchronize()
     # the previous leg ended on input R - 1, so step 0 (input 0) commits its own predecessor
     ms = timed(fn, args.steps, args.warmup)
     value = L * B * Nn * args.steps * world / (ms / 1e3)
     return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": ms / args.steps,
+            "link_h2d_gbs": h2d / (link_ms * 1e-3) / 1e9, "link_ms_per_step": link_ms,
             "copies": "one copy per step, overlapped with the previous step" if overlap
                       else "serial with the step"}
 
