@@ -587,7 +587,12 @@ def run_reference(args, rank, world):
 
 
 def _flush_l2(buf):
-    buf.add_(1)          # 256 MiB written: nothing of the previous launch stays in L2
+    """Cold and clean L2 for the next launch: 256 MiB written (nothing of the previous
+    launch stays), then another 256 MiB read, so the flush's own dirty lines are written
+    back here and not inside the timed launch."""
+    half = buf.numel() // 2
+    buf[:half].add_(1)
+    buf[half:].sum()
 
 
 def _launch_times(torch, stream, fn, iters, flush):
@@ -618,7 +623,7 @@ def run_recurrent_compare(args):
     gen = torch.Generator(device=dev)
     gen.manual_seed(synth.BASE_SEED + 77)
     stream = torch.cuda.Stream(dev)
-    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    flush = torch.zeros(128 * 1024 * 1024, dtype=torch.float32, device=dev)
     dims = tgdn.Dims(cfg.H_qk, cfg.H_v, cfg.dk, cfg.dv, tgdn.BF16)
     B = 16
     rng = np.random.default_rng(synth.BASE_SEED + 78)
@@ -665,7 +670,7 @@ def run_build_times(args):
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     stream = torch.cuda.Stream(dev)
-    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    flush = torch.zeros(128 * 1024 * 1024, dtype=torch.float32, device=dev)
     out = []
     for B, budget, K, w, dmax in [(32, 64, 8, 1, 12), (32, 64, 8, 4, 12), (32, 64, 8, 8, 12),
                                   (32, 64, 8, 16, 12), (32, 128, 8, 8, 16),
@@ -694,7 +699,7 @@ def run_attention_times(args):
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     stream = torch.cuda.Stream(dev)
-    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    flush = torch.zeros(128 * 1024 * 1024, dtype=torch.float32, device=dev)
     gen = torch.Generator(device=dev)
     gen.manual_seed(synth.BASE_SEED + 91)
     rng = np.random.default_rng(synth.BASE_SEED + 92)
@@ -744,7 +749,7 @@ def per_config_summary(hbm):
     from tree_speculative_decoding_gated_gb300 import tgdn
     dev = torch.device("cuda", 0)
     stream = torch.cuda.Stream(dev)
-    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    flush = torch.zeros(128 * 1024 * 1024, dtype=torch.float32, device=dev)
     out = {}
     for name in ("cfg3", "cfg4"):
         cfg = synth.CONFIGS[name]
@@ -785,7 +790,7 @@ def recurrent_ratio(n_nodes: int):
     from tree_speculative_decoding_gated_gb300 import tgdn
     dev = torch.device("cuda", 0)
     stream = torch.cuda.Stream(dev)
-    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    flush = torch.zeros(128 * 1024 * 1024, dtype=torch.float32, device=dev)
     cfg = synth.CONFIGS["cfg3"]
     rng = np.random.default_rng(synth.BASE_SEED + 78)
     parents = [synth.random_recursive_tree(rng, n_nodes, 16) for _ in range(16)]
@@ -822,7 +827,7 @@ def run_config_times(args):
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     stream = torch.cuda.Stream(dev)
-    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    flush = torch.zeros(128 * 1024 * 1024, dtype=torch.float32, device=dev)
     hbm, kind = peaks()
     out = []
     for name in ("cfg2", "cfg3", "cfg4"):

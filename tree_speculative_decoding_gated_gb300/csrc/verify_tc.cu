@@ -119,6 +119,7 @@ constexpr int kOffA2lo = 180224;
 static_assert(kOffGP + kTcPath * 16 <= kOffKK, "commit staging fits its area");
 static_assert(kOffQK + 64 * 64 * 4 <= kOffRhi, "Gram rows fit their area");
 constexpr int kOffMeta = 196608;
+constexpr int kMaxCompact = 2048;  // sequences of a mixed launch that can be listed
 // Output staging after the second product, in the 128-byte swizzled tile layout of
 // the TMA stores that send it out: U in the Gram-row area (free once the solve is
 // done), O in an area of its own after the shared state (below), so that the next
@@ -157,6 +158,10 @@ struct TcShared {
   int c_row[2][kTcPath];  // previous-step node rows of the staged path
   int c_gi[2][kTcPath];   // index of G_s within its staged 16-byte chunk
   ItemMeta meta[2];
+  // Mixed launches: the sequences of at most 64 nodes in order (items are numbered
+  // over them, so that the CTAs only get items of this kernel).
+  int n_small;
+  int16_t small_seq[kMaxCompact];
 };
 // O: 2 tiles (64 columns each) [64 rows][128 B] bf16, 1024-byte aligned
 constexpr int kOffOst = (kOffMeta + (int)sizeof(TcShared) + 1023) / 1024 * 1024;
@@ -342,7 +347,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                  const __grid_constant__ CUtensorMap vmap, const __grid_constant__ OutMaps om,
                  int n_items, int H_qk, int H_v, int depth_max, int words, int small_only,
-                 const int32_t* __restrict__ cu,
+                 int compact, const int32_t* __restrict__ cu,
                  const int32_t* __restrict__ depth, const int32_t* __restrict__ order,
                  const int32_t* __restrict__ pos, const uint64_t* __restrict__ anc,
                  int32_t* __restrict__ status,
@@ -363,8 +368,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
   // are dealt round robin, so that the CTAs work on neighbouring heads of the
   // same rows at the same time (better DRAM locality for the v, U and o rows).
   const bool runs = cm.path != nullptr;
-  const int i_begin = runs ? (int)(((long)blockIdx.x * n_items) / gridDim.x) : (int)blockIdx.x;
-  const int i_end = runs ? (int)(((long)(blockIdx.x + 1) * n_items) / gridDim.x) : n_items;
+  int i_begin = runs ? (int)(((long)blockIdx.x * n_items) / gridDim.x) : (int)blockIdx.x;
+  int i_end = runs ? (int)(((long)(blockIdx.x + 1) * n_items) / gridDim.x) : n_items;
   const int i_step = runs ? 1 : (int)gridDim.x;
   const int grp = H_v / H_qk;  // v-heads per query/key head
   const bool fused = cm.path != nullptr;
@@ -372,7 +377,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
   // griddepcontrol.wait below touches no global memory (the first item's state
   // is only pulled into L2, which stays coherent), so it can overlap the tail of
   // the previous kernel in the stream.
-  if (tid == 0) prefetch_l2(S + (size_t)i_begin * kTcDK * kTcDV, kTcDK * kTcDV * 4);
+  if (tid == 0 && !compact) prefetch_l2(S + (size_t)i_begin * kTcDK * kTcDV, kTcDK * kTcDV * 4);
 
   if (tid == 0) {
     mbar_init(&sh.tma_bar, 1);
@@ -402,7 +407,31 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
   const uint32_t tmem = sh.tmem_slot;
   grid_dependency_wait();     // the previous kernel's writes are visible from here on
   grid_launch_dependents();   // the next kernel may start its own prologue
-  if (small_only) {  // a CTA whose items all belong to the 128-node kernel leaves at once
+  if (compact) {
+    // A mixed launch lists its sequences of at most 64 nodes (warp 0, a ballot per 32
+    // sequences) and numbers its items over them; a CTA left without items leaves.
+    if (warp == 0) {
+      const int B = n_items / H_v;
+      const int lane = tid & 31;
+      int base = 0;
+      for (int b0 = 0; b0 < B; b0 += 32) {
+        const int b = b0 + lane;
+        const bool sm = b < B && cu[b + 1] - cu[b] <= kTcNodes;
+        const unsigned m = __ballot_sync(0xffffffffu, sm);
+        if (sm) sh.small_seq[base + __popc(m & ((1u << lane) - 1u))] = static_cast<int16_t>(b);
+        base += __popc(m);
+      }
+      if (lane == 0) sh.n_small = base;
+    }
+    __syncthreads();
+    const int ni = sh.n_small * H_v;
+    i_begin = runs ? (int)(((long)blockIdx.x * ni) / gridDim.x) : (int)blockIdx.x;
+    i_end = runs ? (int)(((long)(blockIdx.x + 1) * ni) / gridDim.x) : ni;
+    if (i_begin >= i_end) {
+      if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+      return;
+    }
+  } else if (small_only) {  // a CTA whose items all belong to the 128-node kernel leaves at once
     int mine = 0;
     if (warp == 0)
       for (int it = i_begin + (tid & 31) * i_step; it < i_end; it += 32 * i_step) {
@@ -414,6 +443,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       return;
     }
   }
+
+  // the sequence of an item (listed in a mixed launch) and the offset of its state
+  auto seq_of = [&](int it) { return compact ? (int)sh.small_seq[it / H_v] : it / H_v; };
+  auto state_block = [&](int it) {
+    return ((size_t)seq_of(it) * H_v + it % H_v) * (size_t)(kTcDK * kTcDV);
+  };
 
   if (tid < kGroup) {
     // =================================================== producer warps 0-7
@@ -437,12 +472,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     const int jc = 32 * ((p >> 5) & 3) + (p & 31);
     const int rb = 64 * (p >> 7);
     float sreg[64];
-    auto sptr = [&](int item, int i) {
-      return S + (size_t)item * kTcDK * kTcDV + (size_t)(rb + i) * kTcDV + jc;
-    };
     auto issue_state = [&](int item) {  // thread 0 only
       mbar_arrive_expect_tx(&sh.st_bar, kTcDK * kTcDV * 4);
-      bulk_load(smem + kOffState, S + (size_t)item * kTcDK * kTcDV, kTcDK * kTcDV * 4,
+      bulk_load(smem + kOffState, S + state_block(item), kTcDK * kTcDV * 4,
                 &sh.st_bar);
       sh.st_issued += 1;
     };
@@ -452,7 +484,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     // when the item is published, an iteration later.)
     int c_node = -1, c_plo = 0, c_phi = 0, c_st = TGDN_SEQ_OK;
     auto load_commit_meta = [&](int it) {
-      const int bi = it / H_v;
+      const int bi = seq_of(it);
       c_plo = cm.cu[bi];
       c_phi = cm.cu[bi + 1];
       c_st = cm.status[bi];
@@ -495,7 +527,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     // formed when they are used).
     int q_lo = 0, q_hi = 0, q_st = 0;
     auto load_seq = [&](int item) {
-      const int bi = item / H_v;
+      const int bi = seq_of(item);
       q_lo = cu[bi];
       q_hi = cu[bi + 1];
       q_st = status[bi];
@@ -538,7 +570,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     for (int j = 0; item < i_end; ++j, item += i_step) {
       const int slot = j & 1;
       ItemMeta& M = sh.meta[slot];
-      const int bi = item / H_v, h = item % H_v;
+      const int bi = seq_of(item), h = item % H_v;
+      // this thread's column of the item's state (key rows rb .. rb + 63)
+      float* const s_col = S + ((size_t)bi * H_v + h) * (size_t)(kTcDK * kTcDV) +
+                           (size_t)rb * kTcDV + jc;
       const int lo = pf.lo, N = pf.N;
       const int next = item + i_step;
       // (small_only: sequences above 64 nodes belong to the 128-node kernel; their
@@ -670,7 +705,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       // withhold one item's product: the consumer's bounded wait for it then expires.)
       if (p == kGroup - 1) {
         bool ok255 = true;
-        if (item == hold_item) {
+        if (hold_item >= 0 && seq_of(item) * H_v + item % H_v == hold_item) {
           ok255 = false;
         } else if (skip) {
           mbar_arrive(&sh.s1_done[slot]);
@@ -799,7 +834,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       // once per step and never by this SM again within the launch)
       if (L > 0) {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) __stcg(sptr(item, i), sreg[i]);
+        for (int i = 0; i < 64; ++i) __stcg(s_col + (size_t)i * kTcDV, sreg[i]);
       }
       // A block boundary here keeps the compiler from moving the next iteration's work
       // in among these memory instructions (measured: that interleaving made the
@@ -820,8 +855,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     // operand area (the same swizzled layout), where R is then formed in place.
     int cv_lo = 0, cv_hi = 0;  // node rows of the item whose V rows go out next
     auto load_vseq = [&](int item) {
-      cv_lo = cu[item / H_v];
-      cv_hi = cu[item / H_v + 1];
+      cv_lo = cu[seq_of(item)];
+      cv_hi = cu[seq_of(item) + 1];
     };
     // a passed-over item (small_only, above 64 nodes) gets no V rows
     auto v_wanted = [&]() { return !(small_only && cv_hi - cv_lo > kTcNodes); };
@@ -1084,7 +1119,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
   __syncthreads();
   if (sh.abort && tid == 0) {
     for (int it2 = i_begin; it2 < i_end; it2 += i_step)
-      atomicCAS(&status[it2 / H_v], TGDN_SEQ_OK, TGDN_SEQ_TIMEOUT);
+      atomicCAS(&status[seq_of(it2)], TGDN_SEQ_OK, TGDN_SEQ_TIMEOUT);
     if (sh.tma_issued > 0) (void)mbar_wait(&sh.tma_bar, (sh.tma_issued - 1) & 1, wait_ns);
     if (sh.v_issued > 0) (void)mbar_wait(&sh.v_bar, (sh.v_issued - 1) & 1, wait_ns);
   }
@@ -1142,7 +1177,8 @@ cudaError_t launch_verify_tc(const tgdn_tree& t, const tgdn_dims& d, const CUten
   lc.numAttrs = 1;
   const WaitHooks hk = wait_hooks();
   e = cudaLaunchKernelEx(&lc, kern, qmap, kmap, vmap, om, (int)items, d.H_qk, d.H_v, t.depth_max,
-                         t.words, small_only ? 1 : 0, t.cu_nodes, t.depth, t.order, t.pos,
+                         t.words, small_only ? 1 : 0, (small_only && t.B <= kMaxCompact) ? 1 : 0,
+                         t.cu_nodes, t.depth, t.order, t.pos,
                          t.anc, t.status, g, b, S, static_cast<__nv_bfloat16*>(o), U, G, cm,
                          hk.wait_ns ? hk.wait_ns : kWaitLimitNs, hk.hold_item);
   if (e != cudaSuccess) return e;
