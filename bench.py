@@ -587,20 +587,19 @@ def run_reference(args, rank, world):
 
 
 def _flush_l2(buf):
-    """Cold and clean L2 for the next launch: 256 MiB written (nothing of the previous
-    launch stays), then another 256 MiB read, so the flush's own dirty lines are written
-    back here and not inside the timed launch."""
-    half = buf.numel() // 2
-    buf[:half].add_(1)
-    buf[half:].sum()
+    buf.add_(1)          # 256 MiB written: nothing of the previous launch stays in L2
 
 
 def _launch_times(torch, stream, fn, iters, flush):
-    """Per-launch device times (us) with L2 flushed before every launch."""
+    """Per-launch device times (us) with L2 flushed before every launch.  A ~100 us spin on
+    the GPU after the flush keeps the stream busy while the host enqueues the call, so
+    the events bracket the launch's device time and not the host's work for it (tensor
+    maps, launch setup)."""
     ts = []
     for _ in range(iters):
         with torch.cuda.stream(stream):
             _flush_l2(flush)
+            torch.cuda._sleep(200_000)
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
@@ -623,7 +622,7 @@ def run_recurrent_compare(args):
     gen = torch.Generator(device=dev)
     gen.manual_seed(synth.BASE_SEED + 77)
     stream = torch.cuda.Stream(dev)
-    flush = torch.zeros(128 * 1024 * 1024, dtype=torch.float32, device=dev)
+    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)
     dims = tgdn.Dims(cfg.H_qk, cfg.H_v, cfg.dk, cfg.dv, tgdn.BF16)
     B = 16
     rng = np.random.default_rng(synth.BASE_SEED + 78)
@@ -670,7 +669,7 @@ def run_build_times(args):
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     stream = torch.cuda.Stream(dev)
-    flush = torch.zeros(128 * 1024 * 1024, dtype=torch.float32, device=dev)
+    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)
     out = []
     for B, budget, K, w, dmax in [(32, 64, 8, 1, 12), (32, 64, 8, 4, 12), (32, 64, 8, 8, 12),
                                   (32, 64, 8, 16, 12), (32, 128, 8, 8, 16),
@@ -699,7 +698,7 @@ def run_attention_times(args):
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     stream = torch.cuda.Stream(dev)
-    flush = torch.zeros(128 * 1024 * 1024, dtype=torch.float32, device=dev)
+    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)
     gen = torch.Generator(device=dev)
     gen.manual_seed(synth.BASE_SEED + 91)
     rng = np.random.default_rng(synth.BASE_SEED + 92)
@@ -749,7 +748,7 @@ def per_config_summary(hbm):
     from tree_speculative_decoding_gated_gb300 import tgdn
     dev = torch.device("cuda", 0)
     stream = torch.cuda.Stream(dev)
-    flush = torch.zeros(128 * 1024 * 1024, dtype=torch.float32, device=dev)
+    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)
     out = {}
     for name in ("cfg3", "cfg4"):
         cfg = synth.CONFIGS[name]
@@ -790,7 +789,7 @@ def recurrent_ratio(n_nodes: int):
     from tree_speculative_decoding_gated_gb300 import tgdn
     dev = torch.device("cuda", 0)
     stream = torch.cuda.Stream(dev)
-    flush = torch.zeros(128 * 1024 * 1024, dtype=torch.float32, device=dev)
+    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)
     cfg = synth.CONFIGS["cfg3"]
     rng = np.random.default_rng(synth.BASE_SEED + 78)
     parents = [synth.random_recursive_tree(rng, n_nodes, 16) for _ in range(16)]
@@ -827,7 +826,7 @@ def run_config_times(args):
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     stream = torch.cuda.Stream(dev)
-    flush = torch.zeros(128 * 1024 * 1024, dtype=torch.float32, device=dev)
+    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)
     hbm, kind = peaks()
     out = []
     for name in ("cfg2", "cfg3", "cfg4"):
