@@ -392,7 +392,7 @@ def run_gpu(args, rank, world, local):
         v_gbs = verify_bytes / (verify_us * 1e-6) / 1e9
         c_gbs = commit_bytes / (commit_us * 1e-6) / 1e9
         vd = dict(kernel="verify_tc_kernel", us=verify_us, bytes=verify_bytes, gbs=v_gbs)
-        cd = dict(kernel="commit_kernel", us=commit_us, bytes=commit_bytes, gbs=c_gbs)
+        cd = dict(kernel="commit128_kernel", us=commit_us, bytes=commit_bytes, gbs=c_gbs)
         dom, other = (vd, cd) if verify_us >= commit_us else (cd, vd)
 
     e2e = None

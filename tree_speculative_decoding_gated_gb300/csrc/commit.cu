@@ -128,7 +128,7 @@ constexpr uint32_t kC128Bytes = kC128Rows * 128 * 4;  // one state block, 32 KiB
 
 template <typename T>
 __global__ void __launch_bounds__(kC128Threads, 4)
-commit128_kernel(int H_qk, int H_v, int dk, int depth_max, int words,
+commit128_kernel(int H_qk, int H_v, int dk, int depth_max, int n_max, int words,
                  const int32_t* __restrict__ cu, const int32_t* __restrict__ depth,
                  const int32_t* __restrict__ order, const int32_t* __restrict__ pos,
                  const uint64_t* __restrict__ anc, int32_t* __restrict__ status,
@@ -140,12 +140,13 @@ commit128_kernel(int H_qk, int H_v, int dk, int depth_max, int words,
   float* st = c128;                       // [64][128] the state block (bulk copy)
   float* ck = st + kC128Rows * 128;       // [DM1][64]  e^{G*-G_s} k_s[row]
   float* us = ck + DM1 * kC128Rows;       // [DM1][128] u_s
+  // sized by the launch's n_max (so that more CTAs fit an SM for small trees)
+  uint64_t* s_anc = reinterpret_cast<uint64_t*>(us + DM1 * 128);  // [position][word]
+  int* s_ord = reinterpret_cast<int*>(s_anc + (size_t)n_max * words);
+  float* s_G = reinterpret_cast<float*>(s_ord + n_max);
   __shared__ uint64_t bar;
   __shared__ int s_path[TGDN_MAX_DEPTH + 1];
-  __shared__ int s_ord[TGDN_MAX_NODES];
-  __shared__ float s_G[TGDN_MAX_NODES];
   __shared__ float s_c[TGDN_MAX_DEPTH + 1];
-  __shared__ uint64_t s_anc[TGDN_MAX_NODES * (TGDN_MAX_NODES / 64)];  // [position][word]
   __shared__ uint64_t s_mask[TGDN_MAX_NODES / 64];
   __shared__ int s_len;
 
@@ -257,14 +258,16 @@ static cudaError_t launch_commit_t(const tgdn_tree& t, const tgdn_dims& d,
     const long grid = (long)t.B * d.H_v * (d.d_k / kC128Rows);
     if (grid == 0) return cudaSuccess;
     if (grid > 0x7fffffffL) return cudaErrorInvalidConfiguration;
-    const size_t smem = kC128Bytes + (size_t)(t.depth_max + 1) * (kC128Rows + 128) * sizeof(float);
+    const size_t smem = kC128Bytes + (size_t)(t.depth_max + 1) * (kC128Rows + 128) * sizeof(float) +
+                        (size_t)t.n_max * t.words * sizeof(uint64_t) +
+                        (size_t)t.n_max * (sizeof(int) + sizeof(float));
     const auto kern = commit128_kernel<T>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<(unsigned)grid, kC128Threads, smem, s>>>(
-        d.H_qk, d.H_v, d.d_k, t.depth_max, t.words, t.cu_nodes, t.depth, t.order, t.pos, t.anc,
-        t.status, accept_node, static_cast<const T*>(k), U, G, S_in, S_out);
+        d.H_qk, d.H_v, d.d_k, t.depth_max, t.n_max, t.words, t.cu_nodes, t.depth, t.order, t.pos,
+        t.anc, t.status, accept_node, static_cast<const T*>(k), U, G, S_in, S_out);
     return cudaGetLastError();
   }
   const int rblocks = (d.d_k + kCommitRows - 1) / kCommitRows;
