@@ -58,7 +58,12 @@ struct T8Meta {
   float bb[kT8Nodes];
   float G[kT8Nodes];
   uint8_t anc_at[kT8Path + 1][kT8Nodes];  // [depth][node]: ancestor of node at that depth
+  // Mixed launches: the sequences above 64 nodes in order (items are numbered over them,
+  // so that no CTA steps over the 64-node kernel's items).
+  int n_big;
+  int16_t big_seq[2048];
 };
+constexpr int kT8MaxList = 2048;
 constexpr int kT8SmemBytes = kO8Meta + (int)sizeof(T8Meta) + 1024;
 static_assert(kT8SmemBytes <= 227 * 1024, "fits one CTA per SM");
 static_assert(kO8SS + 256 * kT8Path * 4 <= kO8GK, "solve scratch fits");
@@ -117,6 +122,37 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = M.tmem_slot;
+  // In a launch that also runs the 64-node kernel, list the sequences above 64 nodes
+  // (warp 0, a ballot per 32 sequences) and number the items over them.
+  const bool compact = big_only && n_items / H_v <= kT8MaxList;
+  int n_it = n_items;
+  if (compact) {
+    if (warp == 0) {
+      const int B = n_items / H_v;
+      int base = 0;
+      for (int b0 = 0; b0 < B; b0 += 32) {
+        const int bq = b0 + lane;
+        const bool big = bq < B && cu[bq + 1] - cu[bq] > 64;
+        const unsigned m = __ballot_sync(0xffffffffu, big);
+        if (big) M.big_seq[base + __popc(m & ((1u << lane) - 1u))] = static_cast<int16_t>(bq);
+        base += __popc(m);
+      }
+      if (lane == 0) M.n_big = base;
+    }
+    __syncthreads();
+    n_it = M.n_big * H_v;
+    if ((int)blockIdx.x >= n_it) {
+      if (warp == 0) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, 512);
+      }
+      return;
+    }
+  }
+  auto seq_of = [&](int it) { return compact ? (int)M.big_seq[it / H_v] : it / H_v; };
+  auto state_of = [&](int it) {
+    return S0 + ((size_t)seq_of(it) * H_v + it % H_v) * (size_t)(kT8D * kT8D);
+  };
   const int lq = warp & 3;                       // TMEM lane quarter of this warp
   const uint32_t lane_base = static_cast<uint32_t>(lq * 32) << 16;
   const int my_row = lq * 32 + lane;             // node index of this thread's TMEM lane
@@ -139,8 +175,8 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
   int nb_lo = 0, nb_hi = 0, nb_st = 0;             // the item after it
   float4 sr[8];
   auto load_bounds = [&](int it) {
-    if (it < n_items) {
-      const int b2 = it / H_v;
+    if (it < n_it) {
+      const int b2 = seq_of(it);
       nb_lo = cu[b2];
       nb_hi = cu[b2 + 1];
       nb_st = status[b2];
@@ -153,10 +189,10 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
     nx_d0 = 0;
     // (an item this launch passes over, a sequence of at most 64 nodes when the
     // 64-node kernel takes those, is not pulled into L2)
-    if (it < n_items && nx_st == TGDN_SEQ_OK && nx_hi > nx_lo &&
+    if (it < n_it && nx_st == TGDN_SEQ_OK && nx_hi > nx_lo &&
         !(big_only && nx_hi - nx_lo <= 64)) {
       nx_d0 = depth[nx_lo];
-      if (tid == 0) prefetch_l2(S0 + (size_t)it * kT8D * kT8D, kT8D * kT8D * 4);
+      if (tid == 0) prefetch_l2(state_of(it), kT8D * kT8D * 4);
       if (tid < nx_hi - nx_lo && tid <= kT8Nodes)
         prefetch_l2(v + ((size_t)(nx_lo + tid) * H_v + it % H_v) * kT8D, kT8D * 2);
       if (tid >= 32 && tid < 35) {
@@ -180,7 +216,7 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
   load_bounds((int)blockIdx.x);
   T8_PREFETCH((int)blockIdx.x)
 
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+  for (int item = blockIdx.x; item < n_it; item += gridDim.x) {
     const int h = item % H_v, qh = h / grp;
     const int lo = nx_lo, N = nx_hi - nx_lo;
     const int st = nx_st;
@@ -214,7 +250,7 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
       M.tma_n += 1;
     }
     // the item's state rows and this thread's V slice, ahead of their use
-    load_state_rows(sr, S0 + (size_t)item * kT8D * kT8D, r0, sq);
+    load_state_rows(sr, state_of(item), r0, sq);
     uint4 vreg[4];  // this thread's V row slice (32 columns), for R after the product
     if (ok && my_row < Nf) {
       const uint4* vp =
@@ -538,8 +574,8 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
   // reported as timed out, and the latest copy and product are drained (bounded).
   __syncthreads();
   if (M.abort && tid == 0) {
-    for (int it2 = blockIdx.x; it2 < n_items; it2 += gridDim.x)
-      atomicCAS(&status[it2 / H_v], TGDN_SEQ_OK, TGDN_SEQ_TIMEOUT);
+    for (int it2 = blockIdx.x; it2 < n_it; it2 += gridDim.x)
+      atomicCAS(&status[seq_of(it2)], TGDN_SEQ_OK, TGDN_SEQ_TIMEOUT);
     if (M.tma_n > 0) (void)mbar_wait(&M.tma_bar, (M.tma_n - 1) & 1);
     if (M.mma_n > 0) (void)mbar_wait(&M.mma_bar, (M.mma_n - 1) & 1);
   }
