@@ -51,7 +51,9 @@
 // its prologue may overlap the previous kernel's tail and no input is read
 // before griddepcontrol.wait.
 // In a launch above 64 nodes it takes only the sequences of at most 64 nodes
-// (small_only) and passes over the others without touching them.
+// (small_only): up to 2048 sequences each CTA lists them (a warp ballot over cu_nodes)
+// and numbers its items over that list; beyond that it deals every item and passes over
+// the larger sequences without touching them.
 // The state enters the tensor-core products as bf16 (fp32 accumulation); it is
 // read, updated and written back in fp32.
 //

@@ -19,7 +19,8 @@
 // same tree with its root elsewhere is left untouched for the SIMT kernel,
 // launched after this one (verify_simt_kernel's complement mode).
 // Persistent CTAs of 512 threads; every wait is bounded (TGDN_SEQ_TIMEOUT on
-// expiry).
+// expiry).  In a launch that also runs the 64-node kernel, up to 2048 sequences, each
+// CTA lists the sequences above 64 nodes and numbers its items over them.
 #include "tgdn_device.cuh"
 #include "tgdn_kernels.h"
 
