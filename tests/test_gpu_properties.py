@@ -240,3 +240,17 @@ def test_two_step_rollback_free():
 
 def test_non_ancestor_edits_on_the_128_node_kernel():
     test_non_ancestor_edits_leave_outputs_bitwise("bf16", n_max=100)
+
+
+@pytest.mark.parametrize("io,d", [("bf16", 128), ("f32", 64)])
+def test_header_maximum_sizes(io, d):
+    """n_max = TGDN_MAX_NODES (256) and depth_max = TGDN_MAX_DEPTH (64): 256-node trees
+    (random, a star, a 65-node chain reaching depth 64) next to a single node, through prep,
+    verification, acceptance and the commit (four ancestor-mask words per node, a 65-entry
+    accepted path)."""
+    rng = np.random.default_rng(256)
+    parents = [synth.random_recursive_tree(rng, 256, 64), synth.chain_tree(65),
+               np.array([-1] + [0] * 255, np.int32), np.array([-1], np.int32),
+               synth.random_recursive_tree(rng, 200, 40)]
+    p = custom(parents, 1, 2, d, io, 64, n_max=256, depth_max=64)
+    run_and_check(p, TOL_BF16 if io == "bf16" else TOL_F32)
