@@ -24,7 +24,8 @@
 //     tensor cores (128 value columns x 64 key rows, twice, into the TMEM
 //     columns the halves leave free) and each thread forms S = e^{G*} S + D;
 //     S -> bf16 operand (K-major, 128-byte swizzle); TMA of the item's key and
-//     query rows -> A = [K; Q]; tree metadata (prefetched as raw values) ->
+//     query rows -> A = [K; Q]; tree metadata (staged in shared memory by
+//     asynchronous copies an item ahead) ->
 //     root paths (reused for the next head of the same sequence) and
 //     path-cumulative gates; the committed state goes back to HBM last;
 //   the producer's thread 255, item j+1, while the others build the metadata:
@@ -120,6 +121,25 @@ constexpr int kOffA2hi = 163840;  // [T; W] operand, K-major [16 row groups][8][
 constexpr int kOffA2lo = 180224;
 static_assert(kOffGP + kTcPath * 16 <= kOffKK, "commit staging fits its area");
 static_assert(kOffQK + 64 * 64 * 4 <= kOffRhi, "Gram rows fit their area");
+// Small values the producer needs an item later arrive by 4- and 8-byte asynchronous
+// copies into two parity slots, so that no register carries them across an iteration
+// and nothing waits on them before the item's first barrier: the node metadata of the
+// next item (and the ancestor mask of each topological position), and the pending
+// commit's accepted path two items ahead (lane l: entry l) with that sequence's bounds.
+struct NodeStage {
+  int dep[kTcNodes], pos[kTcNodes], ord[kTcNodes];
+  float gg[kTcNodes], bb[kTcNodes];
+  uint64_t anc[kTcNodes];
+};
+struct CommitStage {
+  int path[32];
+  int lo, hi, st, pad;
+};
+constexpr int kOffNS = kOffQK + 64 * 64 * 4;  // the gap after the Gram rows
+constexpr int kOffCS = kOffNS + 2 * (int)sizeof(NodeStage);
+static_assert(kOffNS % 16 == 0 && kOffCS % 16 == 0 &&
+                  kOffCS + 2 * (int)sizeof(CommitStage) <= kOffRhi,
+              "metadata staging fits between the Gram rows and the R operand");
 constexpr int kOffMeta = 196608;
 constexpr int kMaxCompact = 2048;  // sequences of a mixed launch that can be listed
 // Output staging after the second product, in the 128-byte swizzled tile layout of
@@ -211,11 +231,10 @@ __device__ __forceinline__ bool group_wait_n(uint64_t* bar, uint32_t parity, int
   return named_sync_and(bar_id, n, ok);
 }
 
-// Everything the producer prefetches for one item (one node per thread < 64).
+// The bounds and status of the next item's sequence (its node metadata is staged in
+// shared memory).
 struct Prefetch {
   int lo, N, st;
-  int dep, pos, ord;
-  float gg, bb;
 };
 
 // v[k] for a run-time k in [0, N), N a power of two: a binary multiplexer over
@@ -480,21 +499,28 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                 &sh.st_bar);
       sh.st_issued += 1;
     };
+    NodeStage* const NS = reinterpret_cast<NodeStage*>(smem + kOffNS);
+    CommitStage* const CS = reinterpret_cast<CommitStage*>(smem + kOffCS);
     // Warp 0, two items ahead of its staging: the item's accepted path in the
-    // previous tree (lane l holds entry l) and that sequence's bounds and status.
-    // (Raw values only: nothing here waits for these loads; they are combined
-    // when the item is published, an iteration later.)
-    int c_node = -1, c_plo = 0, c_phi = 0, c_st = TGDN_SEQ_OK;
-    auto load_commit_meta = [&](int it) {
+    // previous tree (lane l copies entry l) and that sequence's bounds and status,
+    // into parity slot x.  (Raw values: they are combined when the item is
+    // published, an iteration later, after this thread's cp_async_wait_all.)
+    auto load_commit_meta = [&](int it, int x) {
       const int bi = seq_of(it);
-      c_plo = cm.cu[bi];
-      c_phi = cm.cu[bi + 1];
-      c_st = cm.status[bi];
-      c_node = cm.path[(size_t)bi * cm.path_len + (p < cm.path_len ? p : cm.path_len - 1)];
+      CommitStage& cs = CS[x];
+      cp_async4(&cs.path[p],
+                cm.path + (size_t)bi * cm.path_len + (p < cm.path_len ? p : cm.path_len - 1));
+      if (p == 0) {
+        cp_async4(&cs.lo, cm.cu + bi);
+        cp_async4(&cs.hi, cm.cu + bi + 1);
+        cp_async4(&cs.st, cm.status + bi);
+      }
     };
     // Warp 0: the item's staged path (entries after the first invalid one are
     // ignored) -> c_L[cb], c_row[cb].
     auto publish_commit = [&](int cb) {
+      const CommitStage& cs = CS[cb];
+      const int c_plo = cs.lo, c_phi = cs.hi, c_st = cs.st, c_node = cs.path[p];
       const bool valid = c_st == TGDN_SEQ_OK && p < cm.path_len && c_node >= 0 &&
                          c_node < c_phi - c_plo;
       const int L = __ffs(__ballot_sync(0xffffffffu, !valid)) - 1;  // path_len <= 31
@@ -535,33 +561,39 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       q_st = status[bi];
     };
     Prefetch pf;
-    auto load_meta = [&](int item) {  // node metadata; the bounds come from load_seq
-      const int h = item % H_v;
+    // The bounds come from load_seq; warps 0-1 copy the node metadata (node p) and the
+    // ancestor mask of topological position p (word 0: positions < 64) into slot x.
+    auto load_meta = [&](int item, int x) {
       pf.lo = q_lo;
       pf.N = q_hi - q_lo;
       pf.st = q_st;
       // (rows of a sequence whose bounds tree prep found bad are never touched)
-      if (pf.st == TGDN_SEQ_OK && p < pf.N && p < kTcNodes) {
-        pf.dep = depth[pf.lo + p];
-        pf.pos = pos[pf.lo + p];
-        pf.ord = order[pf.lo + p];
-        pf.gg = g[(size_t)(pf.lo + p) * H_v + h];
-        pf.bb = bta[(size_t)(pf.lo + p) * H_v + h];
+      if (p < kMetaThreads && pf.st == TGDN_SEQ_OK && p < pf.N) {
+        const size_t r = (size_t)(pf.lo + p);
+        const int h = item % H_v;
+        NodeStage& ns = NS[x];
+        cp_async4(&ns.dep[p], depth + r);
+        cp_async4(&ns.pos[p], pos + r);
+        cp_async4(&ns.ord[p], order + r);
+        cp_async4(&ns.gg[p], g + r * H_v + h);
+        cp_async4(&ns.bb[p], bta + r * H_v + h);
+        cp_async8(&ns.anc[p], anc + r * words);
       }
     };
     int item = i_begin;
     load_seq(item);
-    load_meta(item);
+    load_meta(item, 0);
     if (item + i_step < i_end) load_seq(item + i_step);
     if (p == 0 && !(small_only && pf.N > kTcNodes)) issue_state(item);
     if (fused) {
       if (p < 32) {
-        load_commit_meta(item);
+        load_commit_meta(item, 0);
+        cp_async_wait_all();
         publish_commit(0);
       }
       named_sync(kBarP, kGroup);
       stage_commit(item, 0);
-      if (p < 32 && item + i_step < i_end) load_commit_meta(item + i_step);
+      if (p < 32 && item + i_step < i_end) load_commit_meta(item + i_step, 1);
     }
 
     int prev_bi = -1;  // sequence of the previous item when its tree was valid
@@ -582,15 +614,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       // items pass through without state, solve or writes)
       const bool skip = small_only && N > kTcNodes;
       bool ok = (pf.st == TGDN_SEQ_OK) && N > 0 && N <= kTcNodes;
-      // this node's ancestor-mask row (its position came with the prefetched
-      // metadata); used for the root paths at the end of the iteration
-      uint64_t my_anc = 0;
-      if (ok && p < N) {
-        const bool v_ok = pf.dep >= 0 && pf.dep <= depth_max && pf.dep <= kTcDepth &&
-                          pf.pos >= 0 && pf.pos < N && pf.ord >= 0 && pf.ord < N;
-        if (v_ok) my_anc = anc[(size_t)(lo + pf.pos) * words];  // positions < 64: word 0
-        else ok = false;
-      }
       // this item's state, from the bulk copy into the [K;Q] and operand areas
       if (!skip) {
         if (!group_wait(&sh.st_bar, nst & 1, kBarP, p == 0, abort, wait_ns)) break;
@@ -600,12 +623,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         for (int i = 0; i < 64; ++i) sreg[i] = st[i * kTcDV];
       }
       int L = 0;
-      if (fused) {
-        cp_async_wait_all();
-        if (p < 32 && next < i_end) publish_commit(slot ^ 1);  // the next item's path
-      }
-      // every thread has read its state rows (and the staged commit rows are visible):
-      // the areas are free for this item's [K;Q] rows and the commit operands
+      // this thread's staged copies (commit rows, node metadata, path words) have landed
+      if (fused || p < kMetaThreads) cp_async_wait_all();
+      if (fused && p < 32 && next < i_end) publish_commit(slot ^ 1);  // the next item's path
+      // every thread has read its state rows (and the staged rows are visible to the
+      // group after the barrier): the areas are free for this item's [K;Q] rows and the
+      // commit operands
       fence_proxy_async_smem();
       if (!named_sync_and(kBarP, kGroup, !*abort)) break;
       if (fused) L = sh.c_L[slot];
@@ -744,6 +767,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         // (its previous user), then the root paths.
         bool go = j < 2 || group_wait_n(&sh.tmem_free[slot], ((j >> 1) + 1) & 1, kBarM,
                                         kMetaThreads, p == 0, abort, wait_ns);
+        const NodeStage& ns = NS[slot];
         if (go) {
           if (p == 0) {
             M.lo = lo;
@@ -755,17 +779,23 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             M.zrows = (skip || pf.st == TGDN_SEQ_BAD_RANGE || N < 0) ? 0 : N;
           }
           if (ok && p < N) {
-            M.dep[p] = pf.dep;
-            M.pos[p] = pf.pos;
-            M.ord[p] = pf.ord;
-            M.gg[p] = pf.gg;
-            M.bb[p] = pf.bb;
+            const int dp = ns.dep[p], ps = ns.pos[p], od = ns.ord[p];
+            if (dp >= 0 && dp <= depth_max && dp <= kTcDepth && ps >= 0 && ps < N && od >= 0 &&
+                od < N) {
+              M.dep[p] = dp;
+              M.pos[p] = ps;
+              M.ord[p] = od;
+              M.gg[p] = ns.gg[p];
+              M.bb[p] = ns.bb[p];
+            } else {
+              ok = false;
+            }
           }
         }
-        // the next item's small loads and commit bounds go out now; they land while
-        // this item's paths are built
-        if (next < i_end) load_meta(next);
-        if (p < 32 && fused && next + i_step < i_end) load_commit_meta(next + i_step);
+        // the next item's metadata and a later item's commit bounds go out now (into
+        // the other slots); they land while this item's paths are built
+        if (next < i_end) load_meta(next, slot ^ 1);
+        if (p < 32 && fused && next + i_step < i_end) load_commit_meta(next + i_step, slot);
         if (go) {
           named_sync(kBarM, kMetaThreads);  // this slot's node metadata is written
           // root paths from the ancestor masks (bits = topological positions,
@@ -786,7 +816,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             M.G[p] = acc;
           } else if (ok && p < N) {
             const int dn = M.dep[p];
-            uint64_t mk = my_anc;
+            uint64_t mk = ns.anc[M.pos[p]];  // this node's ancestor mask (by its position)
             bool pk = __popcll(mk) == dn + 1 && ((mk >> M.pos[p]) & 1ull);
             uint8_t* prow = M.path[p];
             reinterpret_cast<uint4*>(prow)[0] = make_uint4(0u, 0u, 0u, 0u);
@@ -828,7 +858,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       if (p >= kMetaThreads) named_sync(kBarW, kGroup);
       // (every thread takes the next item's bounds and status, which decide whether
       // it is passed over; only warps 0-1 load node metadata)
-      if (p >= kMetaThreads && next < i_end) load_meta(next);
+      if (p >= kMetaThreads && next < i_end) load_meta(next, slot ^ 1);
       if (next < i_end && next + i_step < i_end) load_seq(next + i_step);
       if (fused && next < i_end) stage_commit(next, slot ^ 1);
       if (!skip) ++npr;
