@@ -68,6 +68,8 @@
 // with the sum as one tensor-core product, writes it back in place (the
 // committed state) and verifies from it.  The state then crosses HBM once in
 // each direction per step.
+#include <type_traits>
+
 #include "tgdn_device.cuh"
 #include "tgdn_kernels.h"
 
@@ -253,6 +255,24 @@ __device__ __forceinline__ float pick(const float (&v)[N], int k) {
   return t[0];
 }
 
+// v[k] for k in [LO, LO + R) (R a power of two, the range within v): the same
+// multiplexer over R candidates only.  (k outside the range picks some candidate.)
+template <int LO, int R, int N>
+__device__ __forceinline__ float pick_range(const float (&v)[N], int k) {
+  static_assert(LO >= 0 && LO + R <= N && (R & (R - 1)) == 0, "range within the sums");
+  const int d = k - LO;
+  float t[R];
+#pragma unroll
+  for (int m = 0; m < R; ++m) t[m] = v[LO + m];
+#pragma unroll
+  for (int w = R / 2, bit = 0; w >= 1; w /= 2, ++bit) {
+    const bool hi = (d >> bit) & 1;
+#pragma unroll
+    for (int m = 0; m < w; ++m) t[m] = hi ? t[2 * m + 1] : t[2 * m];
+  }
+  return t[0];
+}
+
 // Byte j of the packed root path (a node index).
 __device__ __forceinline__ int path_at(const uint32_t (&pw)[8], int j) {
   return static_cast<int>((pw[j >> 2] >> (8 * (j & 3))) & 0xffu);
@@ -320,7 +340,10 @@ __device__ __forceinline__ void solve_path_row(const ItemMeta& M, const float* K
   int pn = wmax > 0 ? prow[wmax - 1] : 0;  // the next entry's node
   float Gi = M.G[pi], bi = M.bb[pi];
   float qi = t_row ? 0.f : GRq[pi ^ xq];
-  for (int i = wmax; i >= 0; --i) {
+  // One step at index i: its update width W (entries 0 .. W-1 cover 0 .. i-2) and the
+  // range [LO, LO + R) that holds acc_{i-1}.
+  auto step = [&](int i, auto Wc, auto LOc, auto Rc) {
+    constexpr int W = decltype(Wc)::value, LO = decltype(LOc)::value, R = decltype(Rc)::value;
     const int pnn = i > 1 ? prow[i - 2] : 0;
     const float Gnx = M.G[pn], bnx = M.bb[pn];
     const float qnx = t_row ? 0.f : GRq[pn ^ xq];
@@ -328,7 +351,7 @@ __device__ __forceinline__ void solve_path_row(const ItemMeta& M, const float* K
     const uint32_t GRs = smem_addr(GRi);
     const float kn = GRi[pn];                // k_{p_i}.k_{p_{i-1}}
     const float yp = t_row ? (i == dn ? 1.f : 0.f) : qi;
-    const float base = pick<NA>(acc, i - 1);  // acc_{i-1} before this step's term
+    const float base = pick_range<LO, R>(acc, i - 1);  // acc_{i-1} before this step's term
     const float rho = yp - ai;
     const bool own = i <= dn;
     const float s = own ? rho * bi : 0.f;
@@ -340,26 +363,69 @@ __device__ __forceinline__ void solve_path_row(const ItemMeta& M, const float* K
       *reinterpret_cast<__nv_bfloat16*>(smem + kOffA2hi + off) = hi;
       *reinterpret_cast<__nv_bfloat16*>(smem + kOffA2lo + off) = lw;
     }
-    const int lim = i - 1;  // entries 0 .. i-2 take their terms here
-    if (lim <= 4) {
-      path_update<4>(acc, pw, s, GRs);
-    } else if (lim <= 8) {
-      path_update<8>(acc, pw, s, GRs);
-    } else if (lim <= 12) {
-      path_update<12>(acc, pw, s, GRs);
-    } else if (lim <= 16) {
-      path_update<16>(acc, pw, s, GRs);
-    } else if (lim <= 24) {
-      path_update<(NA < 24 ? NA : 24)>(acc, pw, s, GRs);
-    } else {
-      path_update<NA>(acc, pw, s, GRs);
-    }
+    path_update<W>(acc, pw, s, GRs);
     ai = fmaf(s, kn, base);
     pi = pn;
     pn = pnn;
     Gi = Gnx;
     bi = bnx;
     qi = qnx;
+  };
+  using C4 = std::integral_constant<int, 4>;
+  using C8 = std::integral_constant<int, 8>;
+  using C12 = std::integral_constant<int, 12>;
+  using C16 = std::integral_constant<int, 16>;
+  if constexpr (NA == 16) {
+    // Four phases by the width of the update (i - 1 in [13, 15], [9, 12], [5, 8],
+    // [-1, 4]); within a phase acc_{i-1} is one of 4 (or 8) entries, a small
+    // multiplexer instead of one over all 16.  (At i = 0 the picked value is unused.)
+    int i = wmax;
+    for (; i >= 14; --i) step(i, C16{}, std::integral_constant<int, 12>{}, C4{});
+    for (; i >= 10; --i) step(i, C12{}, std::integral_constant<int, 9>{}, C4{});
+    for (; i >= 6; --i) step(i, C8{}, std::integral_constant<int, 5>{}, C4{});
+    for (; i >= 0; --i) step(i, C4{}, std::integral_constant<int, 0>{}, C8{});
+  } else {
+    for (int i = wmax; i >= 0; --i) {
+      const int pnn = i > 1 ? prow[i - 2] : 0;
+      const float Gnx = M.G[pn], bnx = M.bb[pn];
+      const float qnx = t_row ? 0.f : GRq[pn ^ xq];
+      const float* GRi = KK + pi * kKKStride;  // K K^T row p_i (padded, unrotated)
+      const uint32_t GRs = smem_addr(GRi);
+      const float kn = GRi[pn];                // k_{p_i}.k_{p_{i-1}}
+      const float yp = t_row ? (i == dn ? 1.f : 0.f) : qi;
+      const float base = pick<NA>(acc, i - 1);  // acc_{i-1} before this step's term
+      const float rho = yp - ai;
+      const bool own = i <= dn;
+      const float s = own ? rho * bi : 0.f;
+      if (own) {
+        const float rw = rho * __expf(gofs - Gi);
+        const __nv_bfloat16 hi = __float2bfloat16_rn(rw);
+        const __nv_bfloat16 lw = __float2bfloat16_rn(rw - __bfloat162float(hi));
+        const int off = atom_off(a2row, pi >> 3) + (pi & 7) * 2;
+        *reinterpret_cast<__nv_bfloat16*>(smem + kOffA2hi + off) = hi;
+        *reinterpret_cast<__nv_bfloat16*>(smem + kOffA2lo + off) = lw;
+      }
+      const int lim = i - 1;  // entries 0 .. i-2 take their terms here
+      if (lim <= 4) {
+        path_update<4>(acc, pw, s, GRs);
+      } else if (lim <= 8) {
+        path_update<8>(acc, pw, s, GRs);
+      } else if (lim <= 12) {
+        path_update<12>(acc, pw, s, GRs);
+      } else if (lim <= 16) {
+        path_update<16>(acc, pw, s, GRs);
+      } else if (lim <= 24) {
+        path_update<(NA < 24 ? NA : 24)>(acc, pw, s, GRs);
+      } else {
+        path_update<NA>(acc, pw, s, GRs);
+      }
+      ai = fmaf(s, kn, base);
+      pi = pn;
+      pn = pnn;
+      Gi = Gnx;
+      bi = bnx;
+      qi = qnx;
+    }
   }
 }
 
