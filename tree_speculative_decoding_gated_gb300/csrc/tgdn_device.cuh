@@ -139,6 +139,11 @@ __device__ __forceinline__ void named_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Arrival on hardware barrier `id` (of `count` threads) without waiting for it.
+__device__ __forceinline__ void named_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Barrier among `count` threads that also returns the AND of `pred` over them.
 __device__ __forceinline__ bool named_sync_and(int id, int count, bool pred) {
   uint32_t r;

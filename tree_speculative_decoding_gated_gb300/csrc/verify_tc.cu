@@ -27,7 +27,8 @@
 //     query rows -> A = [K; Q]; tree metadata (staged in shared memory by
 //     asynchronous copies an item ahead) ->
 //     root paths (reused for the next head of the same sequence) and
-//     path-cumulative gates; the committed state goes back to HBM last;
+//     path-cumulative gates; the committed state goes back to HBM last (warps
+//     2-7 while warps 0-1 build the paths, once the metadata copies are out);
 //   the producer's thread 255, item j+1, while the others build the metadata:
 //     the first product into TMEM half (j+1) & 1,
 //        D[:, 0:128] = A S0,  D[:, 128:192] = A K^T,
@@ -862,6 +863,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         // the other slots); they land while this item's paths are built
         if (next < i_end) load_meta(next, slot ^ 1);
         if (p < 32 && fused && next + i_step < i_end) load_commit_meta(next + i_step, slot);
+        // those copies are out: warps 2-7 may now fill the global-memory path with the
+        // commit staging and their share of the state write-back
+        named_arrive(kBarW, kGroup);
         if (go) {
           named_sync(kBarM, kMetaThreads);  // this slot's node metadata is written
           // root paths from the ancestor masks (bits = topological positions,
@@ -916,11 +920,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             mbar_arrive(&sh.s1_done[slot]);  // the metadata above is written
           }
         }
-        named_sync(kBarW, kGroup);
       }
-      // The state goes back only once warps 0-1 have their paths: a burst of stores
-      // issued earlier sits in the load/store queue ahead of their metadata loads
-      // (measured: the metadata phase then took up to twice as long).
+      // Warps 2-7 stage the next commit and send their share of the state back once warps
+      // 0-1 have issued their metadata copies (a burst of stores issued earlier would sit
+      // in the global-memory path ahead of them: measured, the metadata phase then took
+      // up to twice as long); warps 0-1 follow after their paths.
       if (p >= kMetaThreads) named_sync(kBarW, kGroup);
       // (every thread takes the next item's bounds and status, which decide whether
       // it is passed over; only warps 0-1 load node metadata)
