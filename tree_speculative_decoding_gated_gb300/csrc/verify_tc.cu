@@ -586,6 +586,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     // Warp 0: the item's staged path (entries after the first invalid one are
     // ignored) -> c_L[cb], c_row[cb].
     auto publish_commit = [&](int cb) {
+      __syncwarp();  // lane 0's copies (the bounds) are visible to the whole warp
       const CommitStage& cs = CS[cb];
       const int c_plo = cs.lo, c_phi = cs.hi, c_st = cs.st, c_node = cs.path[p];
       const bool valid = c_st == TGDN_SEQ_OK && p < cm.path_len && c_node >= 0 &&
@@ -648,14 +649,20 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
       }
     };
     int item = i_begin;
+    // (the first item's commit path does not depend on its bounds: it goes out first,
+    // as a copy group of its own, so that its staging need not wait for them)
+    if (fused && p < 32) {
+      load_commit_meta(item, 0);
+      cp_async_commit();
+    }
     load_seq(item);
     load_meta(item, 0);
+    cp_async_commit();
     if (item + i_step < i_end) load_seq(item + i_step);
     if (p == 0 && !(small_only && pf.N > kTcNodes)) issue_state(item);
     if (fused) {
       if (p < 32) {
-        load_commit_meta(item, 0);
-        cp_async_wait_all();
+        cp_async_wait_all_but_last();  // the commit path (the metadata may still be in flight)
         publish_commit(0);
       }
       named_sync(kBarP, kGroup);
