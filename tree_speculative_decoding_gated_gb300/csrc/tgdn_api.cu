@@ -405,7 +405,7 @@ namespace {
 
 // One array per device that loads the library, alive until the process exits.
 // In host code this name is only a host-side stand-in: the device address is
-// looked up once per device with cudaGetSymbolAddress and passed to kernels.
+// looked up with cudaGetSymbolAddress (below) and passed to kernels.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[TGDN_NOALLOC_SCRATCH_BYTES];
 
 // Device address of the array in the current context.  It is looked up on every
