@@ -5,7 +5,8 @@ separate passes, and the fused call — and both are compared with the fp64 orac
 which commits each step by replaying the accepted root path and verifies the next
 tree from that committed state.  Covers the tensor-core path, its two-pass
 fallbacks (a previous tree deeper than 30, a tree above 64 nodes), invalid and
-empty sequences on either side, and the final separate commit.
+empty sequences on either side, accepted paths of the full 31 entries, and the final
+separate commit.
 """
 import numpy as np
 import pytest
@@ -149,6 +150,23 @@ def test_deep_previous_tree_runs_two_passes():
                  all_match=True)
     p2 = _custom([synth.random_recursive_tree(rng, 64, 12), synth.chain_tree(20)], 4, 64, 30)
     check_decode([p1, p2], p1.S0)
+
+
+def test_deep_trees_and_long_accepted_paths_fused():
+    """Depth-30 chains and deep random trees on three consecutive steps with every draft
+    token matching: the accepted paths (up to 31 entries) go through the fused commit's
+    32-entry product, and each step's verify through the 30-deep path solve."""
+    rng = np.random.default_rng(11)
+    steps = []
+    for s in range(3):
+        parents = [synth.chain_tree(31), synth.random_recursive_tree(rng, 64, 30),
+                   synth.random_recursive_tree(rng, 50, 25), synth.chain_tree(17)]
+        steps.append(_custom(parents, 20 + s, 64, 30, all_match=True))
+    for p in steps:
+        acc = oracle.accept(p.trees.cu_nodes, p.trees.parent, p.trees.n_max, p.trees.depth_max,
+                            p.draft_ids, p.target_ids)
+        assert acc["accept_len"][0] == 31  # the whole chain is accepted
+    check_decode(steps, steps[0].S0)
 
 
 def test_trees_above_64_nodes_run_two_passes():
