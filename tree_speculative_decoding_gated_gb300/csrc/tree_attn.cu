@@ -26,9 +26,10 @@
 // runs while the softmax warps form P for tile u; P goes to TMEM over its own
 // score columns (two score buffers) and is the A operand of O += P V straight
 // from TMEM, issued once every softmax warp has arrived on the tile's "P ready"
-// barrier.  Key and value tiles are double-buffered with separate barriers: a
-// key buffer is refilled once its score product is done (two tiles ahead), a
-// value buffer once its P V product is done.  The tile is 128 keys wide because
+// barrier.  Key tiles have three buffers and value tiles two, with separate
+// barriers: a key buffer is refilled once its score product is done (three tiles
+// ahead: with two, the key copy was the chain that set the pace), a value buffer
+// once its P V product is done.  The tile is 128 keys wide because
 // the SM issues tcgen05.mma instructions at a bounded rate: a 128-key score
 // product is 8 instructions of N = 128, where two 64-key tiles took 16 of N = 64.
 //
@@ -58,9 +59,10 @@ constexpr int kAtMaxNodes = 128;         // tree nodes per sequence on this kern
 constexpr uint32_t kAtTmemCols = 512;    // S / P buffers: cols 0-127, 256-383; O: cols 128-255
 constexpr int kAtTileBytes = kAtKeys * 128;  // one d half (or atom) of a key or value tile
 constexpr int kAtOffQ = 0;               // [2 d halves][128 rows][128 B]      32 KiB
-constexpr int kAtOffK = 32768;           // 2 x [2 d halves][128 keys][128 B]  2 x 32 KiB
-constexpr int kAtOffV = 98304;           // 2 x [2 d atoms][128 keys][128 B]   2 x 32 KiB
-constexpr int kAtOffMask = 163840;       // [kAtMaxNodes][2] uint64           2 KiB
+constexpr int kAtKStages = 3;            // key tiles in flight (value tiles: 2)
+constexpr int kAtOffK = 32768;           // 3 x [2 d halves][128 keys][128 B]  3 x 32 KiB
+constexpr int kAtOffV = kAtOffK + kAtKStages * 32768;  // 2 x [2 d atoms][128 keys][128 B]
+constexpr int kAtOffMask = kAtOffV + 2 * 32768;  // [kAtMaxNodes][2] uint64      2 KiB
 constexpr int kAtOffStat = kAtOffMask + kAtMaxNodes * 16;  // [2 tiles][2][128] row max, [2][128] sum
 constexpr int kAtOffBar = kAtOffStat + 6 * kAtRows * 4;
 constexpr int kAtSmemBytes = kAtOffBar + 128 + 1024;
@@ -93,8 +95,8 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(at_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* amask = reinterpret_cast<uint64_t*>(smem + kAtOffMask);
-  uint64_t* kbar = reinterpret_cast<uint64_t*>(smem + kAtOffBar);  // [2] key tile (+ Q)
-  uint64_t* vbar = kbar + 2;     // [2] value tile
+  uint64_t* kbar = reinterpret_cast<uint64_t*>(smem + kAtOffBar);  // [3] key tile (+ Q)
+  uint64_t* vbar = kbar + kAtKStages;  // [2] value tile
   uint64_t* sbar = vbar + 2;     // [2] score product of tile u (buffer u & 1)
   uint64_t* pvbar = sbar + 2;    // [2] P V product of tile u
   uint64_t* pready = pvbar + 2;  // [2] P of tile u in TMEM: one arrival per softmax warp
@@ -126,8 +128,8 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   const int P = max(0, min(a.prefix_len[b], a.P_max));
 
   if (tid == 0) {
+    for (int i = 0; i < kAtKStages; ++i) mbar_init(&kbar[i], 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&kbar[i], 1);
       mbar_init(&vbar[i], 1);
       mbar_init(&sbar[i], 1);
       mbar_init(&pvbar[i], 1);
@@ -180,7 +182,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   // TMEM buffer u & 1.  Lane 0 of the issuing warp issues every copy and product;
   // each barrier of a pair serves every other tile, so no waiter can be a whole
   // phase behind.
-  int k_issued[2] = {0, 0}, v_issued[2] = {0, 0};   // copies issued per buffer
+  int k_issued[kAtKStages] = {0, 0, 0}, v_issued[2] = {0, 0};  // copies issued per buffer
   int s_issued[2] = {0, 0}, pv_issued[2] = {0, 0};  // products issued per barrier
   auto tile_row = [&](int u, const CUtensorMap*& km, const CUtensorMap*& vm) {
     const int t = tile_of(u);
@@ -189,19 +191,19 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
     vm = pre ? &vcmap : &vtmap;
     return pre ? b * a.P_max + t * kAtKeys : lo + (t - nt_pre) * kAtKeys;
   };
-  auto issue_k = [&](int u) {  // key tile u (with Q for u = 0) into key buffer u & 1
+  auto issue_k = [&](int u) {  // key tile u (with Q for u = 0) into key buffer u % 3
     const CUtensorMap *km, *vm;
     const int r = tile_row(u, km, vm);
-    uint64_t* bar = &kbar[u & 1];
+    uint64_t* bar = &kbar[u % kAtKStages];
     mbar_arrive_expect_tx(bar, 2 * kAtKeys * 128 + (u == 0 ? 32768 : 0));
     if (u == 0) {
       tma_load_3d(smem + kAtOffQ, &qmap, bar, 0, hk * a.G, lo + node0);
       tma_load_3d(smem + kAtOffQ + 16384, &qmap, bar, 64, hk * a.G, lo + node0);
     }
-    uint8_t* kdst = smem + kAtOffK + (u & 1) * (2 * kAtTileBytes);
+    uint8_t* kdst = smem + kAtOffK + (u % kAtKStages) * (2 * kAtTileBytes);
     tma_load_3d(kdst, km, bar, 0, hk, r);
     tma_load_3d(kdst + kAtTileBytes, km, bar, 64, hk, r);
-    k_issued[u & 1] += 1;
+    k_issued[u % kAtKStages] += 1;
   };
   auto issue_v = [&](int u) {  // value tile u into value buffer u & 1
     const CUtensorMap *km, *vm;
@@ -215,10 +217,10 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   };
   // S = Q K^T of tile u into score buffer u & 1 (once its key tile has landed)
   auto score = [&](int u) -> bool {
-    if (!mbar_wait_suspend(&kbar[u & 1], (u >> 1) & 1, abort)) return false;
+    if (!mbar_wait_suspend(&kbar[u % kAtKStages], (u / kAtKStages) & 1, abort)) return false;
     tc_fence_after_sync();
     const uint32_t sQ = smem_addr(smem + kAtOffQ);
-    const uint32_t sK = smem_addr(smem + kAtOffK + (u & 1) * (2 * kAtTileBytes));
+    const uint32_t sK = smem_addr(smem + kAtOffK + (u % kAtKStages) * (2 * kAtTileBytes));
     constexpr uint32_t id_s = idesc_bf16_f32(128, kAtKeys, 0, 0);
 #pragma unroll
     for (int s = 0; s < kAtD / 16; ++s) {
@@ -270,8 +272,10 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   const float gap_raw = kRescaleGap / a.scale;
   float lsum = 0.f;     // this thread's half of the row's sum of exp(logit - m)
   if (warp == kAtCopyWarp) {
-    // ---- the copy warp: key tile u + 2 into key buffer u & 1 once S(u) is done,
-    // value tile u + 2 into value buffer u & 1 once P V of tile u is done
+    // ---- the copy warp: key tile u + 3 into key buffer u % 3 once S(u) is done,
+    // value tile u + 2 into value buffer u & 1 once P V of tile u is done (a key tile
+    // is requested three tiles ahead: its copy, not the products, was the chain that
+    // set the pace with two key buffers)
     if (lane == 0 && nt > 0) {
       issue_k(0);
       issue_v(0);
@@ -279,10 +283,11 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
         issue_k(1);
         issue_v(1);
       }
+      if (nt > 2) issue_k(2);
       for (int u = 0; ok && u + 2 < nt; ++u) {
         const uint32_t ph = (u >> 1) & 1;
         ok = mbar_wait_suspend(&sbar[u & 1], ph, abort);
-        if (ok) issue_k(u + 2);
+        if (ok && u + 3 < nt) issue_k(u + 3);
         if (ok) ok = mbar_wait_suspend(&pvbar[u & 1], ph, abort);
         if (ok) issue_v(u + 2);
       }
@@ -417,8 +422,9 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
     if (!ok && lane == 0) {
       // an expired wait: report it, and let the latest copies and products land (bounded)
       atomicCAS(&a.status[b], TGDN_SEQ_OK, TGDN_SEQ_TIMEOUT);
-      for (int bf = 0; bf < 2; ++bf) {
+      for (int bf = 0; bf < kAtKStages; ++bf)
         if (k_issued[bf] > 0) (void)mbar_wait(&kbar[bf], (k_issued[bf] - 1) & 1);
+      for (int bf = 0; bf < 2; ++bf) {
         if (v_issued[bf] > 0) (void)mbar_wait(&vbar[bf], (v_issued[bf] - 1) & 1);
         if (s_issued[bf] > 0) (void)mbar_wait(&sbar[bf], (s_issued[bf] - 1) & 1);
         if (pv_issued[bf] > 0) (void)mbar_wait(&pvbar[bf], (pv_issued[bf] - 1) & 1);
