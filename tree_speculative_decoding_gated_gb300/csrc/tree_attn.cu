@@ -109,23 +109,25 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   const int hk = (item / a.mtiles) % a.H_kv;
   const int b = item / (a.mtiles * a.H_kv);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int lo = a.cu[b], N = a.cu[b + 1] - lo;
+  // the sequence's bounds, status and context length in one round trip
+  const int c0 = a.cu[b], c1 = a.cu[b + 1], st_b = a.status[b], pl_b = a.prefix_len[b];
+  const int lo = c0, N = c1 - c0;
   const int npt = kAtRows / a.G;             // nodes per tile of query rows
   const int node0 = mt * npt;
   if (N <= 0 || node0 >= N) return;          // no rows of this tile exist
-  if (a.status[b] == TGDN_SEQ_BAD_RANGE) return;  // rows outside the arrays: untouched
+  if (st_b == TGDN_SEQ_BAD_RANGE) return;  // rows outside the arrays: untouched
   const int row = tid & (kAtRows - 1), kh = tid >> 7;  // TMEM lane; key / column half
   const int my_node = node0 + row / a.G, my_g = row % a.G;
   const bool row_live = my_node < N;
   __nv_bfloat16* orow =
       a.o + ((size_t)(lo + my_node) * a.H_q + hk * a.G + my_g) * kAtD;
-  if (a.status[b] != TGDN_SEQ_OK || N > kAtMaxNodes || N > a.n_max) {
+  if (st_b != TGDN_SEQ_OK || N > kAtMaxNodes || N > a.n_max) {
     if (row_live && tid < kAtThreads)
       for (int c = kh * 8; c < kh * 8 + 8; ++c)
         reinterpret_cast<uint4*>(orow)[c] = make_uint4(0, 0, 0, 0);
     return;
   }
-  const int P = max(0, min(a.prefix_len[b], a.P_max));
+  const int P = max(0, min(pl_b, a.P_max));
 
   if (tid == 0) {
     for (int i = 0; i < kAtKStages; ++i) mbar_init(&kbar[i], 1);
@@ -138,35 +140,6 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
     fence_mbar_init();
     *s_abort = 0;
   }
-  // ancestor-or-self sets in node-index space (bit s of word s / 64)
-  if (tid < N) {
-    uint64_t m0 = 0, m1 = 0;
-    const int p = a.pos[lo + tid];
-    if (p >= 0 && p < N) {
-      for (int w = 0; w < a.words && w < 2; ++w) {
-        uint64_t bits = a.anc[(size_t)(lo + p) * a.words + w];
-        while (bits) {
-          const int bp = w * 64 + __ffsll(static_cast<long long>(bits)) - 1;
-          bits &= bits - 1;
-          const int s = bp < N ? a.order[lo + bp] : -1;
-          if (s >= 0 && s < 64) m0 |= 1ull << s;
-          else if (s >= 64 && s < 128) m1 |= 1ull << (s - 64);
-        }
-      }
-    }
-    amask[2 * tid] = m0;
-    amask[2 * tid + 1] = m1;
-  }
-  if (warp == 0) tmem_alloc(tmem_slot, kAtTmemCols);
-  tc_fence_before_sync();
-  __syncthreads();
-  tc_fence_after_sync();
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t tO = tmem + 128;
-  auto tS_of = [&](int u) -> uint32_t { return tmem + ((u & 1) ? 256u : 0u); };
-  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-  volatile int* abort = s_abort;
-
   const int nt_pre = (P + kAtKeys - 1) / kAtKeys;
   const int nt_tree = (N + kAtKeys - 1) / kAtKeys;
   // this CTA's key tiles: context tiles [t_begin, t_end), then (last split) the tree's
@@ -175,13 +148,10 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   const int n_ctx = t_end - t_begin;
   const int nt = n_ctx + (sp == a.splits - 1 ? nt_tree : 0);  // steps of this CTA
   auto tile_of = [&](int u) { return u < n_ctx ? t_begin + u : nt_pre + (u - n_ctx); };
-  const uint64_t m_lo = row_live ? amask[2 * my_node] : 0;
-  const uint64_t m_hi = row_live ? amask[2 * my_node + 1] : 0;
 
-  // Steps u = 0 .. nt - 1: key and value tile u in buffer u & 1, scores and P in
-  // TMEM buffer u & 1.  Lane 0 of the issuing warp issues every copy and product;
-  // each barrier of a pair serves every other tile, so no waiter can be a whole
-  // phase behind.
+  // Steps u = 0 .. nt - 1: key tile u in buffer u % 3, value tile u in buffer u & 1,
+  // scores and P in TMEM buffer u & 1.  Lane 0 of the copy warp issues every copy and
+  // lane 0 of the product warp every product; no waiter can be a whole phase behind.
   int k_issued[kAtKStages] = {0, 0, 0}, v_issued[2] = {0, 0};  // copies issued per buffer
   int s_issued[2] = {0, 0}, pv_issued[2] = {0, 0};  // products issued per barrier
   auto tile_row = [&](int u, const CUtensorMap*& km, const CUtensorMap*& vm) {
@@ -215,6 +185,65 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
     tma_load_3d(vdst + kAtTileBytes, vm, bar, 64, hk, r);
     v_issued[u & 1] += 1;
   };
+
+  // ancestor-or-self sets in node-index space (bit s of word s / 64).  The topological
+  // order goes to shared memory first (one coalesced load), so that the bit loop does
+  // not wait a global-memory round trip per ancestor.
+  int* sord = reinterpret_cast<int*>(smem + kAtOffStat);  // free until the first tile
+  int p_anc = -1, ord_v = -1;
+  if (tid < N) {
+    ord_v = a.order[lo + tid];
+    p_anc = a.pos[lo + tid];
+  }
+  if (warp == 0) tmem_alloc(tmem_slot, kAtTmemCols);
+  __syncthreads();
+  // the first key and value tiles (and Q) go out while the masks are built
+  if (warp == kAtCopyWarp && lane == 0 && nt > 0) {
+    issue_k(0);
+    issue_v(0);
+    if (nt > 1) {
+      issue_k(1);
+      issue_v(1);
+    }
+    if (nt > 2) issue_k(2);
+  }
+  uint64_t wb[2] = {0ull, 0ull};
+  if (tid < N) {
+    if (p_anc >= 0 && p_anc < N)
+      for (int w = 0; w < a.words && w < 2; ++w) wb[w] = a.anc[(size_t)(lo + p_anc) * a.words + w];
+    sord[tid] = ord_v;
+  }
+  __syncthreads();
+  if (tid < N) {
+    uint64_t m0 = 0, m1 = 0;
+    const int p = p_anc;
+    if (p >= 0 && p < N) {
+#pragma unroll
+      for (int w = 0; w < 2; ++w) {
+        uint64_t bits = wb[w];
+        while (bits) {
+          const int bp = w * 64 + __ffsll(static_cast<long long>(bits)) - 1;
+          bits &= bits - 1;
+          const int s = bp < N ? sord[bp] : -1;
+          if (s >= 0 && s < 64) m0 |= 1ull << s;
+          else if (s >= 64 && s < 128) m1 |= 1ull << (s - 64);
+        }
+      }
+    }
+    amask[2 * tid] = m0;
+    amask[2 * tid + 1] = m1;
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tO = tmem + 128;
+  auto tS_of = [&](int u) -> uint32_t { return tmem + ((u & 1) ? 256u : 0u); };
+  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  volatile int* abort = s_abort;
+
+  const uint64_t m_lo = row_live ? amask[2 * my_node] : 0;
+  const uint64_t m_hi = row_live ? amask[2 * my_node + 1] : 0;
   // S = Q K^T of tile u into score buffer u & 1 (once its key tile has landed)
   auto score = [&](int u) -> bool {
     if (!mbar_wait_suspend(&kbar[u % kAtKStages], (u / kAtKStages) & 1, abort)) return false;
@@ -277,13 +306,6 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
     // is requested three tiles ahead: its copy, not the products, was the chain that
     // set the pace with two key buffers)
     if (lane == 0 && nt > 0) {
-      issue_k(0);
-      issue_v(0);
-      if (nt > 1) {
-        issue_k(1);
-        issue_v(1);
-      }
-      if (nt > 2) issue_k(2);
       for (int u = 0; ok && u + 2 < nt; ++u) {
         const uint32_t ph = (u >> 1) & 1;
         ok = mbar_wait_suspend(&sbar[u & 1], ph, abort);
