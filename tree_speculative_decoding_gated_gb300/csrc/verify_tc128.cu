@@ -62,6 +62,7 @@ struct T8Meta {
   // Mixed launches: the sequences above 64 nodes in order (items are numbered over them,
   // so that no CTA steps over the 64-node kernel's items).
   int n_big;
+  float g_root;  // the folded root's gate, for the path gates written at the end of an item
   int16_t big_seq[2048];
 };
 constexpr int kT8MaxList = 2048;
@@ -289,7 +290,9 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
         float* kr = part + 16 * kT8D;
         float* qr = kr + kT8D;
         float* ur = qr + kT8D;
-        const float ar = __expf(g[obase0]), br = bta[obase0];
+        const float gr = g[obase0];
+        const float ar = __expf(gr), br = bta[obase0];
+        if (tid == 0) M.g_root = gr;
         if (tid < kT8D) {
           kr[tid] = __bfloat162float(k[((size_t)lo * H_qk + qh) * kT8D + tid]);
           qr[tid] = __bfloat162float(q[((size_t)lo * H_qk + qh) * kT8D + tid]);
@@ -334,7 +337,7 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
           float acc = 0.f;
           for (int i = 0; i < 16; ++i) acc += part[i * kT8D + tid];
           o[obase0 * kT8D + tid] = __float2bfloat16_rn(acc);
-          if (tid == 0) Gws[obase0] = g[obase0];
+          if (tid == 0) Gws[obase0] = gr;
         }
       }
 #pragma unroll
@@ -563,7 +566,7 @@ verify_tc128_kernel(const __grid_constant__ CUtensorMap qmap,
                               pack2(w[c8 * 8 + 4], w[c8 * 8 + 5]),
                               pack2(w[c8 * 8 + 6], w[c8 * 8 + 7]));
         if (cg == 0)  // stored from the root down (the folded root's gate included)
-          Gws[obase + (size_t)my_row * H_v] = M.G[my_row] + (fold ? g[obase0] : 0.f);
+          Gws[obase + (size_t)my_row * H_v] = M.G[my_row] + (fold ? M.g_root : 0.f);
       }
     }
     tc_fence_before_sync();
