@@ -189,11 +189,17 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
   // ancestor-or-self sets in node-index space (bit s of word s / 64).  The topological
   // order goes to shared memory first (one coalesced load), so that the bit loop does
   // not wait a global-memory round trip per ancestor.
+  // The topological order and the ancestor masks of every position go to shared memory
+  // first (one round trip, issued before the first tiles' copies), so that no load waits
+  // behind those copies and the bit loop waits no round trip per ancestor.
   int* sord = reinterpret_cast<int*>(smem + kAtOffStat);  // free until the first tile
+  uint64_t* sanc = reinterpret_cast<uint64_t*>(smem + kAtOffStat + kAtMaxNodes * 4);  // [pos][2]
   int p_anc = -1, ord_v = -1;
+  uint64_t anc_v[2] = {0ull, 0ull};
   if (tid < N) {
     ord_v = a.order[lo + tid];
     p_anc = a.pos[lo + tid];
+    for (int w = 0; w < a.words && w < 2; ++w) anc_v[w] = a.anc[(size_t)(lo + tid) * a.words + w];
   }
   if (warp == 0) tmem_alloc(tmem_slot, kAtTmemCols);
   __syncthreads();
@@ -207,11 +213,10 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
     }
     if (nt > 2) issue_k(2);
   }
-  uint64_t wb[2] = {0ull, 0ull};
   if (tid < N) {
-    if (p_anc >= 0 && p_anc < N)
-      for (int w = 0; w < a.words && w < 2; ++w) wb[w] = a.anc[(size_t)(lo + p_anc) * a.words + w];
     sord[tid] = ord_v;
+    sanc[2 * tid] = anc_v[0];
+    sanc[2 * tid + 1] = anc_v[1];
   }
   __syncthreads();
   if (tid < N) {
@@ -220,7 +225,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap qmap,
     if (p >= 0 && p < N) {
 #pragma unroll
       for (int w = 0; w < 2; ++w) {
-        uint64_t bits = wb[w];
+        uint64_t bits = sanc[2 * p + w];
         while (bits) {
           const int bp = w * 64 + __ffsll(static_cast<long long>(bits)) - 1;
           bits &= bits - 1;
