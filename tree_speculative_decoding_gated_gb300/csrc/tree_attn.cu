@@ -65,7 +65,12 @@ constexpr int kAtOffV = kAtOffK + kAtKStages * 32768;  // 2 x [2 d atoms][128 ke
 constexpr int kAtOffMask = kAtOffV + 2 * 32768;  // [kAtMaxNodes][2] uint64      2 KiB
 constexpr int kAtOffStat = kAtOffMask + kAtMaxNodes * 16;  // [2 tiles][2][128] row max, [2][128] sum
 constexpr int kAtOffBar = kAtOffStat + 6 * kAtRows * 4;
+// (before the first tile the statistics area holds the copies of the topological order
+// and of every position's ancestor masks that the mask build reads)
+static_assert(kAtMaxNodes * 4 + kAtMaxNodes * 2 * 8 <= 6 * kAtRows * 4,
+              "order and mask copies fit the statistics area");
 constexpr int kAtSmemBytes = kAtOffBar + 128 + 1024;
+static_assert(kAtSmemBytes <= 227 * 1024, "fits one CTA per SM");
 
 __device__ __forceinline__ int at_swz(int row, int chunk) {
   return (row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4);
